@@ -1,0 +1,403 @@
+"""Benchmark of one Muon/NorMuon optimizer step on the GPT-2-124M body.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  The step is the whole hot path -- momentum,
+Nesterov, normalisation, five Newton-Schulz iterations, NorMuon, write-back --
+on seeded synthetic gradients (a bank of 4 gradient sets cycled through,
+inputs larger than L2).  ``value`` is device time per step (CUDA graph of
+``muon_step``, CUDA events, max over ranks); ``e2e`` is the same step through
+the public Python API with the step's gradients copied in from pinned host
+memory and the updated parameters copied back, inside the timed region.
+Per-kernel times come from a second pass of K steps with per-stage CUDA
+events.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of
+the same workload instead.  With torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (no data-path collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon/NorMuon step ms on GPT-2-124M body; NS TFLOP/s & % of bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------- work model
+
+def work_model(wl, grad_bytes):
+    """Algorithmic flops / bytes of one step of workload ``wl``."""
+    ns = wl.ns_steps
+    gram = poly = upd = 0
+    elems = 0
+    for (r, c) in wl.sub_shapes():
+        m, n = min(r, c), max(r, c)
+        gram += m * (m + 1) * n          # upper triangle of X X^T (incl. diagonal)
+        poly += m * m * (m + 1)          # upper triangle of A A
+        upd += 2 * m * m * n             # P X
+        elems += r * c
+    return {
+        "elems": elems,
+        "gram_flops": gram, "poly_flops": poly, "update_flops": upd,
+        "ns_flops": ns * (gram + poly + upd),
+        "ns_flops_dense": ns * sum(4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3 for r, c in wl.sub_shapes()),
+        "momentum_bytes": elems * (grad_bytes + 4 + 4 + 4 + 2),   # g, buf r/w, u fp32 + bf16
+        "apply_bytes": elems * (2 + 4 + 4),                        # O bf16, p r/w
+    }
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def oracle_sample_time(wl, layers=1, repeats=1, seed_step=0):
+    """fp64 oracle on the first ``layers`` layers' matrices, scaled to the whole workload."""
+    import numpy as np
+
+    import oracle
+    from workloads import grads_for, params_for
+
+    per_layer = 3
+    nl = max(1, len(wl.matrices) // per_layer)
+    idx = list(range(min(len(wl.matrices), layers * per_layer)))
+    shapes = [(wl.matrices[i].rows, wl.matrices[i].cols, wl.matrices[i].split, wl.matrices[i].lr_mul,
+               wl.matrices[i].wd_mul) for i in idx]
+    params = [p.double().numpy() for p in params_for(wl, idx)]
+    grads = [g.double().numpy() for g in grads_for(wl, seed_step, indices=idx)]
+    cfg = oracle.OracleConfig(lr=wl.lr, momentum=wl.momentum, beta2=wl.beta2, ns_steps=wl.ns_steps,
+                              normuon=wl.normuon)
+    times = []
+    for _ in range(repeats):
+        orc = oracle.MuonOracle(shapes, cfg)
+        t0 = time.perf_counter()
+        orc.step(params, grads)
+        times.append(time.perf_counter() - t0)
+    scale = nl / layers
+    return min(times) * 1e3 * scale, f"{layers} of {nl} layers ({len(idx)} of {len(wl.matrices)} parameters), " \
+                                     f"one step, fp64 numpy, scaled x{scale:g}"
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import workload
+
+    wl = workload(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample_time(wl, layers=1)
+    vals = []
+    sample = ""
+    for k in range(args.steps):
+        ms, sample = oracle_sample_time(wl, layers=1, seed_step=k % 4)
+        vals.append(ms)
+    v = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description},
+        "cpu_baseline": {"value": v, "unit": "ms", "cores": cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from optimizer_nesterov_momentum_gb300 import MatrixSpec, Muon
+    from workloads import grads_for, params_for, workload
+
+    wl = workload(args.workload)
+    nbank = 4
+    specs = [MatrixSpec(m.rows, m.cols, m.split, m.lr_mul, m.wd_mul) for m in wl.matrices]
+    params = [p.to(dev) for p in params_for(wl)]
+    bank = [[g.to(dev) for g in grads_for(wl, k, device=str(dev))] for k in range(nbank)]
+    grad_bytes = 2 if wl.grad_dtype == "bf16" else 4
+    opt = Muon(specs, lr=wl.lr, momentum=wl.momentum, beta2=wl.beta2, weight_decay=wl.weight_decay,
+               ns_steps=wl.ns_steps, normuon=wl.normuon, grad_dtype=wl.grad_dtype)
+    launches = opt.launch_count()
+    model = work_model(wl, grad_bytes)
+
+    # warm-up (eager), then capture one graph per gradient set, then reset state
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 3)):
+            opt.step(params, bank[k % nbank])
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for k in range(nbank):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            opt.step(params, bank[k])
+        graphs.append(g)
+    opt.reset()
+    for k in range(max(args.warmup, 3)):
+        graphs[k % nbank].replay()
+    opt.sync_status()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- timed region: graph replays
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record()
+        for k in range(args.steps):
+            graphs[k % nbank].replay()
+        end.record()
+        torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps)
+    clocks = clk.summary()
+    opt.sync_status()
+
+    # ---- eager step timing (same work, launched through the API each step)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(args.steps):
+        opt.step(params, bank[k % nbank])
+    end.record()
+    torch.cuda.synchronize()
+    eager_ms = max_over_ranks(start.elapsed_time(end) / args.steps)
+
+    # ---- per-stage times: second pass with CUDA events around every launch
+    opt.set_profiling(True)
+    acc = None
+    for k in range(args.steps):
+        opt.step(params, bank[k % nbank])
+        st = opt.stage_times()
+        acc = st if acc is None else {kk: acc[kk] + st[kk] for kk in acc}
+    opt.set_profiling(False)
+    stage_ms = {kk: v / args.steps for kk, v in acc.items()}
+
+    # ---- end to end through the public API with host buffers
+    host_grads = [[g.cpu().pin_memory() for g in gs] for gs in bank]
+    host_params = [torch.empty_like(p, device="cpu").pin_memory() for p in params]
+    h2d = sum(g.numel() * g.element_size() for g in host_grads[0])
+    d2h = sum(p.numel() * p.element_size() for p in params)
+    dev_grads = [torch.empty_like(g) for g in bank[0]]
+    torch.cuda.synchronize()
+    barrier()
+    start.record()
+    for k in range(args.steps):
+        for dst, src in zip(dev_grads, host_grads[k % nbank]):
+            dst.copy_(src, non_blocking=True)
+        opt.step(params, dev_grads)
+        for dst, src in zip(host_params, params):
+            dst.copy_(src, non_blocking=True)
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(start.elapsed_time(end) / args.steps)
+    opt.sync_status()
+
+    # ---- roofline of each stage
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    nsi = wl.ns_steps
+    kern = {}
+    kern["momentum"] = {"ms": stage_ms["momentum"], "bound": "hbm",
+                        "achieved": model["momentum_bytes"] / (stage_ms["momentum"] * 1e-3) / 1e9, "unit": "GB/s",
+                        "algorithmic_per_launch": model["momentum_bytes"]}
+    kern["apply"] = {"ms": stage_ms["apply"], "bound": "hbm",
+                     "achieved": model["apply_bytes"] / (stage_ms["apply"] * 1e-3) / 1e9, "unit": "GB/s",
+                     "algorithmic_per_launch": model["apply_bytes"]}
+    for name in ("gram", "poly", "update"):
+        per_launch_ms = stage_ms[name] / nsi
+        flops = model[f"{name}_flops"]
+        kern[name] = {"ms": stage_ms[name], "ms_per_launch": per_launch_ms, "bound": "tensor",
+                      "achieved": flops / (per_launch_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "algorithmic_per_launch": flops}
+    for name in ("norm_scale", "lane_stats"):
+        kern[name] = {"ms": stage_ms[name]}
+    for k, v in kern.items():
+        if "achieved" in v:
+            v["peak"] = hbm if v["unit"] == "GB/s" else tc_peak
+            v["frac"] = v["achieved"] / v["peak"]
+    ns_ms = stage_ms["gram"] + stage_ms["poly"] + stage_ms["update"]
+    ns_tflops = model["ns_flops"] / (ns_ms * 1e-3) / 1e12
+    total_stage = sum(stage_ms.values())
+    dom = max(("momentum", "apply", "gram", "poly", "update"), key=lambda k: kern[k]["ms"])
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            traffic = json.load(f).get(wl.name, {}).get(dom)
+    d = kern[dom]
+    roofline = {"bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"],
+                "frac": d["frac"], "traffic": traffic, "kernel": dom,
+                "peak_source": f"{peak_src} ({'hbm_gbs' if d['unit'] == 'GB/s' else 'bf16_tflops_sustained'})",
+                "share_of_step": d["ms"] / total_stage}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample = oracle_sample_time(wl, layers=args.cpu_layers)
+        cpu = {"value": v, "unit": "ms", "cores": cores(), "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "description": wl.description, "matrices": len(wl.sub_shapes()),
+                       "elements": model["elems"], "ns_steps": nsi, "grad_dtype": wl.grad_dtype,
+                       "launch": "cuda graph of muon_step", "l2": "inputs larger than L2 (grads+params+momentum "
+                       f"{(model['elems'] * (grad_bytes + 8)) / 1e6:.0f} MB > 129 MB)",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "ns": {"tflops_algorithmic": ns_tflops, "frac_of_bf16_peak": ns_tflops / tc_peak,
+                   "tflops_dense_equivalent": model["ns_flops_dense"] / (ns_ms * 1e-3) / 1e12,
+                   "ms": ns_ms, "peak_tflops": tc_peak, "peak_source": peak_src},
+            "eager_ms_per_step": eager_ms,
+            "kernels": kern,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    opt.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="gpt2-124m")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-layers", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

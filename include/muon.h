@@ -1,0 +1,203 @@
+/*
+ * muon.h -- C ABI of the GB300 (sm_103a) Muon / NorMuon optimizer step.
+ *
+ * One call, muon_step(), applies one optimizer step to a list of 2-D fp32
+ * parameter matrices given their gradients:
+ *
+ *   S1  momentum        buf <- lerp(buf, g, 1 - mu)            (or buf <- mu*buf + g)
+ *   S2  Nesterov        u   <- lerp(g, buf, mu)                (or u <- g + mu*buf; or u <- buf)
+ *   S3  split + orient  a bank [R, C] with split = k is viewed as k matrices
+ *                       [R, C/k]; each matrix is worked on in its wide
+ *                       orientation (transposed when R > C)
+ *   S4  normalise       X0 = u / (||u||_F + 1e-7)
+ *   S5-S7 Newton-Schulz ns_steps times: A = X X^T; P = b A + c A A; X <- a X + P X
+ *   S8  second moment   r_i = mean_j O_ij^2 over the long side; v <- lerp(v, r, 1 - beta2)
+ *   S9  lane scale      O'_ij = O_ij / sqrt(max(v_i, 1e-10)), rescaled to ||O||_F
+ *   S10 write-back      p <- p * (1 - lr*lr_mul*wd*wd_mul) - lr*lr_mul*O'
+ *                       (plain Muon: no S8/S9, update scaled by lr*lr_mul*max(1, R/C)^0.5)
+ *
+ * Sources (web pages on the modded-nanogpt speedrun):
+ *   - "modded-nanogpt 50B-token 长时程训练实验解析：Muon vs Adam 与数据复用策略的实证对比",
+ *     section "从源码看 Muon 的分布式正交化实现" (Muon from the source): S1 (mul/add form),
+ *     S2, S3 (transpose to the short side), S4, S5-S7 (coefficients (3.4445, -4.7750,
+ *     2.0315), bf16 iteration), S10 (max(1, rows/cols)^0.5, p.add_(g, alpha=-lr));
+ *     section "优化器三件套": Muon(lr=0.02, momentum=0.95), Nesterov on by default.
+ *   - the 2025-10-27 FixMuonLR record write-up: S1 lerp form and reset() (change 2,
+ *     momentum buffer moved to the group), S3 bank view as 4 matrices (change 2,
+ *     attention reshape), S8/S9 NorMuon second_momentum_buffer (background; change 2),
+ *     per-matrix lr_mul / wd_mul with c_fc.lr_mul = 2.0 (change 1).
+ *
+ * Threading and streams.  A handle may be used from one host thread at a time.
+ * Every call that takes a stream only enqueues work on it (no host
+ * synchronisation, no allocation) unless stated otherwise.  Streams are passed
+ * as `void*` holding a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Errors.  Functions return MUON_OK (0) or a negative muon_status.  The text
+ * of the last error of a handle is available from muon_last_error(); errors
+ * raised before a handle exists go to muon_last_error(NULL).  Errors detected
+ * on the device (a bounded wait that gave up) are recorded in a device status
+ * word and reported by muon_sync_status().
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct muon_s* muon_handle;
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_ERR_ARG = -1,         /* invalid argument (NULL pointer, bad count, bad enum, ...) */
+    MUON_ERR_ALIGN = -2,       /* a parameter / gradient pointer is not 16-byte aligned */
+    MUON_ERR_SHAPE = -3,       /* unsupported or inconsistent shape */
+    MUON_ERR_CUDA = -4,        /* a CUDA runtime / driver call failed (text in muon_last_error) */
+    MUON_ERR_TIMEOUT = -5,     /* a kernel's bounded wait gave up (device status word) */
+    MUON_ERR_DESTROYED = -6,   /* the handle was destroyed */
+    MUON_ERR_NOMEM = -7,       /* device allocation failed in muon_create */
+    MUON_ERR_UNSUPPORTED = -8  /* the current device is not an sm_103 GPU */
+} muon_status;
+
+typedef enum { MUON_GRAD_BF16 = 0, MUON_GRAD_F32 = 1 } muon_grad_dtype;
+
+/* muon_shape.flags */
+#define MUON_SPLIT_CONTIGUOUS 0  /* bank split = view of contiguous [R, C] as [split, R, C/split] */
+#define MUON_SPLIT_COLUMNS 1     /* bank split = column blocks [:, q*C/split : (q+1)*C/split] */
+
+/* Newton-Schulz gemm engine (muon_config.gemm_engine) */
+#define MUON_GEMM_TCGEN05 0      /* tcgen05 / TMEM / TMA grouped kernels (the product path) */
+#define MUON_GEMM_SIMT 1         /* plain CUDA-core kernels; a slow debugging cross-check */
+
+#define MUON_MAX_MATRICES 1024   /* parameter matrices per handle */
+#define MUON_MAX_NS_STEPS 16
+
+/* One parameter matrix as the caller stores it: row-major fp32 params and
+ * row-major gradients (bf16 or fp32, see muon_config.grad_dtype) of shape
+ * rows x cols with row stride ld elements (ld = 0 means ld = cols).  With
+ * split > 1 the matrix is a bank viewed as `split` matrices (flags select how);
+ * a contiguous split needs ld == cols. */
+typedef struct {
+    int64_t rows;
+    int64_t cols;
+    int64_t ld;
+    int32_t split;
+    int32_t flags;
+} muon_shape;
+
+typedef struct {
+    float lr;              /* base learning rate (device scalar; see muon_set_hparams) */
+    float momentum;        /* mu (device scalar) */
+    float beta2;           /* NorMuon second-moment decay (device scalar) */
+    float weight_decay;    /* decoupled weight decay (device scalar) */
+    int32_t ns_steps;      /* Newton-Schulz iterations, 1..MUON_MAX_NS_STEPS */
+    int32_t nesterov;      /* 1: Nesterov direction (default) */
+    int32_t lerp_form;     /* 1: buf.lerp_(g, 1-mu) (default); 0: buf = mu*buf + g */
+    int32_t normuon;       /* 1: NorMuon lane scaling (S8/S9); 0: plain Muon */
+    int32_t norm_preserve; /* 1: rescale O' to ||O||_F (default) */
+    int32_t grad_dtype;    /* muon_grad_dtype */
+    int32_t gemm_engine;   /* MUON_GEMM_TCGEN05 (default) or MUON_GEMM_SIMT */
+    const float* lr_mul;   /* host array [n_mats] or NULL (all 1.0); copied at create */
+    const float* wd_mul;   /* host array [n_mats] or NULL (all 1.0); copied at create */
+    const float* ns_coeffs;/* host array [ns_steps * 3] of (a, b, c) per iteration, or NULL
+                              for (3.4445, -4.7750, 2.0315) every iteration; copied */
+} muon_config;
+
+/* Fills *cfg with: lr 0.02, momentum 0.95, beta2 0.95, weight_decay 0, ns_steps 5,
+ * nesterov 1, lerp_form 1, normuon 1, norm_preserve 1, grad_dtype BF16,
+ * gemm_engine TCGEN05, NULL arrays. */
+void muon_config_default(muon_config* cfg);
+
+/* Builds the execution plan for `n_mats` matrices on CUDA device `device`:
+ * validates shapes, groups the (split) matrices by their wide shape, allocates
+ * and zeroes all optimizer state (momentum: fp32, one per parameter; second
+ * moment: fp32, one per lane) and the Newton-Schulz workspace, and encodes the
+ * TMA descriptors.  This is the only call that allocates device memory.
+ * Synchronous.  On success *out owns everything until muon_destroy. */
+int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg,
+                int32_t device, muon_handle* out);
+
+/* One optimizer step.  params[i] (fp32, device, updated in place) and grads[i]
+ * (device, read only) follow shapes[i] of muon_create; both 16-byte aligned.
+ * The pointer arrays themselves are host arrays read during the call.
+ * Enqueues all work on `stream`: no allocation, no host synchronisation, so it
+ * can be captured in a CUDA graph (a captured graph keeps the pointers it was
+ * captured with).  The caller keeps the buffers alive until the work is done. */
+int muon_step(muon_handle h, float* const* params, const void* const* grads, void* stream);
+
+/* Zeroes the momentum and second-moment buffers on `stream` (the reset() the
+ * FixMuonLR record adds to clear state dirtied by warm-up / graph capture). */
+int muon_reset(muon_handle h, void* stream);
+
+/* Sets the device-resident scalars read by later steps (stream-ordered, so a
+ * captured step graph follows schedule updates made between replays). */
+int muon_set_hparams(muon_handle h, float lr, float momentum, float beta2,
+                     float weight_decay, void* stream);
+
+/* Synchronises `stream`, reads and clears the device status word.
+ * Returns MUON_OK, MUON_ERR_TIMEOUT, or MUON_ERR_CUDA. */
+int muon_sync_status(muon_handle h, void* stream);
+
+/* Releases all device memory of the handle.  Synchronises the device. */
+int muon_destroy(muon_handle h);
+
+const char* muon_error_string(int code);
+const char* muon_last_error(muon_handle h);
+
+/* ---- introspection and state access (checkpointing, tests) -------------- */
+
+/* Number of matrices after bank splits. */
+int muon_num_matrices(muon_handle h, int32_t* out);
+
+/* Describes split matrix `index`: out[0] = parent parameter index, out[1] =
+ * split index, out[2] = rows, out[3] = cols (as stored), out[4] = 1 if it is
+ * worked on transposed, out[5] = m = min(rows, cols), out[6] = n = max(rows, cols). */
+int muon_matrix_info(muon_handle h, int32_t index, int64_t out[7]);
+
+/* Bytes of device memory owned by the handle. */
+int muon_workspace_bytes(muon_handle h, int64_t* out);
+
+/* Number of kernel launches one muon_step enqueues. */
+int muon_launch_count(muon_handle h, int32_t* out);
+
+/* ---- stage timing (benchmarks) -------------------------------------------- */
+
+/* Stages of one step, in launch order. */
+#define MUON_STAGE_MOMENTUM 0    /* S1-S3 + norm partials (k_momentum) */
+#define MUON_STAGE_NORM 1        /* S4 scale per matrix (k_norm_scale) */
+#define MUON_STAGE_GRAM 2        /* S5, all iterations summed */
+#define MUON_STAGE_POLY 3        /* S6, all iterations summed */
+#define MUON_STAGE_UPDATE 4      /* S7, all iterations summed */
+#define MUON_STAGE_LANE 5        /* S8 + S9 factors (k_lane_stats) */
+#define MUON_STAGE_APPLY 6       /* S10 (k_apply) */
+#define MUON_NUM_STAGES 7
+
+/* enable != 0: every later muon_step records CUDA events around each launch
+ * on its stream (creates the events on first use; no device allocation). */
+int muon_set_profiling(muon_handle h, int32_t enable);
+
+/* Per-stage device time (ms) of the most recent profiled step, summed over
+ * that stage's launches: out[MUON_NUM_STAGES].  Waits for the step's events. */
+int muon_get_stage_times(muon_handle h, float* out);
+
+#define MUON_STATE_MOMENTUM 0      /* per parameter i: fp32 rows x cols, row-major, dense */
+#define MUON_STATE_SECOND_MOMENT 1 /* per split matrix: fp32 [m] */
+#define MUON_STATE_ORTHO 2         /* per split matrix: last Newton-Schulz output O, wide
+                                      orientation m x n, dense, raw bf16 (2 bytes each) */
+#define MUON_STATE_DIRECTION 3     /* per split matrix: last Nesterov direction u, wide
+                                      orientation m x n, fp32 */
+
+/* Copies one state array into `dst` (host or device memory; cudaMemcpyDefault)
+ * on `stream`.  Layouts as listed above. */
+int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void* stream);
+
+/* Overwrites one state array (MOMENTUM or SECOND_MOMENT) from `src`. */
+int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

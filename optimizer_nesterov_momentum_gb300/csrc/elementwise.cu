@@ -1,0 +1,343 @@
+// Elementwise stages of the step (HBM-bound; 128-bit accesses, 64 x 64 tiles).
+//
+//   k_momentum    S1 + S2 + S3 + S4 partials: momentum buffer update (lerp form
+//                 of the FixMuonLR record, or the mul/add form of the
+//                 "modded-nanogpt 50B-token" write-up), Nesterov direction u,
+//                 u written in the wide orientation (through shared memory for
+//                 tall matrices) as fp32 and bf16, per-tile partial sums of u^2
+//   k_norm_scale  S4: s = 1 / (||u||_F + 1e-7) per matrix (fixed-order reduction)
+//   k_lane_stats  S8 + S9 factors: r_i from the update epilogue's row sums,
+//                 v <- lerp(v, r, 1 - beta2), q_i = 1/sqrt(max(v_i, 1e-10)),
+//                 norm-preserving gamma, lane factor lr * lr_mul * gamma * q_i
+//                 (plain Muon: lr * lr_mul * max(1, R/C)^0.5)
+//   k_apply       S10: p <- p * (1 - lr*lr_mul*wd*wd_mul) - lane_factor * O,
+//                 O read in the wide orientation and written back in the
+//                 caller's orientation
+// Reductions are two-stage with a fixed order, so results are reproducible.
+#include "muon_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace muon {
+
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (w == 0) {
+        t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (l == 0) red[0] = t;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+template <bool GRAD_F32>
+__device__ __forceinline__ void load_grad8(const void* base, int64_t off, float (&g)[8]) {
+    if (GRAD_F32) {
+        const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+        const float4 a = s[0], b = s[1];
+        g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+        g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+    } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            g[2 * h] = __uint_as_float(ws[h] << 16);
+            g[2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+        }
+    }
+}
+
+template <bool GRAD_F32>
+__device__ __forceinline__ float load_grad1(const void* base, int64_t off) {
+    if (GRAD_F32) return static_cast<const float*>(base)[off];
+    return bf2f(static_cast<const uint16_t*>(base)[off]);
+}
+
+__device__ __forceinline__ void store8_f32(float* dst, const float (&v)[8]) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+__device__ __forceinline__ void load8_f32(const float* src, float (&v)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(src)[0];
+    const float4 b = reinterpret_cast<const float4*>(src)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void store8_bf16(uint16_t* dst, const float (&v)[8]) {
+    uint4 w;
+    w.x = pack_bf2(v[0], v[1]);
+    w.y = pack_bf2(v[2], v[3]);
+    w.z = pack_bf2(v[4], v[5]);
+    w.w = pack_bf2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(dst) = w;
+}
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* src, float (&v)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        v[2 * h] = __uint_as_float(ws[h] << 16);
+        v[2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+    }
+}
+
+// momentum and Nesterov direction of one element
+__device__ __forceinline__ float momentum_elem(float g, float& b, float mu, int lerp_form, int nesterov) {
+    if (lerp_form) {
+        b = fmaf(1.f - mu, g - b, b);          // buf.lerp_(g, 1 - mu)
+        return nesterov ? fmaf(mu, b - g, g)   // lerp(g, buf, mu)
+                        : b;
+    }
+    b = fmaf(mu, b, g);                        // buf.mul_(mu).add_(g)
+    return nesterov ? fmaf(mu, b, g) : b;      // g + mu * buf
+}
+
+template <int CAP, bool GRAD_F32>
+__global__ void __launch_bounds__(256) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
+    __shared__ float su[kTile][kTile + 1];
+    __shared__ float red[8];
+    const int4 tile = p.tiles[blockIdx.x];
+    const SubDesc d = p.subs[tile.x];
+    const int r0 = tile.y, c0 = tile.z;
+    const float mu = p.hp[HP_MU];
+    const int tr = threadIdx.x >> 3, tc = threadIdx.x & 7;
+    const void* gbase = p.ptr.grad[d.parent];
+    float sumsq = 0.f;
+
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int rl = pass * 32 + tr, cl = tc * 8;
+        const int r = r0 + rl, c = c0 + cl;
+        float u[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[e] = 0.f;
+        if (r < d.rows && c < d.cols) {
+            const int64_t goff = d.grad_off + (int64_t)r * d.ld + c;
+            float* bptr = d.mom + (int64_t)r * d.ld_mom + c;
+            if (d.vec) {
+                float g[8], b[8];
+                load_grad8<GRAD_F32>(gbase, goff, g);
+                load8_f32(bptr, b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) u[e] = momentum_elem(g[e], b[e], mu, p.lerp_form, p.nesterov);
+                store8_f32(bptr, b);
+            } else {
+                for (int e = 0; e < 8 && c + e < d.cols; ++e) {
+                    float b = bptr[e];
+                    u[e] = momentum_elem(load_grad1<GRAD_F32>(gbase, goff + e), b, mu, p.lerp_form, p.nesterov);
+                    bptr[e] = b;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sumsq = fmaf(u[e], u[e], sumsq);
+            if (!d.transposed) {
+                const int64_t xo = (int64_t)r * d.ldx + c;
+                if (d.vec) {
+                    store8_f32(d.u32 + xo, u);
+                    store8_bf16(d.u16 + xo, u);
+                } else {
+                    for (int e = 0; e < 8 && c + e < d.cols; ++e) {
+                        d.u32[xo + e] = u[e];
+                        d.u16[xo + e] = f2bf(u[e]);
+                    }
+                }
+            }
+        }
+        if (d.transposed) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) su[cl + e][rl] = u[e];
+        }
+    }
+
+    if (d.transposed) {
+        __syncthreads();
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int i = pass * 32 + tr;         // wide row (caller column) within the tile
+            const int wr = c0 + i, wc = r0 + tc * 8;
+            if (wr < d.cols && wc < d.rows) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = su[i][tc * 8 + e];
+                const int64_t xo = (int64_t)wr * d.ldx + wc;
+                if (wc + 8 <= d.rows) {
+                    store8_f32(d.u32 + xo, v);
+                    store8_bf16(d.u16 + xo, v);
+                } else {
+                    for (int e = 0; e < 8 && wc + e < d.rows; ++e) {
+                        d.u32[xo + e] = v[e];
+                        d.u16[xo + e] = f2bf(v[e]);
+                    }
+                }
+            }
+        }
+    }
+    const float total = block_sum_256(sumsq, red);
+    if (threadIdx.x == 0) p.norm_part[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(256) k_norm_scale(const __grid_constant__ NormParams p) {
+    __shared__ float red[8];
+    const SubDesc& d = p.subs[blockIdx.x];
+    float s = 0.f;
+    for (int t = threadIdx.x; t < d.k1_ntiles; t += 256) s += p.norm_part[d.k1_tile0 + t];
+    const float total = block_sum_256(s, red);
+    if (threadIdx.x == 0) p.norm_scale[blockIdx.x] = 1.f / (sqrtf(total) + kNormEps);
+}
+
+__global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ LaneParams p) {
+    __shared__ float red[8];
+    const SubDesc& d = p.subs[blockIdx.x];
+    const float eff = p.hp[HP_LR] * d.lr_mul;
+    if (!p.normuon) {
+        const float f = eff * d.shape_scale;
+        for (int i = threadIdx.x; i < d.m; i += 256) d.lane[i] = f;
+        return;
+    }
+    const float beta2 = p.hp[HP_BETA2];
+    const float inv_n = 1.f / (float)d.n;
+    float before = 0.f, after = 0.f;
+    for (int i = threadIdx.x; i < d.m; i += 256) {
+        float rs = 0.f;
+        for (int t = 0; t < d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n + t];
+        const float r = rs * inv_n;
+        const float v0 = d.v[i];
+        const float v1 = fmaf(1.f - beta2, r - v0, v0);  // v.lerp_(r, 1 - beta2)
+        d.v[i] = v1;
+        const float q = 1.f / sqrtf(fmaxf(v1, kVFloor));
+        d.lane[i] = q;
+        before += rs;
+        after = fmaf(rs, q * q, after);
+    }
+    const float sb = block_sum_256(before, red);
+    const float sa = block_sum_256(after, red);
+    const float gamma = p.norm_preserve ? sqrtf(sb) / fmaxf(sqrtf(sa), kVFloor) : 1.f;
+    const float f = eff * gamma;
+    for (int i = threadIdx.x; i < d.m; i += 256) d.lane[i] *= f;
+}
+
+template <int CAP>
+__global__ void __launch_bounds__(256) k_apply(const __grid_constant__ ElemParams<CAP> p) {
+    __shared__ float so[kTile][kTile + 1];
+    const int4 tile = p.tiles[blockIdx.x];
+    const SubDesc d = p.subs[tile.x];
+    const int r0 = tile.y, c0 = tile.z;
+    const int tr = threadIdx.x >> 3, tc = threadIdx.x & 7;
+    const float decay = 1.f - p.hp[HP_LR] * d.lr_mul * p.hp[HP_WD] * d.wd_mul;
+    float* P = p.ptr.param[d.parent] + d.grad_off;
+
+    if (d.transposed) {
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int i = pass * 32 + tr;
+            const int wr = c0 + i, wc = r0 + tc * 8;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+            if (wr < d.cols && wc < d.rows) {
+                const uint16_t* src = d.o16 + (int64_t)wr * d.ldx + wc;
+                if (wc + 8 <= d.rows)
+                    load8_bf16(src, v);
+                else
+                    for (int e = 0; e < 8 && wc + e < d.rows; ++e) v[e] = bf2f(src[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) so[i][tc * 8 + e] = v[e];
+        }
+        __syncthreads();
+    }
+
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int rl = pass * 32 + tr, cl = tc * 8;
+        const int r = r0 + rl, c = c0 + cl;
+        if (r >= d.rows || c >= d.cols) continue;
+        float* pp = P + (int64_t)r * d.ld + c;
+        float o[8], f[8];
+        if (d.transposed) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = so[cl + e][rl];
+            for (int e = 0; e < 8; ++e) f[e] = (c + e < d.cols) ? d.lane[c + e] : 0.f;
+        } else {
+            const uint16_t* src = d.o16 + (int64_t)r * d.ldx + c;
+            if (d.vec)
+                load8_bf16(src, o);
+            else
+                for (int e = 0; e < 8; ++e) o[e] = (c + e < d.cols) ? bf2f(src[e]) : 0.f;
+            const float fr = d.lane[r];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = fr;
+        }
+        if (d.vec) {
+            float pv[8];
+            load8_f32(pp, pv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pv[e] = fmaf(-f[e], o[e], pv[e] * decay);
+            store8_f32(pp, pv);
+        } else {
+            for (int e = 0; e < 8 && c + e < d.cols; ++e) pp[e] = fmaf(-f[e], o[e], pp[e] * decay);
+        }
+    }
+}
+
+__global__ void k_set_hparams(float* hp, float lr, float mu, float beta2, float wd) {
+    hp[HP_LR] = lr;
+    hp[HP_MU] = mu;
+    hp[HP_BETA2] = beta2;
+    hp[HP_WD] = wd;
+}
+
+// ------------------------------------------------------------------ launchers
+template <int CAP>
+cudaError_t launch_momentum(const ElemParams<CAP>& p, bool grad_f32, cudaStream_t s) {
+    if (p.ntiles <= 0) return cudaSuccess;
+    if (grad_f32)
+        k_momentum<CAP, true><<<p.ntiles, 256, 0, s>>>(p);
+    else
+        k_momentum<CAP, false><<<p.ntiles, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int CAP>
+cudaError_t launch_apply(const ElemParams<CAP>& p, cudaStream_t s) {
+    if (p.ntiles <= 0) return cudaSuccess;
+    k_apply<CAP><<<p.ntiles, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_scale(const NormParams& p, cudaStream_t s) {
+    if (p.nsubs <= 0) return cudaSuccess;
+    k_norm_scale<<<p.nsubs, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lane_stats(const LaneParams& p, cudaStream_t s) {
+    if (p.nsubs <= 0) return cudaSuccess;
+    k_lane_stats<<<p.nsubs, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_hparams(float* hp, float lr, float mu, float beta2, float wd, cudaStream_t s) {
+    k_set_hparams<<<1, 1, 0, s>>>(hp, lr, mu, beta2, wd);
+    return cudaGetLastError();
+}
+
+#define MUON_INSTANTIATE_CAP(CAP)                                                           \
+    template cudaError_t launch_momentum<CAP>(const ElemParams<CAP>&, bool, cudaStream_t); \
+    template cudaError_t launch_apply<CAP>(const ElemParams<CAP>&, cudaStream_t);
+MUON_INSTANTIATE_CAP(64)
+MUON_INSTANTIATE_CAP(256)
+MUON_INSTANTIATE_CAP(1024)
+
+}  // namespace muon

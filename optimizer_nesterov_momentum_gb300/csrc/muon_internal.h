@@ -1,0 +1,125 @@
+// Internal types shared by the host runtime (muon_runtime.cu) and the kernels.
+//
+// Layout of the device state for one handle:
+//   * momentum arena: one dense fp32 [rows x cols] block per parameter (S1).
+//   * per split matrix ("sub"), in the wide orientation m x n (m <= n):
+//       u32 / u16   Nesterov direction, fp32 and its bf16 copy (S2)
+//       x32 / x16   Newton-Schulz iterate, fp32 master + bf16 tensor-core operand,
+//                   two buffers used in turn (S5-S7)
+//       a16 / p16   A = X X^T and P = b A + c A A, bf16, m x m (S5, S6)
+//       rowsq       per (row, 256-column tile) sums of O^2 from the last iteration (S8)
+//       v           second moment, fp32 [m] (S8)
+//       lane        per-lane update factor lr*lr_mul*gamma/sqrt(v) (S9)
+//   Matrices with the same (m, n) form a group and sit back to back in each
+//   arena, so one 3-D TMA descriptor (n, m, count) covers a whole group.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace muon {
+
+constexpr int kMaxGroupsPerLaunch = 8;
+constexpr int kTile = 64;            // edge of the elementwise tiles (K1 / K5)
+constexpr int kBM = 128;             // Newton-Schulz tile rows (TMEM lanes)
+constexpr int kBK = 64;              // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int kBNSym = 128;          // Gram / polynomial tile columns
+constexpr int kBNUpd = 256;          // update tile columns
+constexpr float kNormEps = 1e-7f;
+constexpr float kVFloor = 1e-10f;
+
+// device hyper-parameter slots (muon_set_hparams)
+enum { HP_LR = 0, HP_MU = 1, HP_BETA2 = 2, HP_WD = 3, HP_COUNT = 4 };
+
+// bits of the device status word
+enum { STATUS_TIMEOUT = 1 };
+
+enum GemmMode { MODE_GRAM = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
+
+struct SubDesc {
+    // caller-side addressing (original orientation, rows x cols)
+    int64_t grad_off;    // element offset of (0, 0) in the parent's grad / param
+    int64_t ld;          // caller row stride (elements)
+    float* mom;          // momentum of this sub, row stride ld_mom
+    int64_t ld_mom;
+    int32_t rows, cols;
+    int32_t parent;
+    int32_t transposed;  // rows > cols: worked on as its transpose
+    int32_t vec;         // 8-wide vector access is legal (cols, ld, offsets multiples of 8)
+    int32_t m, n;        // wide shape
+    int32_t ldx;         // row stride of the wide arenas
+    int32_t ntile_n;     // 256-column tiles per row (rowsq entries per row)
+    int32_t k1_tile0, k1_ntiles;  // range of this sub's elementwise tiles
+    float lr_mul, wd_mul, shape_scale;
+    // wide-orientation arenas of this sub
+    float* u32;
+    uint16_t* u16;
+    const uint16_t* o16;  // final Newton-Schulz output (bf16), m x n, row stride ldx
+    float* rowsq;         // m x ntile_n
+    float* v;             // m
+    float* lane;          // m
+};
+
+// Per-launch pointer table of the caller's buffers (kernel parameter; CAP
+// entries so the parameter block stays small for small models).
+template <int CAP>
+struct PtrTable {
+    const void* grad[CAP];
+    float* param[CAP];
+};
+
+template <int CAP>
+struct ElemParams {
+    PtrTable<CAP> ptr;
+    const SubDesc* subs;
+    const int4* tiles;       // {sub, row0, col0, 0} over the original orientation
+    int32_t ntiles;
+    const float* hp;         // HP_* slots
+    float* norm_part;        // one partial sum of u^2 per tile
+    int32_t nesterov, lerp_form;
+};
+
+struct GemmGroup {
+    int32_t m, n, ldx, lda;
+    int32_t ntile_n;
+    int32_t sub0;            // sub index of the group's first matrix (subs are group-ordered)
+    int64_t x_stride;        // elements between matrices in x / u arenas (m * ldx)
+    int64_t a_stride;        // elements between matrices in a / p arenas (m * lda)
+    const float* x32_in;     // update: fp32 iterate read by the a*X term
+    float* x32_out;          // update: next fp32 iterate (nullptr on the last iteration)
+    uint16_t* x16_out;       // update: next bf16 iterate / final O
+    const uint16_t* a16;     // poly epilogue: A (also simt operand)
+    uint16_t* out16;         // gram: A, poly: P
+    float* rowsq;            // update, last iteration: per-row sums of O^2 (m * ntile_n per matrix)
+    const uint16_t* opl16;   // simt: left operand base (gram: X, poly: A, update: P)
+    const uint16_t* opr16;   // simt: right operand base (gram: X, poly: A, update: X)
+};
+
+struct GemmParams {
+    CUtensorMap map_a[kMaxGroupsPerLaunch];  // left operand (K-major)
+    CUtensorMap map_b[kMaxGroupsPerLaunch];  // right operand of the update (MN-major X)
+    GemmGroup grp[kMaxGroupsPerLaunch];
+    const int4* tiles;       // {group slot, index in group, tile row, tile col}
+    int32_t ntiles;
+    int32_t ngroups;
+    const float* norm_scale; // s per sub (first iteration), else nullptr
+    float ca, cb, cc;        // (a, b, c) of this iteration
+    int32_t first, last, want_rowsq;
+    int* status;
+};
+
+struct LaneParams {
+    const SubDesc* subs;
+    int32_t nsubs;
+    const float* hp;
+    int32_t normuon, norm_preserve;
+};
+
+struct NormParams {
+    const SubDesc* subs;
+    int32_t nsubs;
+    const float* norm_part;
+    float* norm_scale;
+};
+
+}  // namespace muon

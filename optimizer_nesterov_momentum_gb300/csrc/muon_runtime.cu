@@ -1,0 +1,884 @@
+// Host runtime behind include/muon.h: validates shapes, builds the execution
+// plan (matrix groups, tile work lists, arenas, TMA descriptors) once at
+// muon_create, and replays a fixed launch sequence on every muon_step:
+//
+//   k_momentum -> k_norm_scale -> ns_steps x (gram -> poly -> update) -> k_lane_stats -> k_apply
+//
+// muon_step allocates nothing and never synchronises the host, so a caller
+// can capture it in a CUDA graph.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "muon_internal.h"
+
+namespace muon {
+// kernels (elementwise.cu, ns_gemm_tc.cu, ns_gemm_simt.cu)
+template <int CAP>
+cudaError_t launch_momentum(const ElemParams<CAP>&, bool, cudaStream_t);
+template <int CAP>
+cudaError_t launch_apply(const ElemParams<CAP>&, cudaStream_t);
+cudaError_t launch_norm_scale(const NormParams&, cudaStream_t);
+cudaError_t launch_lane_stats(const LaneParams&, cudaStream_t);
+cudaError_t launch_set_hparams(float*, float, float, float, float, cudaStream_t);
+cudaError_t ns_gemm_tc_configure();
+template <int MODE>
+cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
+template <int MODE>
+cudaError_t launch_ns_gemm_simt(const GemmParams&, int, int, cudaStream_t);
+}  // namespace muon
+
+using namespace muon;
+
+namespace {
+
+constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
+
+thread_local std::string g_create_error;
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct Group {
+    int32_t m = 0, n = 0;
+    int32_t count = 0;
+    int32_t ldx = 0, lda = 0, ntile_n = 0;
+    int32_t sub0 = 0;
+    // device arenas (count matrices back to back)
+    float* u32 = nullptr;
+    uint16_t* u16 = nullptr;
+    float* x32[2] = {nullptr, nullptr};
+    uint16_t* x16[2] = {nullptr, nullptr};
+    uint16_t* a16 = nullptr;
+    uint16_t* p16 = nullptr;
+    float* rowsq = nullptr;
+    float* v = nullptr;
+    float* lane = nullptr;
+    // TMA descriptors
+    CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
+};
+
+struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
+    int32_t g0 = 0, ng = 0;
+    int32_t gram_off = 0, gram_n = 0;
+    int32_t poly_off = 0, poly_n = 0;
+    int32_t upd_off = 0, upd_n = 0;
+};
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+struct muon_s {
+    bool alive = true;
+    int device = 0;
+    int num_sms = 0;
+    muon_config cfg{};
+    std::vector<float> coeffs;          // ns_steps * 3
+    std::vector<muon_shape> shapes;
+    std::vector<float> lr_mul, wd_mul;
+    std::vector<SubDesc> subs;          // group-ordered
+    std::vector<int32_t> sub_parent_q;  // split index of each sub
+    std::vector<Group> groups;
+    std::vector<Chunk> chunks;
+    std::vector<int64_t> mom_off;       // per parent, offset into momentum arena (floats)
+    int32_t n_elem_tiles = 0;
+    // device memory
+    void* arena = nullptr;
+    size_t arena_bytes = 0;
+    float* hp = nullptr;
+    int* status = nullptr;
+    float* norm_scale = nullptr;
+    float* norm_part = nullptr;
+    float* momentum = nullptr;
+    SubDesc* d_subs = nullptr;
+    int4* d_elem_tiles = nullptr;
+    int4* d_gemm_tiles = nullptr;
+    // pre-built GEMM parameter blocks: [iteration][chunk][mode]
+    std::vector<GemmParams> gparams;
+    std::string last_error;
+    // profiling: one event before every launch plus one at the end
+    bool profiling = false;
+    std::vector<cudaEvent_t> events;
+    std::vector<int> event_stage;  // stage of the launch that follows event k
+    int n_recorded = 0;
+};
+
+namespace {
+
+std::mutex g_handles_mu;
+std::set<muon_s*> g_handles;
+
+int fail(muon_s* h, int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    if (h)
+        h->last_error = buf;
+    else
+        g_create_error = buf;
+    return code;
+}
+
+int check_handle(muon_s* h) {
+    if (h == nullptr) return fail(nullptr, MUON_ERR_ARG, "null handle");
+    std::lock_guard<std::mutex> lk(g_handles_mu);
+    if (g_handles.find(h) == g_handles.end()) return fail(nullptr, MUON_ERR_ARG, "unknown handle");
+    if (!h->alive) return fail(h, MUON_ERR_DESTROYED, "handle was destroyed");
+    return MUON_OK;
+}
+
+#define MUON_CUDA(h, call)                                                                              \
+    do {                                                                                               \
+        cudaError_t e_ = (call);                                                                       \
+        if (e_ != cudaSuccess) return fail((h), MUON_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+    } while (0)
+
+PFN_encodeTiled get_encode_fn() {
+    static PFN_encodeTiled fn = nullptr;
+    if (fn) return fn;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    fn = reinterpret_cast<PFN_encodeTiled>(p);
+    return fn;
+}
+
+// 3-D bf16 tensor map over `count` matrices of rows x cols, row stride ld
+// (elements), 128-byte swizzle, box {64, box_rows, 1}.
+bool encode_bf16_3d(PFN_encodeTiled enc, CUtensorMap* map, void* base, int64_t cols, int64_t rows, int64_t count,
+                    int64_t ld, uint32_t box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(ld * 2 * rows)};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int CAP>
+void fill_ptrs(PtrTable<CAP>& t, float* const* params, const void* const* grads, int n) {
+    for (int i = 0; i < n; ++i) {
+        t.param[i] = params[i];
+        t.grad[i] = grads[i];
+    }
+}
+
+template <int CAP>
+cudaError_t run_elem(muon_s* h, float* const* params, const void* const* grads, bool apply, cudaStream_t s) {
+    ElemParams<CAP> ep;
+    memset(&ep, 0, sizeof(ep));
+    fill_ptrs<CAP>(ep.ptr, params, grads, (int)h->shapes.size());
+    ep.subs = h->d_subs;
+    ep.tiles = h->d_elem_tiles;
+    ep.ntiles = h->n_elem_tiles;
+    ep.hp = h->hp;
+    ep.norm_part = h->norm_part;
+    ep.nesterov = h->cfg.nesterov;
+    ep.lerp_form = h->cfg.lerp_form;
+    if (apply) return launch_apply<CAP>(ep, s);
+    return launch_momentum<CAP>(ep, h->cfg.grad_dtype == MUON_GRAD_F32, s);
+}
+
+cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* grads, bool apply, cudaStream_t s) {
+    const size_t n = h->shapes.size();
+    if (n <= 64) return run_elem<64>(h, params, grads, apply, s);
+    if (n <= 256) return run_elem<256>(h, params, grads, apply, s);
+    return run_elem<1024>(h, params, grads, apply, s);
+}
+
+int launches_per_step(const muon_s* h) {
+    // k_momentum, k_norm_scale, k_lane_stats, k_apply + the Newton-Schulz products
+    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) return 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps;
+    const int per_iter = 3 * (int)h->groups.size();
+    const int rowsq = h->cfg.normuon ? (int)h->groups.size() : 0;  // extra pass after the last update
+    return 4 + per_iter * h->cfg.ns_steps + rowsq;
+}
+
+cudaError_t mark(muon_s* h, int stage, cudaStream_t s) {
+    if (!h->profiling) return cudaSuccess;
+    if (h->n_recorded >= (int)h->events.size()) return cudaErrorInvalidValue;
+    h->event_stage[h->n_recorded] = stage;
+    return cudaEventRecord(h->events[h->n_recorded++], s);
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+extern "C" {
+
+void muon_config_default(muon_config* cfg) {
+    if (!cfg) return;
+    memset(cfg, 0, sizeof(*cfg));
+    cfg->lr = 0.02f;
+    cfg->momentum = 0.95f;
+    cfg->beta2 = 0.95f;
+    cfg->weight_decay = 0.f;
+    cfg->ns_steps = 5;
+    cfg->nesterov = 1;
+    cfg->lerp_form = 1;
+    cfg->normuon = 1;
+    cfg->norm_preserve = 1;
+    cfg->grad_dtype = MUON_GRAD_BF16;
+    cfg->gemm_engine = MUON_GEMM_TCGEN05;
+}
+
+const char* muon_error_string(int code) {
+    switch (code) {
+        case MUON_OK: return "ok";
+        case MUON_ERR_ARG: return "invalid argument";
+        case MUON_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case MUON_ERR_SHAPE: return "unsupported or inconsistent shape";
+        case MUON_ERR_CUDA: return "CUDA error";
+        case MUON_ERR_TIMEOUT: return "device wait timed out";
+        case MUON_ERR_DESTROYED: return "handle destroyed";
+        case MUON_ERR_NOMEM: return "out of device memory";
+        case MUON_ERR_UNSUPPORTED: return "device is not sm_103";
+        default: return "unknown error";
+    }
+}
+
+const char* muon_last_error(muon_handle h) {
+    if (h == nullptr) return g_create_error.c_str();
+    std::lock_guard<std::mutex> lk(g_handles_mu);
+    if (g_handles.find(h) == g_handles.end()) return "unknown handle";
+    return h->last_error.c_str();
+}
+
+int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg_in, int32_t device,
+                muon_handle* out) {
+    g_create_error.clear();
+    if (out == nullptr) return fail(nullptr, MUON_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (shapes == nullptr || n_mats <= 0) return fail(nullptr, MUON_ERR_ARG, "need at least one shape");
+    if (n_mats > MUON_MAX_MATRICES) return fail(nullptr, MUON_ERR_ARG, "too many matrices (max %d)", MUON_MAX_MATRICES);
+    muon_config cfg;
+    if (cfg_in)
+        cfg = *cfg_in;
+    else
+        muon_config_default(&cfg);
+    if (cfg.ns_steps < 1 || cfg.ns_steps > MUON_MAX_NS_STEPS)
+        return fail(nullptr, MUON_ERR_ARG, "ns_steps must be in [1, %d]", MUON_MAX_NS_STEPS);
+    if (cfg.grad_dtype != MUON_GRAD_BF16 && cfg.grad_dtype != MUON_GRAD_F32)
+        return fail(nullptr, MUON_ERR_ARG, "bad grad_dtype");
+    if (cfg.gemm_engine != MUON_GEMM_TCGEN05 && cfg.gemm_engine != MUON_GEMM_SIMT)
+        return fail(nullptr, MUON_ERR_ARG, "bad gemm_engine");
+
+    // ---- shapes -> split matrices (host-only validation first)
+    struct Pending {
+        int parent, q;
+        int64_t rows, cols, ld, off, mom_off_in_parent, ld_mom;
+    };
+    std::vector<Pending> pend;
+    std::vector<int64_t> mom_off(n_mats);
+    int64_t mom_total = 0;
+    for (int i = 0; i < n_mats; ++i) {
+        const muon_shape& s = shapes[i];
+        const int64_t ld = s.ld == 0 ? s.cols : s.ld;
+        const int split = s.split <= 0 ? 1 : s.split;
+        if (s.rows < 1 || s.cols < 1) return fail(nullptr, MUON_ERR_SHAPE, "shape %d: rows and cols must be >= 1", i);
+        if (s.rows > (1 << 20) || s.cols > (1 << 20))
+            return fail(nullptr, MUON_ERR_SHAPE, "shape %d: dimensions above 2^20 are not supported", i);
+        if (ld < s.cols) return fail(nullptr, MUON_ERR_SHAPE, "shape %d: ld < cols", i);
+        if (s.cols % split) return fail(nullptr, MUON_ERR_SHAPE, "shape %d: cols not divisible by split", i);
+        if (s.flags != MUON_SPLIT_CONTIGUOUS && s.flags != MUON_SPLIT_COLUMNS)
+            return fail(nullptr, MUON_ERR_ARG, "shape %d: bad flags", i);
+        if (split > 1 && s.flags == MUON_SPLIT_CONTIGUOUS && ld != s.cols)
+            return fail(nullptr, MUON_ERR_SHAPE, "shape %d: a contiguous split needs ld == cols", i);
+        mom_off[i] = mom_total;
+        mom_total += round_up(s.rows * s.cols, 64);
+        const int64_t cs = s.cols / split;
+        for (int q = 0; q < split; ++q) {
+            Pending p;
+            p.parent = i;
+            p.q = q;
+            p.rows = s.rows;
+            p.cols = cs;
+            if (split == 1) {
+                p.ld = ld;
+                p.off = 0;
+                p.mom_off_in_parent = 0;
+                p.ld_mom = s.cols;
+            } else if (s.flags == MUON_SPLIT_CONTIGUOUS) {
+                p.ld = cs;
+                p.off = (int64_t)q * s.rows * cs;
+                p.mom_off_in_parent = p.off;
+                p.ld_mom = cs;
+            } else {
+                p.ld = ld;
+                p.off = (int64_t)q * cs;
+                p.mom_off_in_parent = (int64_t)q * cs;
+                p.ld_mom = s.cols;
+            }
+            pend.push_back(p);
+        }
+    }
+
+    // ---- device checks
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0)
+        return fail(nullptr, MUON_ERR_CUDA, "no CUDA device");
+    if (device < 0 || device >= ndev) return fail(nullptr, MUON_ERR_ARG, "bad device %d", device);
+    if (cudaSetDevice(device) != cudaSuccess) return fail(nullptr, MUON_ERR_CUDA, "cudaSetDevice failed");
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess)
+        return fail(nullptr, MUON_ERR_CUDA, "cudaGetDeviceProperties failed");
+    if (!(prop.major == 10 && prop.minor == 3))
+        return fail(nullptr, MUON_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                    device, prop.major, prop.minor);
+    PFN_encodeTiled enc = get_encode_fn();
+    if (!enc) return fail(nullptr, MUON_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+
+    muon_s* h = new muon_s();
+    h->device = device;
+    h->num_sms = prop.multiProcessorCount;
+    h->cfg = cfg;
+    h->cfg.lr_mul = h->cfg.wd_mul = h->cfg.ns_coeffs = nullptr;
+    h->shapes.assign(shapes, shapes + n_mats);
+    h->mom_off = mom_off;
+    for (int i = 0; i < n_mats; ++i) {
+        h->lr_mul.push_back(cfg.lr_mul ? cfg.lr_mul[i] : 1.f);
+        h->wd_mul.push_back(cfg.wd_mul ? cfg.wd_mul[i] : 1.f);
+    }
+    for (int it = 0; it < cfg.ns_steps; ++it)
+        for (int k = 0; k < 3; ++k) h->coeffs.push_back(cfg.ns_coeffs ? cfg.ns_coeffs[3 * it + k] : kDefaultCoeffs[k]);
+
+    // ---- groups by wide shape, in order of first appearance
+    std::map<std::pair<int, int>, int> gid;
+    std::vector<int> sub_group(pend.size());
+    for (size_t k = 0; k < pend.size(); ++k) {
+        const int m = (int)std::min(pend[k].rows, pend[k].cols), n = (int)std::max(pend[k].rows, pend[k].cols);
+        auto key = std::make_pair(m, n);
+        auto it = gid.find(key);
+        if (it == gid.end()) {
+            Group g;
+            g.m = m;
+            g.n = n;
+            g.ldx = (int)round_up(n, 8);
+            g.lda = (int)round_up(m, 8);
+            g.ntile_n = (n + kBNUpd - 1) / kBNUpd;
+            it = gid.emplace(key, (int)h->groups.size()).first;
+            h->groups.push_back(g);
+        }
+        sub_group[k] = it->second;
+    }
+    std::vector<size_t> order(pend.size());
+    for (size_t k = 0; k < order.size(); ++k) order[k] = k;
+    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) { return sub_group[a] < sub_group[b]; });
+
+    // ---- arena layout
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += (bytes + 255) / 256 * 256;
+        return o;
+    };
+    const int nsubs = (int)pend.size();
+    const size_t o_hp = take(sizeof(float) * HP_COUNT);
+    const size_t o_status = take(sizeof(int));
+    const size_t o_norm_scale = take(sizeof(float) * nsubs);
+    // elementwise tiles
+    std::vector<int4> elem_tiles;
+    std::vector<int32_t> k1_tile0(nsubs), k1_ntiles(nsubs);
+    for (int sidx = 0; sidx < nsubs; ++sidx) {
+        const Pending& pd = pend[order[sidx]];
+        k1_tile0[sidx] = (int32_t)elem_tiles.size();
+        for (int64_t r0 = 0; r0 < pd.rows; r0 += kTile)
+            for (int64_t c0 = 0; c0 < pd.cols; c0 += kTile) elem_tiles.push_back(make_int4(sidx, (int)r0, (int)c0, 0));
+        k1_ntiles[sidx] = (int32_t)elem_tiles.size() - k1_tile0[sidx];
+    }
+    if (elem_tiles.size() > (size_t)0x7fffffff / 2) {
+        delete h;
+        return fail(nullptr, MUON_ERR_SHAPE, "too many elementwise tiles");
+    }
+    h->n_elem_tiles = (int32_t)elem_tiles.size();
+    const size_t o_norm_part = take(sizeof(float) * elem_tiles.size());
+    const size_t o_mom = take(sizeof(float) * (size_t)mom_total);
+    std::vector<size_t> go_u32, go_u16, go_x32[2], go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane;
+    for (auto& g : h->groups) g.count = 0;
+    for (int sidx = 0; sidx < nsubs; ++sidx) h->groups[sub_group[order[sidx]]].count++;
+    {
+        int s0 = 0;
+        for (auto& g : h->groups) {
+            g.sub0 = s0;
+            s0 += g.count;
+        }
+    }
+    for (auto& g : h->groups) {
+        const size_t xe = (size_t)g.count * g.m * g.ldx, ae = (size_t)g.count * g.m * g.lda;
+        go_u32.push_back(take(xe * 4));
+        go_u16.push_back(take(xe * 2));
+        for (int b = 0; b < 2; ++b) {
+            go_x32[b].push_back(take(xe * 4));
+            go_x16[b].push_back(take(xe * 2));
+        }
+        go_a16.push_back(take(ae * 2));
+        go_p16.push_back(take(ae * 2));
+        go_rowsq.push_back(take((size_t)g.count * g.m * g.ntile_n * 4));
+        go_v.push_back(take((size_t)g.count * g.m * 4));
+        go_lane.push_back(take((size_t)g.count * g.m * 4));
+    }
+    const size_t o_subs = take(sizeof(SubDesc) * nsubs);
+    const size_t o_etiles = take(sizeof(int4) * elem_tiles.size());
+
+    // GEMM tile lists, per chunk of groups
+    std::vector<int4> gemm_tiles;
+    for (int g0 = 0; g0 < (int)h->groups.size(); g0 += kMaxGroupsPerLaunch) {
+        Chunk ch;
+        ch.g0 = g0;
+        ch.ng = std::min<int>(kMaxGroupsPerLaunch, (int)h->groups.size() - g0);
+        struct T {
+            int4 t;
+            int64_t cost;
+        };
+        auto emit = [&](std::vector<T>& v, int32_t& o, int32_t& n) {
+            std::stable_sort(v.begin(), v.end(), [](const T& a, const T& b) { return a.cost > b.cost; });
+            o = (int32_t)gemm_tiles.size();
+            for (auto& x : v) gemm_tiles.push_back(x.t);
+            n = (int32_t)v.size();
+        };
+        std::vector<T> gram, poly, upd;
+        for (int sl = 0; sl < ch.ng; ++sl) {
+            const Group& g = h->groups[g0 + sl];
+            const int tm = (g.m + kBM - 1) / kBM;
+            const int tn = (g.n + kBNUpd - 1) / kBNUpd;
+            for (int idx = 0; idx < g.count; ++idx) {
+                for (int ti = 0; ti < tm; ++ti)
+                    for (int tj = ti; tj < tm; ++tj) {
+                        gram.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
+                        poly.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+                    }
+                for (int ti = 0; ti < tm; ++ti)
+                    for (int tj = 0; tj < tn; ++tj) upd.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+            }
+        }
+        emit(gram, ch.gram_off, ch.gram_n);
+        emit(poly, ch.poly_off, ch.poly_n);
+        emit(upd, ch.upd_off, ch.upd_n);
+        h->chunks.push_back(ch);
+    }
+    const size_t o_gtiles = take(sizeof(int4) * std::max<size_t>(gemm_tiles.size(), 1));
+
+    h->arena_bytes = off;
+    if (cudaMalloc(&h->arena, off) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return fail(nullptr, MUON_ERR_NOMEM, "cudaMalloc of %zu bytes failed", off);
+    }
+    char* base = static_cast<char*>(h->arena);
+    if (cudaMemset(h->arena, 0, off) != cudaSuccess) {
+        cudaFree(h->arena);
+        delete h;
+        return fail(nullptr, MUON_ERR_CUDA, "cudaMemset failed");
+    }
+    h->hp = reinterpret_cast<float*>(base + o_hp);
+    h->status = reinterpret_cast<int*>(base + o_status);
+    h->norm_scale = reinterpret_cast<float*>(base + o_norm_scale);
+    h->norm_part = reinterpret_cast<float*>(base + o_norm_part);
+    h->momentum = reinterpret_cast<float*>(base + o_mom);
+    h->d_subs = reinterpret_cast<SubDesc*>(base + o_subs);
+    h->d_elem_tiles = reinterpret_cast<int4*>(base + o_etiles);
+    h->d_gemm_tiles = reinterpret_cast<int4*>(base + o_gtiles);
+    for (size_t gi = 0; gi < h->groups.size(); ++gi) {
+        Group& g = h->groups[gi];
+        g.u32 = reinterpret_cast<float*>(base + go_u32[gi]);
+        g.u16 = reinterpret_cast<uint16_t*>(base + go_u16[gi]);
+        for (int b = 0; b < 2; ++b) {
+            g.x32[b] = reinterpret_cast<float*>(base + go_x32[b][gi]);
+            g.x16[b] = reinterpret_cast<uint16_t*>(base + go_x16[b][gi]);
+        }
+        g.a16 = reinterpret_cast<uint16_t*>(base + go_a16[gi]);
+        g.p16 = reinterpret_cast<uint16_t*>(base + go_p16[gi]);
+        g.rowsq = reinterpret_cast<float*>(base + go_rowsq[gi]);
+        g.v = reinterpret_cast<float*>(base + go_v[gi]);
+        g.lane = reinterpret_cast<float*>(base + go_lane[gi]);
+        bool ok = encode_bf16_3d(enc, &g.map_u_k, g.u16, g.n, g.m, g.count, g.ldx, kBM) &&
+                  encode_bf16_3d(enc, &g.map_u_mn, g.u16, g.n, g.m, g.count, g.ldx, 64) &&
+                  encode_bf16_3d(enc, &g.map_a_k, g.a16, g.m, g.m, g.count, g.lda, kBM) &&
+                  encode_bf16_3d(enc, &g.map_p_k, g.p16, g.m, g.m, g.count, g.lda, kBM);
+        for (int b = 0; b < 2 && ok; ++b)
+            ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
+                 encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64);
+        if (!ok) {
+            cudaFree(h->arena);
+            delete h;
+            return fail(nullptr, MUON_ERR_CUDA, "cuTensorMapEncodeTiled rejected a descriptor");
+        }
+    }
+
+    // ---- sub descriptors (group order)
+    const int last_buf = (cfg.ns_steps - 1) % 2;
+    std::vector<int> idx_in_group(h->groups.size(), 0);
+    for (int sidx = 0; sidx < nsubs; ++sidx) {
+        const Pending& pd = pend[order[sidx]];
+        Group& g = h->groups[sub_group[order[sidx]]];
+        const int gi = idx_in_group[sub_group[order[sidx]]]++;
+        SubDesc d;
+        memset(&d, 0, sizeof(d));
+        d.grad_off = pd.off;
+        d.ld = pd.ld;
+        d.mom = h->momentum + h->mom_off[pd.parent] + pd.mom_off_in_parent;
+        d.ld_mom = pd.ld_mom;
+        d.rows = (int32_t)pd.rows;
+        d.cols = (int32_t)pd.cols;
+        d.parent = pd.parent;
+        d.transposed = pd.rows > pd.cols ? 1 : 0;
+        d.vec = (pd.cols % 8 == 0 && pd.ld % 8 == 0 && pd.off % 8 == 0 && pd.ld_mom % 8 == 0 &&
+                 (h->mom_off[pd.parent] + pd.mom_off_in_parent) % 8 == 0)
+                    ? 1
+                    : 0;
+        d.m = g.m;
+        d.n = g.n;
+        d.ldx = g.ldx;
+        d.ntile_n = g.ntile_n;
+        d.k1_tile0 = k1_tile0[sidx];
+        d.k1_ntiles = k1_ntiles[sidx];
+        d.lr_mul = h->lr_mul[pd.parent];
+        d.wd_mul = h->wd_mul[pd.parent];
+        d.shape_scale = (float)std::sqrt(std::max(1.0, (double)pd.rows / (double)pd.cols));
+        const int64_t xo = (int64_t)gi * g.m * g.ldx;
+        d.u32 = g.u32 + xo;
+        d.u16 = g.u16 + xo;
+        d.o16 = g.x16[last_buf] + xo;
+        d.rowsq = g.rowsq + (int64_t)gi * g.m * g.ntile_n;
+        d.v = g.v + (int64_t)gi * g.m;
+        d.lane = g.lane + (int64_t)gi * g.m;
+        h->subs.push_back(d);
+        h->sub_parent_q.push_back(pd.q);
+    }
+
+    // ---- upload descriptors and tiles, default hyper-parameters
+    bool ok = cudaMemcpy(h->d_subs, h->subs.data(), sizeof(SubDesc) * nsubs, cudaMemcpyHostToDevice) == cudaSuccess &&
+              cudaMemcpy(h->d_elem_tiles, elem_tiles.data(), sizeof(int4) * elem_tiles.size(),
+                         cudaMemcpyHostToDevice) == cudaSuccess &&
+              (gemm_tiles.empty() || cudaMemcpy(h->d_gemm_tiles, gemm_tiles.data(), sizeof(int4) * gemm_tiles.size(),
+                                                cudaMemcpyHostToDevice) == cudaSuccess);
+    float hpv[HP_COUNT] = {cfg.lr, cfg.momentum, cfg.beta2, cfg.weight_decay};
+    ok = ok && cudaMemcpy(h->hp, hpv, sizeof(hpv), cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && ns_gemm_tc_configure() == cudaSuccess;
+    if (!ok) {
+        cudaFree(h->arena);
+        delete h;
+        return fail(nullptr, MUON_ERR_CUDA, "upload / kernel configuration failed");
+    }
+
+    // ---- GEMM parameter blocks: [iteration][chunk][mode]
+    for (int it = 0; it < cfg.ns_steps; ++it) {
+        const bool first = it == 0, last = it == cfg.ns_steps - 1;
+        const int in_buf = (it - 1) % 2, out_buf = it % 2;
+        for (const Chunk& ch : h->chunks) {
+            for (int mode = 0; mode < 3; ++mode) {
+                GemmParams gp;
+                memset(&gp, 0, sizeof(gp));
+                gp.ngroups = ch.ng;
+                gp.norm_scale = h->norm_scale;
+                gp.ca = h->coeffs[3 * it + 0];
+                gp.cb = h->coeffs[3 * it + 1];
+                gp.cc = h->coeffs[3 * it + 2];
+                gp.first = first;
+                gp.last = last;
+                gp.want_rowsq = last && cfg.normuon;
+                gp.status = h->status;
+                if (mode == MODE_GRAM) {
+                    gp.tiles = h->d_gemm_tiles + ch.gram_off;
+                    gp.ntiles = ch.gram_n;
+                } else if (mode == MODE_POLY) {
+                    gp.tiles = h->d_gemm_tiles + ch.poly_off;
+                    gp.ntiles = ch.poly_n;
+                } else {
+                    gp.tiles = h->d_gemm_tiles + ch.upd_off;
+                    gp.ntiles = ch.upd_n;
+                }
+                for (int sl = 0; sl < ch.ng; ++sl) {
+                    const Group& g = h->groups[ch.g0 + sl];
+                    GemmGroup& G = gp.grp[sl];
+                    G.m = g.m;
+                    G.n = g.n;
+                    G.ldx = g.ldx;
+                    G.lda = g.lda;
+                    G.ntile_n = g.ntile_n;
+                    G.sub0 = g.sub0;
+                    G.x_stride = (int64_t)g.m * g.ldx;
+                    G.a_stride = (int64_t)g.m * g.lda;
+                    const uint16_t* xin16 = first ? g.u16 : g.x16[in_buf];
+                    G.x32_in = first ? g.u32 : g.x32[in_buf];
+                    G.x32_out = last ? nullptr : g.x32[out_buf];
+                    G.x16_out = g.x16[out_buf];
+                    G.a16 = g.a16;
+                    G.rowsq = g.rowsq;
+                    if (mode == MODE_GRAM) {
+                        gp.map_a[sl] = first ? g.map_u_k : g.map_x_k[in_buf];
+                        G.out16 = g.a16;
+                        G.opl16 = xin16;
+                        G.opr16 = xin16;
+                    } else if (mode == MODE_POLY) {
+                        gp.map_a[sl] = g.map_a_k;
+                        G.out16 = g.p16;
+                        G.opl16 = g.a16;
+                        G.opr16 = g.a16;
+                    } else {
+                        gp.map_a[sl] = g.map_p_k;
+                        gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
+                        G.opl16 = g.p16;
+                        G.opr16 = xin16;
+                    }
+                }
+                h->gparams.push_back(gp);
+            }
+        }
+    }
+
+    {
+        std::lock_guard<std::mutex> lk(g_handles_mu);
+        g_handles.insert(h);
+    }
+    *out = h;
+    return MUON_OK;
+}
+
+int muon_step(muon_handle h, float* const* params, const void* const* grads, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (params == nullptr || grads == nullptr) return fail(h, MUON_ERR_ARG, "params / grads array is NULL");
+    const int n = (int)h->shapes.size();
+    for (int i = 0; i < n; ++i) {
+        if (params[i] == nullptr || grads[i] == nullptr) return fail(h, MUON_ERR_ARG, "matrix %d: NULL pointer", i);
+        if ((reinterpret_cast<uintptr_t>(params[i]) | reinterpret_cast<uintptr_t>(grads[i])) & 15u)
+            return fail(h, MUON_ERR_ALIGN, "matrix %d: pointer not 16-byte aligned", i);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    h->n_recorded = 0;
+    MUON_CUDA(h, mark(h, MUON_STAGE_MOMENTUM, s));
+    MUON_CUDA(h, run_elem_any(h, params, grads, false, s));
+    NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale};
+    MUON_CUDA(h, mark(h, MUON_STAGE_NORM, s));
+    MUON_CUDA(h, launch_norm_scale(np, s));
+    const int nch = (int)h->chunks.size();
+    for (int it = 0; it < h->cfg.ns_steps; ++it) {
+        for (int mode = 0; mode < 3; ++mode) {
+            for (int c = 0; c < nch; ++c) {
+                const GemmParams& gp = h->gparams[((size_t)it * nch + c) * 3 + mode];
+                MUON_CUDA(h, mark(h, MUON_STAGE_GRAM + mode, s));
+                if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
+                    if (mode == MODE_GRAM) MUON_CUDA(h, launch_ns_gemm_tc<MODE_GRAM>(gp, h->num_sms, s));
+                    if (mode == MODE_POLY) MUON_CUDA(h, launch_ns_gemm_tc<MODE_POLY>(gp, h->num_sms, s));
+                    if (mode == MODE_UPDATE) MUON_CUDA(h, launch_ns_gemm_tc<MODE_UPDATE>(gp, h->num_sms, s));
+                } else {
+                    for (int sl = 0; sl < gp.ngroups; ++sl) {
+                        const int cnt = h->groups[h->chunks[c].g0 + sl].count;
+                        if (mode == MODE_GRAM) MUON_CUDA(h, launch_ns_gemm_simt<MODE_GRAM>(gp, sl, cnt, s));
+                        if (mode == MODE_POLY) MUON_CUDA(h, launch_ns_gemm_simt<MODE_POLY>(gp, sl, cnt, s));
+                        if (mode == MODE_UPDATE) MUON_CUDA(h, launch_ns_gemm_simt<MODE_UPDATE>(gp, sl, cnt, s));
+                    }
+                }
+            }
+        }
+    }
+    LaneParams lp{h->d_subs, (int32_t)h->subs.size(), h->hp, h->cfg.normuon, h->cfg.norm_preserve};
+    MUON_CUDA(h, mark(h, MUON_STAGE_LANE, s));
+    MUON_CUDA(h, launch_lane_stats(lp, s));
+    MUON_CUDA(h, mark(h, MUON_STAGE_APPLY, s));
+    MUON_CUDA(h, run_elem_any(h, params, grads, true, s));
+    MUON_CUDA(h, mark(h, -1, s));
+    return MUON_OK;
+}
+
+int muon_reset(muon_handle h, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    int64_t mom_floats = 0;
+    for (size_t i = 0; i < h->shapes.size(); ++i) mom_floats += round_up(h->shapes[i].rows * h->shapes[i].cols, 64);
+    MUON_CUDA(h, cudaMemsetAsync(h->momentum, 0, sizeof(float) * (size_t)mom_floats, s));
+    for (const Group& g : h->groups) MUON_CUDA(h, cudaMemsetAsync(g.v, 0, sizeof(float) * (size_t)g.count * g.m, s));
+    return MUON_OK;
+}
+
+int muon_set_hparams(muon_handle h, float lr, float momentum, float beta2, float weight_decay, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    MUON_CUDA(h, launch_set_hparams(h->hp, lr, momentum, beta2, weight_decay, static_cast<cudaStream_t>(stream)));
+    h->cfg.lr = lr;
+    h->cfg.momentum = momentum;
+    h->cfg.beta2 = beta2;
+    h->cfg.weight_decay = weight_decay;
+    return MUON_OK;
+}
+
+int muon_sync_status(muon_handle h, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_CUDA(h, cudaStreamSynchronize(s));
+    int st = 0;
+    MUON_CUDA(h, cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (st != 0) {
+        MUON_CUDA(h, cudaMemset(h->status, 0, sizeof(int)));
+        if (st & STATUS_TIMEOUT) return fail(h, MUON_ERR_TIMEOUT, "a kernel's bounded wait gave up");
+    }
+    return MUON_OK;
+}
+
+int muon_destroy(muon_handle h) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    if (h->arena) cudaFree(h->arena);
+    h->arena = nullptr;
+    for (cudaEvent_t e : h->events) cudaEventDestroy(e);
+    h->events.clear();
+    h->profiling = false;
+    h->alive = false;  // the host object stays as a tombstone so stale handles are recognised
+    h->gparams.clear();
+    h->gparams.shrink_to_fit();
+    return MUON_OK;
+}
+
+int muon_num_matrices(muon_handle h, int32_t* out) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!out) return fail(h, MUON_ERR_ARG, "out is NULL");
+    *out = (int32_t)h->subs.size();
+    return MUON_OK;
+}
+
+int muon_matrix_info(muon_handle h, int32_t index, int64_t out[7]) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!out || index < 0 || index >= (int32_t)h->subs.size()) return fail(h, MUON_ERR_ARG, "bad index");
+    const SubDesc& d = h->subs[index];
+    out[0] = d.parent;
+    out[1] = h->sub_parent_q[index];
+    out[2] = d.rows;
+    out[3] = d.cols;
+    out[4] = d.transposed;
+    out[5] = d.m;
+    out[6] = d.n;
+    return MUON_OK;
+}
+
+int muon_workspace_bytes(muon_handle h, int64_t* out) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!out) return fail(h, MUON_ERR_ARG, "out is NULL");
+    *out = (int64_t)h->arena_bytes;
+    return MUON_OK;
+}
+
+int muon_launch_count(muon_handle h, int32_t* out) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!out) return fail(h, MUON_ERR_ARG, "out is NULL");
+    *out = launches_per_step(h);
+    return MUON_OK;
+}
+
+int muon_set_profiling(muon_handle h, int32_t enable) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    if (enable && h->events.empty()) {
+        const int n = 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps + 1;
+        h->events.resize(n);
+        h->event_stage.assign(n, -1);
+        for (int k = 0; k < n; ++k) MUON_CUDA(h, cudaEventCreate(&h->events[k]));
+    }
+    h->profiling = enable != 0;
+    h->n_recorded = 0;
+    return MUON_OK;
+}
+
+int muon_get_stage_times(muon_handle h, float* out) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!out) return fail(h, MUON_ERR_ARG, "out is NULL");
+    for (int k = 0; k < MUON_NUM_STAGES; ++k) out[k] = 0.f;
+    if (h->n_recorded < 2) return fail(h, MUON_ERR_ARG, "no profiled step recorded");
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    MUON_CUDA(h, cudaEventSynchronize(h->events[h->n_recorded - 1]));
+    for (int k = 0; k + 1 < h->n_recorded; ++k) {
+        float ms = 0.f;
+        MUON_CUDA(h, cudaEventElapsedTime(&ms, h->events[k], h->events[k + 1]));
+        const int st = h->event_stage[k];
+        if (st >= 0 && st < MUON_NUM_STAGES) out[st] += ms;
+    }
+    return MUON_OK;
+}
+
+int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!dst) return fail(h, MUON_ERR_ARG, "dst is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    if (which == MUON_STATE_MOMENTUM) {
+        if (index < 0 || index >= (int32_t)h->shapes.size()) return fail(h, MUON_ERR_ARG, "bad parameter index");
+        const muon_shape& sh = h->shapes[index];
+        MUON_CUDA(h, cudaMemcpyAsync(dst, h->momentum + h->mom_off[index], sizeof(float) * sh.rows * sh.cols,
+                                     cudaMemcpyDefault, s));
+        return MUON_OK;
+    }
+    if (index < 0 || index >= (int32_t)h->subs.size()) return fail(h, MUON_ERR_ARG, "bad matrix index");
+    const SubDesc& d = h->subs[index];
+    if (which == MUON_STATE_SECOND_MOMENT) {
+        MUON_CUDA(h, cudaMemcpyAsync(dst, d.v, sizeof(float) * d.m, cudaMemcpyDefault, s));
+    } else if (which == MUON_STATE_ORTHO) {
+        MUON_CUDA(h, cudaMemcpy2DAsync(dst, sizeof(uint16_t) * d.n, d.o16, sizeof(uint16_t) * d.ldx,
+                                       sizeof(uint16_t) * d.n, d.m, cudaMemcpyDefault, s));
+    } else if (which == MUON_STATE_DIRECTION) {
+        MUON_CUDA(h, cudaMemcpy2DAsync(dst, sizeof(float) * d.n, d.u32, sizeof(float) * d.ldx, sizeof(float) * d.n,
+                                       d.m, cudaMemcpyDefault, s));
+    } else {
+        return fail(h, MUON_ERR_ARG, "bad state selector %d", which);
+    }
+    return MUON_OK;
+}
+
+int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!src) return fail(h, MUON_ERR_ARG, "src is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    if (which == MUON_STATE_MOMENTUM) {
+        if (index < 0 || index >= (int32_t)h->shapes.size()) return fail(h, MUON_ERR_ARG, "bad parameter index");
+        const muon_shape& sh = h->shapes[index];
+        MUON_CUDA(h, cudaMemcpyAsync(h->momentum + h->mom_off[index], src, sizeof(float) * sh.rows * sh.cols,
+                                     cudaMemcpyDefault, s));
+        return MUON_OK;
+    }
+    if (which == MUON_STATE_SECOND_MOMENT) {
+        if (index < 0 || index >= (int32_t)h->subs.size()) return fail(h, MUON_ERR_ARG, "bad matrix index");
+        const SubDesc& d = h->subs[index];
+        MUON_CUDA(h, cudaMemcpyAsync(d.v, src, sizeof(float) * d.m, cudaMemcpyDefault, s));
+        return MUON_OK;
+    }
+    return fail(h, MUON_ERR_ARG, "state %d cannot be written", which);
+}
+
+}  // extern "C"

@@ -26,6 +26,7 @@ from .muon_oracle import (
     orient_wide,
     frobenius_normalise,
     newton_schulz,
+    newton_schulz_closed_form,
     zeropower_via_newtonschulz5,
     normuon_scale,
     shape_scale,
@@ -46,6 +47,7 @@ __all__ = [
     "orient_wide",
     "frobenius_normalise",
     "newton_schulz",
+    "newton_schulz_closed_form",
     "zeropower_via_newtonschulz5",
     "normuon_scale",
     "shape_scale",

@@ -207,6 +207,32 @@ def zeropower_via_newtonschulz5(g: np.ndarray, steps: int = 5, eps: float = NORM
     return x.T.copy() if transposed else x
 
 
+def newton_schulz_closed_form(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarray:
+    """The exact value of ``steps`` quintic iterations on a wide matrix, from the spectrum.
+
+    Every iterate is an odd polynomial of X0, so with X0 = U S V^T the result is
+    ``U f(S) V^T = U diag(f(s)/s) U^T X0`` where f composes the per-iteration
+    maps ``s -> a s + b s^3 + c s^5``.  U and s^2 come from the symmetric
+    eigendecomposition of the Gram matrix X0 X0^T (LAPACK via numpy).  Equal
+    to :func:`newton_schulz` in exact arithmetic; much cheaper for tall
+    matrices (one Gram, one eigendecomposition, one product).
+    """
+    gram = x @ x.T
+    lam, u = np.linalg.eigh(gram)
+    s = np.sqrt(np.maximum(lam, 0.0))
+    g = np.empty_like(s)
+    small = s < 1e-150
+    f = s.copy()
+    for a, b, c in _coeff_list(coeffs, steps):
+        f = a * f + b * f ** 3 + c * f ** 5
+    g[~small] = f[~small] / s[~small]
+    slope = 1.0
+    for a, _b, _c in _coeff_list(coeffs, steps):
+        slope *= a
+    g[small] = slope  # limit of f(s)/s at s -> 0
+    return (u * g[None, :]) @ (u.T @ x)
+
+
 # ---------------------------------------------------------------------------
 # S8 / S9: NorMuon second moment and lane scaling
 # ---------------------------------------------------------------------------
@@ -265,6 +291,7 @@ class OracleConfig:
     eps: float = NORM_EPS
     split_mode: str = "contiguous"
     ns_form: str = "page"
+    ns_impl: str = "iterate"  # or "closed_form" (exact spectral value; large matrices)
     bf16: bool = False
 
 
@@ -282,12 +309,14 @@ class SubRecord:
 class MuonOracle:
     """State (momentum per parameter, second moment per optimizer matrix) + step.
 
-    ``shapes``: list of (rows, cols, split, lr_mul, wd_mul).
+    ``shapes``: list of (rows, cols, split, lr_mul, wd_mul[, split_mode]); the
+    split mode defaults to ``cfg.split_mode``.
     """
 
     def __init__(self, shapes, cfg: OracleConfig):
         self.cfg = cfg
-        self.shapes = [tuple(s) for s in shapes]
+        self.shapes = [tuple(s[:5]) for s in shapes]
+        self.split_modes = [s[5] if len(s) > 5 else cfg.split_mode for s in shapes]
         self.momentum = [np.zeros((r, c)) for (r, c, *_rest) in self.shapes]
         self.v = []
         for (r, c, split, *_rest) in self.shapes:
@@ -312,14 +341,18 @@ class MuonOracle:
             p = np.asarray(params[i], dtype=np.float64)
             self.momentum[i] = momentum_update(self.momentum[i], g, cfg.momentum, cfg.lerp_form)
             u = nesterov_direction(g, self.momentum[i], cfg.momentum, cfg.lerp_form, cfg.nesterov)
-            subs_u = split_matrix(u, split, cfg.split_mode)
-            subs_p = split_matrix(p, split, cfg.split_mode)
+            mode = self.split_modes[i]
+            subs_u = split_matrix(u, split, mode)
+            subs_p = split_matrix(p, split, mode)
             new_subs, recs = [], []
             for q, (su, sp) in enumerate(zip(subs_u, subs_p)):
                 rnd = bf16_round if cfg.bf16 else _id
                 x = frobenius_normalise(rnd(su), cfg.eps, rnd)
                 x, transposed = orient_wide(x)
-                o = newton_schulz(x, cfg.ns_steps, cfg.ns_coeffs, cfg.ns_form, cfg.bf16)
+                if cfg.ns_impl == "closed_form" and not cfg.bf16:
+                    o = newton_schulz_closed_form(x, cfg.ns_steps, cfg.ns_coeffs)
+                else:
+                    o = newton_schulz(x, cfg.ns_steps, cfg.ns_coeffs, cfg.ns_form, cfg.bf16)
                 if cfg.normuon:
                     o_scaled, self.v[i][q] = normuon_scale(o, self.v[i][q], cfg.beta2, cfg.norm_preserve)
                     scale = 1.0
@@ -331,6 +364,6 @@ class MuonOracle:
                 upd = o_scaled.T if transposed else o_scaled
                 new_subs.append(write_back(sp, upd, cfg.lr, lr_mul, cfg.weight_decay, wd_mul, scale))
                 recs.append(SubRecord(su, o, o_scaled, vrec, transposed))
-            out.append(merge_matrix(new_subs, r, c, cfg.split_mode))
+            out.append(merge_matrix(new_subs, r, c, mode))
             self.records.append(recs)
         return out

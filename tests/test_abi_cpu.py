@@ -1,0 +1,131 @@
+"""The C-ABI library on the host: it loads, exports every entry point that
+include/muon.h declares, and rejects bad arguments before any device work.
+No kernel runs here (there is no GPU in the build container)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from optimizer_nesterov_momentum_gb300 import _abi, build
+
+    build.build()
+    return _abi.load_library()
+
+
+def _declared_entry_points():
+    with open(os.path.join(ROOT, "include", "muon.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(muon_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    from optimizer_nesterov_momentum_gb300 import _abi
+
+    assert _declared_entry_points() == sorted(_abi.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_entry_points():
+        assert hasattr(lib, name), name
+
+
+def test_struct_layouts_match_header():
+    from optimizer_nesterov_momentum_gb300 import _abi
+
+    assert ctypes.sizeof(_abi.muon_shape) == 32
+    assert _abi.muon_config.lr_mul.offset == 48
+    assert ctypes.sizeof(_abi.muon_config) == 72
+
+
+def test_config_default(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi
+
+    cfg = _abi.muon_config_default()
+    assert abs(cfg.lr - 0.02) < 1e-9 and abs(cfg.momentum - 0.95) < 1e-7
+    assert cfg.ns_steps == 5 and cfg.nesterov == 1 and cfg.lerp_form == 1 and cfg.normuon == 1
+    assert not cfg.lr_mul and not cfg.ns_coeffs
+
+
+def _create(lib, shapes, cfg=None, n=None, out=True):
+    from optimizer_nesterov_momentum_gb300 import _abi
+
+    arr = (_abi.muon_shape * max(len(shapes), 1))(*shapes)
+    h = ctypes.c_void_p()
+    return lib.muon_create(arr, len(shapes) if n is None else n, ctypes.byref(cfg) if cfg else None, 0,
+                           ctypes.byref(h) if out else None)
+
+
+def test_create_rejects_bad_arguments_on_the_host(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    good = [A.muon_shape(64, 256, 0, 1, 0)]
+    assert _create(lib, good, out=False) == A.MUON_ERR_ARG
+    assert _create(lib, good, n=0) == A.MUON_ERR_ARG
+    assert _create(lib, good, n=A.MUON_MAX_MATRICES + 1) == A.MUON_ERR_ARG
+    cfg = A.muon_config_default()
+    cfg.ns_steps = 0
+    assert _create(lib, good, cfg) == A.MUON_ERR_ARG
+    cfg = A.muon_config_default()
+    cfg.ns_steps = A.MUON_MAX_NS_STEPS + 1
+    assert _create(lib, good, cfg) == A.MUON_ERR_ARG
+    cfg = A.muon_config_default()
+    cfg.grad_dtype = 7
+    assert _create(lib, good, cfg) == A.MUON_ERR_ARG
+    assert _create(lib, [A.muon_shape(0, 256, 0, 1, 0)]) == A.MUON_ERR_SHAPE
+    assert _create(lib, [A.muon_shape(64, 256, 100, 1, 0)]) == A.MUON_ERR_SHAPE      # ld < cols
+    assert _create(lib, [A.muon_shape(64, 250, 0, 4, 0)]) == A.MUON_ERR_SHAPE        # cols % split
+    assert _create(lib, [A.muon_shape(64, 256, 512, 4, 0)]) == A.MUON_ERR_SHAPE      # contiguous split, ld != cols
+    assert _create(lib, [A.muon_shape(64, 256, 0, 1, 9)]) == A.MUON_ERR_ARG          # bad flags
+    assert "split" in lib.muon_last_error(None).decode() or "flags" in lib.muon_last_error(None).decode()
+
+
+def test_create_without_a_device_reports_cuda_error(lib):
+    import torch
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _create(lib, [A.muon_shape(64, 256, 0, 1, 0)]) == A.MUON_ERR_CUDA
+    assert "device" in lib.muon_last_error(None).decode().lower()
+
+
+def test_calls_on_invalid_handles(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    assert lib.muon_step(None, None, None, None) == A.MUON_ERR_ARG
+    assert lib.muon_reset(None, None) == A.MUON_ERR_ARG
+    assert lib.muon_destroy(None) == A.MUON_ERR_ARG
+    bogus = ctypes.c_void_p(0x1234)
+    assert lib.muon_step(bogus, None, None, None) == A.MUON_ERR_ARG
+    assert lib.muon_sync_status(bogus, None) == A.MUON_ERR_ARG
+    n = ctypes.c_int32()
+    assert lib.muon_num_matrices(bogus, ctypes.byref(n)) == A.MUON_ERR_ARG
+
+
+def test_error_strings(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    for code in range(0, -9, -1):
+        assert lib.muon_error_string(code).decode() != "unknown error"
+    assert lib.muon_error_string(-99).decode() == "unknown error"
+    assert A.muon_error_string(A.MUON_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from optimizer_nesterov_momentum_gb300 import _abi
+
+    saved = _abi._lib
+    _abi._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="no CPU or fallback path"):
+            _abi.load_library(str(tmp_path / "absent.so"))
+    finally:
+        _abi._lib = saved

@@ -112,6 +112,18 @@ def test_ns_per_iteration_coefficients_closed_form():
     assert _rel(out, (u * s) @ vt) < 1e-12
 
 
+@pytest.mark.parametrize("m,n", [(16, 40), (24, 24), (8, 200)])
+def test_closed_form_matches_iteration(m, n):
+    rng = np.random.default_rng(m + n)
+    s = np.geomspace(1e-5, 1.0, m)
+    x = _rand_with_spectrum(rng, m, n, s) * 0.5
+    it = oracle.newton_schulz(x, steps=5)
+    cf = oracle.newton_schulz_closed_form(x, steps=5)
+    assert _rel(cf, it) < 1e-9
+    table = [(3.0, -3.2, 1.2), (2.0, -1.5, 0.5)]
+    assert _rel(oracle.newton_schulz_closed_form(x, 2, table), oracle.newton_schulz(x, 2, table)) < 1e-9
+
+
 def test_classic_newton_schulz_converges_to_polar_factor():
     rng = np.random.default_rng(11)
     s = np.linspace(0.05, 1.0, 24)

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every case compares, per step and per matrix (tolerances in parity_util):
+momentum (1e-5), the Newton-Schulz output O (2e-2), the second moment
+stage-wise (1e-5, oracle fed the GPU's O) and end to end (2e-2), the
+parameter update stage-wise (1e-5) and end to end (2e-2).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.parity_util import Shape, TOL_NS, TOL_STATE, make_optimizer, rel, run_parity
+from workloads import grads_for, params_for, workload
+from workloads.generators import _rng, gaussian_params, lowrank_plus_noise
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(shapes, steps, seed, grad_dtype="bf16"):
+    dt = torch.bfloat16 if grad_dtype == "bf16" else torch.float32
+    params = [gaussian_params(_rng(seed + 7777, i), s.rows, s.cols) for i, s in enumerate(shapes)]
+    grads = [[lowrank_plus_noise(_rng(seed + k, i), s.rows, s.cols).to(dt).contiguous()
+              for i, s in enumerate(shapes)] for k in range(steps)]
+    return params, grads
+
+
+def _wl_shapes(wl):
+    return [Shape(m.rows, m.cols, m.split, m.lr_mul, m.wd_mul) for m in wl.matrices]
+
+
+# ----------------------------------------------------------------- named workloads
+
+def test_tiny_plain_muon_fp32_grads():
+    wl = workload("tiny")
+    errs, opt, _ = run_parity(_wl_shapes(wl), params_for(wl), [grads_for(wl, 0)], lr=wl.lr,
+                              normuon=False, grad_dtype="f32")
+    errs.assert_within(normuon=False)
+
+
+def test_gpt2_124m_normuon_full_step():
+    """The timed workload, every matrix, in the launch configuration the benchmark uses."""
+    wl = workload("gpt2-124m")
+    errs, _, _ = run_parity(_wl_shapes(wl), params_for(wl), [grads_for(wl, 0)], lr=wl.lr, normuon=True)
+    errs.assert_within()
+
+
+def test_gpt2_124m_plain_muon():
+    wl = workload("gpt2-124m-plain")
+    sample = [0, 1, 2, 33, 34, 35]
+    errs, _, _ = run_parity(_wl_shapes(wl), params_for(wl), [grads_for(wl, 0)], lr=wl.lr, normuon=False,
+                            check_parents=sample)
+    errs.assert_within(normuon=False)
+
+
+def test_gpt2_medium_sampled():
+    wl = workload("gpt2-medium")
+    sample = [0, 1, 2, 70, 71]
+    grads = [g.cpu() for g in grads_for(wl, 0, device="cuda")]
+    errs, _, _ = run_parity(_wl_shapes(wl), params_for(wl), [grads], lr=wl.lr, check_parents=sample)
+    errs.assert_within()
+
+
+def test_stress_sampled_closed_form():
+    """4096-wide stress set (ill-conditioned spectrum); a square and a tall matrix checked."""
+    wl = workload("stress")
+    sample = [0, 20]
+    grads = [g.cpu() for g in grads_for(wl, 0, device="cuda")]
+    errs, _, _ = run_parity(_wl_shapes(wl), params_for(wl), [grads], lr=wl.lr, check_parents=sample,
+                            ns_impl="closed_form")
+    errs.assert_within()
+
+
+# ----------------------------------------------------------------- shapes and edges
+
+RAGGED = [Shape(96, 200), Shape(200, 96), Shape(130, 300), Shape(8, 40), Shape(33, 70), Shape(70, 33),
+          Shape(256, 1024, split=4, lr_mul=2.0), Shape(300, 520), Shape(1, 17), Shape(5, 5),
+          Shape(64, 512, split=4, split_mode="columns", wd_mul=0.5)]
+
+
+@pytest.mark.parametrize("engine", ["tcgen05", "simt"])
+def test_ragged_shapes_three_steps(engine):
+    params, grads = _inputs(RAGGED, 3, seed=11)
+    errs, _, _ = run_parity(RAGGED, params, grads, lr=0.03, gemm_engine=engine, weight_decay=0.01)
+    errs.assert_within()
+
+
+def test_ragged_shapes_fp32_grads_plain():
+    params, grads = _inputs(RAGGED, 2, seed=12, grad_dtype="f32")
+    errs, _, _ = run_parity(RAGGED, params, grads, lr=0.02, normuon=False, grad_dtype="f32")
+    errs.assert_within(normuon=False)
+
+
+@pytest.mark.parametrize("lerp_form,nesterov", [(False, True), (True, False), (False, False)])
+def test_momentum_variants(lerp_form, nesterov):
+    shapes = [Shape(128, 384), Shape(384, 128)]
+    params, grads = _inputs(shapes, 3, seed=13)
+    errs, _, _ = run_parity(shapes, params, grads, lr=0.03, lerp_form=lerp_form, nesterov=nesterov)
+    errs.assert_within()
+
+
+def test_per_iteration_coefficients_and_step_counts():
+    shapes = [Shape(192, 320), Shape(256, 256)]
+    params, grads = _inputs(shapes, 1, seed=14)
+    table = [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.0, -1.5, 0.5)]
+    errs, _, _ = run_parity(shapes, params, grads, ns_steps=3, ns_coeffs=table)
+    errs.assert_within()
+    errs, _, _ = run_parity(shapes, params, grads, ns_steps=1)
+    errs.assert_within()
+
+
+def test_lr_schedule_through_device_scalars():
+    shapes = [Shape(128, 512), Shape(512, 128)]
+    params, grads = _inputs(shapes, 3, seed=15)
+    errs, _, _ = run_parity(shapes, params, grads, lr=0.03, lr_schedule=[0.03, 0.01, 0.002])
+    errs.assert_within()
+
+
+def test_zero_gradient_keeps_params_and_is_finite():
+    shapes = [Shape(64, 192), Shape(192, 64)]
+    opt = make_optimizer(shapes, lr=0.03)
+    params = [torch.randn(s.rows, s.cols, device="cuda") for s in shapes]
+    before = [p.clone() for p in params]
+    grads = [torch.zeros(s.rows, s.cols, device="cuda", dtype=torch.bfloat16) for s in shapes]
+    opt.step(params, grads)
+    opt.sync_status()
+    for a, b in zip(params, before):
+        assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------- state handling
+
+def test_reset_restores_fresh_state():
+    shapes = [Shape(128, 256), Shape(256, 128, split=2)]
+    params, grads = _inputs(shapes, 2, seed=16)
+    errs, opt, _ = run_parity(shapes, params, grads[:1], lr=0.03)
+    opt.reset()
+    # after reset, a step from the same params must match a fresh optimizer's step
+    fresh = make_optimizer(shapes, lr=0.03)
+    pa = [p.cuda() for p in params]
+    pb = [p.cuda() for p in params]
+    g = [x.cuda() for x in grads[1]]
+    opt.step(pa, g)
+    fresh.step(pb, g)
+    torch.cuda.synchronize()
+    for a, b in zip(pa, pb):
+        assert torch.equal(a, b)
+
+
+def test_runs_are_bitwise_reproducible():
+    shapes = [Shape(256, 768), Shape(768, 256), Shape(128, 512, split=4)]
+    params, grads = _inputs(shapes, 1, seed=17)
+    outs = []
+    for _ in range(2):
+        opt = make_optimizer(shapes, lr=0.03)
+        p = [x.cuda() for x in params]
+        opt.step(p, [x.cuda() for x in grads[0]])
+        torch.cuda.synchronize()
+        outs.append([x.cpu() for x in p])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+def test_state_roundtrip_checkpoint():
+    from optimizer_nesterov_momentum_gb300 import MUON_STATE_MOMENTUM, MUON_STATE_SECOND_MOMENT
+
+    shapes = [Shape(128, 256), Shape(64, 256, split=2)]
+    params, grads = _inputs(shapes, 2, seed=18)
+    _, opt, p_gpu = run_parity(shapes, params, grads[:1], lr=0.03)
+    saved_m = [opt.get_state(MUON_STATE_MOMENTUM, i).clone() for i in range(len(shapes))]
+    saved_v = [opt.get_state(MUON_STATE_SECOND_MOMENT, k).clone() for k in range(opt.num_matrices())]
+    other = make_optimizer(shapes, lr=0.03)
+    for i, t in enumerate(saved_m):
+        other.set_state(MUON_STATE_MOMENTUM, i, t)
+    for k, t in enumerate(saved_v):
+        other.set_state(MUON_STATE_SECOND_MOMENT, k, t)
+    pa = [p.clone() for p in p_gpu]
+    pb = [p.clone() for p in p_gpu]
+    g = [x.cuda() for x in grads[1]]
+    opt.step(pa, g)
+    other.step(pb, g)
+    torch.cuda.synchronize()
+    for a, b in zip(pa, pb):
+        assert torch.equal(a, b)
+
+
+def test_bad_pointer_alignment_is_rejected():
+    from optimizer_nesterov_momentum_gb300 import MuonError
+
+    shapes = [Shape(64, 64)]
+    opt = make_optimizer(shapes)
+    buf = torch.zeros(64 * 64 + 4, device="cuda")
+    p = buf[1:1 + 64 * 64].view(64, 64)  # 4-byte offset
+    g = torch.zeros(64, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(MuonError) as ei:
+        opt.step([p], [g])
+    assert ei.value.code == -2
+
+
+def test_graph_capture_replay_matches_eager():
+    shapes = [Shape(128, 384), Shape(384, 128), Shape(128, 512, split=4)]
+    params, grads = _inputs(shapes, 3, seed=19)
+    eager = make_optimizer(shapes, lr=0.03)
+    graphed = make_optimizer(shapes, lr=0.03)
+    pe = [p.cuda() for p in params]
+    pg = [p.cuda() for p in params]
+    gbuf = [g.cuda() for g in grads[0]]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graphed.step(pg, gbuf)  # warm-up (also exercises the pointer cache)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        graphed.step(pg, gbuf)
+    graphed.reset()
+    for p, p0 in zip(pg, params):
+        p.copy_(p0.cuda())
+    for k in range(3):
+        for dst, src in zip(gbuf, grads[k]):
+            dst.copy_(src.cuda())
+        graph.replay()
+        eager.step(pe, gbuf)
+    torch.cuda.synchronize()
+    for a, b in zip(pe, pg):
+        assert torch.equal(a, b)
