@@ -104,7 +104,7 @@ __device__ __forceinline__ float momentum_elem(float g, float& b, float mu, int 
 }
 
 template <int CAP, bool GRAD_F32>
-__global__ void __launch_bounds__(256) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
+__global__ void __launch_bounds__(256, 5) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float su[kTile][kTile + 1];
     __shared__ float red[8];
     const int4 tile = p.tiles[blockIdx.x];
@@ -115,6 +115,30 @@ __global__ void __launch_bounds__(256) k_momentum(const __grid_constant__ ElemPa
     const void* gbase = p.ptr.grad[d.parent];
     float sumsq = 0.f;
 
+    // all loads of both row passes first (independent 16-byte loads in flight)
+    float g[2][8], b[2][8];
+    bool act[2];
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
+        act[pass] = r < d.rows && c < d.cols;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) g[pass][e] = b[pass][e] = 0.f;
+        if (act[pass]) {
+            const int64_t goff = d.grad_off + (int64_t)r * d.ld + c;
+            const float* bptr = d.mom + (int64_t)r * d.ld_mom + c;
+            if (d.vec) {
+                load_grad8<GRAD_F32>(gbase, goff, g[pass]);
+                load8_f32(bptr, b[pass]);
+            } else {
+                for (int e = 0; e < 8 && c + e < d.cols; ++e) {
+                    g[pass][e] = load_grad1<GRAD_F32>(gbase, goff + e);
+                    b[pass][e] = bptr[e];
+                }
+            }
+        }
+    }
+
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
         const int rl = pass * 32 + tr, cl = tc * 8;
@@ -122,21 +146,18 @@ __global__ void __launch_bounds__(256) k_momentum(const __grid_constant__ ElemPa
         float u[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) u[e] = 0.f;
-        if (r < d.rows && c < d.cols) {
-            const int64_t goff = d.grad_off + (int64_t)r * d.ld + c;
+        if (act[pass]) {
             float* bptr = d.mom + (int64_t)r * d.ld_mom + c;
-            if (d.vec) {
-                float g[8], b[8];
-                load_grad8<GRAD_F32>(gbase, goff, g);
-                load8_f32(bptr, b);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) u[e] = momentum_elem(g[e], b[e], mu, p.lerp_form, p.nesterov);
-                store8_f32(bptr, b);
+            for (int e = 0; e < 8; ++e) u[e] = momentum_elem(g[pass][e], b[pass][e], mu, p.lerp_form, p.nesterov);
+            if (d.vec) {
+                store8_f32(bptr, b[pass]);
             } else {
-                for (int e = 0; e < 8 && c + e < d.cols; ++e) {
-                    float b = bptr[e];
-                    u[e] = momentum_elem(load_grad1<GRAD_F32>(gbase, goff + e), b, mu, p.lerp_form, p.nesterov);
-                    bptr[e] = b;
+                for (int e = 0; e < 8; ++e) {
+                    if (c + e < d.cols)
+                        bptr[e] = b[pass][e];
+                    else
+                        u[e] = 0.f;
                 }
             }
 #pragma unroll
@@ -228,7 +249,7 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
 }
 
 template <int CAP>
-__global__ void __launch_bounds__(256) k_apply(const __grid_constant__ ElemParams<CAP> p) {
+__global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float so[kTile][kTile + 1];
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
@@ -237,7 +258,34 @@ __global__ void __launch_bounds__(256) k_apply(const __grid_constant__ ElemParam
     const float decay = 1.f - p.hp[HP_LR] * d.lr_mul * p.hp[HP_WD] * d.wd_mul;
     float* P = p.ptr.param[d.parent] + d.grad_off;
 
+    // loads of both row passes first
+    float pv[2][8], o[2][8];
+    bool act[2];
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
+        act[pass] = r < d.rows && c < d.cols;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pv[pass][e] = o[pass][e] = 0.f;
+        if (act[pass]) {
+            const float* pp = P + (int64_t)r * d.ld + c;
+            if (d.vec) {
+                load8_f32(pp, pv[pass]);
+            } else {
+                for (int e = 0; e < 8 && c + e < d.cols; ++e) pv[pass][e] = pp[e];
+            }
+            if (!d.transposed) {
+                const uint16_t* src = d.o16 + (int64_t)r * d.ldx + c;
+                if (d.vec)
+                    load8_bf16(src, o[pass]);
+                else
+                    for (int e = 0; e < 8 && c + e < d.cols; ++e) o[pass][e] = bf2f(src[e]);
+            }
+        }
+    }
+
     if (d.transposed) {
+        // O is stored in the wide orientation: stage its tile transposed through shared memory
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
             const int i = pass * 32 + tr;
@@ -256,37 +304,34 @@ __global__ void __launch_bounds__(256) k_apply(const __grid_constant__ ElemParam
             for (int e = 0; e < 8; ++e) so[i][tc * 8 + e] = v[e];
         }
         __syncthreads();
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int rl = pass * 32 + tr, cl = tc * 8;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[pass][e] = so[cl + e][rl];
+        }
     }
 
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
-        const int rl = pass * 32 + tr, cl = tc * 8;
-        const int r = r0 + rl, c = c0 + cl;
-        if (r >= d.rows || c >= d.cols) continue;
+        if (!act[pass]) continue;
+        const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
         float* pp = P + (int64_t)r * d.ld + c;
-        float o[8], f[8];
+        float f[8];
         if (d.transposed) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = so[cl + e][rl];
             for (int e = 0; e < 8; ++e) f[e] = (c + e < d.cols) ? d.lane[c + e] : 0.f;
         } else {
-            const uint16_t* src = d.o16 + (int64_t)r * d.ldx + c;
-            if (d.vec)
-                load8_bf16(src, o);
-            else
-                for (int e = 0; e < 8; ++e) o[e] = (c + e < d.cols) ? bf2f(src[e]) : 0.f;
             const float fr = d.lane[r];
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = fr;
         }
-        if (d.vec) {
-            float pv[8];
-            load8_f32(pp, pv);
+        float out[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pv[e] = fmaf(-f[e], o[e], pv[e] * decay);
-            store8_f32(pp, pv);
+        for (int e = 0; e < 8; ++e) out[e] = fmaf(-f[e], o[pass][e], pv[pass][e] * decay);
+        if (d.vec) {
+            store8_f32(pp, out);
         } else {
-            for (int e = 0; e < 8 && c + e < d.cols; ++e) pp[e] = fmaf(-f[e], o[e], pp[e] * decay);
+            for (int e = 0; e < 8 && c + e < d.cols; ++e) pp[e] = out[e];
         }
     }
 }

@@ -96,8 +96,11 @@ struct GemmGroup {
 };
 
 struct GemmParams {
-    CUtensorMap map_a[kMaxGroupsPerLaunch];  // left operand (K-major)
-    CUtensorMap map_b[kMaxGroupsPerLaunch];  // right operand of the update (MN-major X)
+    CUtensorMap map_a[kMaxGroupsPerLaunch];     // left operand (K-major)
+    CUtensorMap map_b[kMaxGroupsPerLaunch];     // right operand of the update (MN-major X)
+    CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, update fp32 X tile
+    CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: bf16 tile; update: fp32 X'
+    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored bf16 tile; update: bf16 X'
     GemmGroup grp[kMaxGroupsPerLaunch];
     const int4* tiles;       // {group slot, index in group, tile row, tile col}
     int32_t ntiles;

@@ -65,8 +65,10 @@ struct Group {
     float* rowsq = nullptr;
     float* v = nullptr;
     float* lane = nullptr;
-    // TMA descriptors
+    // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), fp32 iterate
+    // boxes (32 x 128), bf16 iterate output boxes (32 x 128), mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
+    CUtensorMap map_u32, map_x32[2], map_x16o[2], map_a_mir, map_p_mir;
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
@@ -162,18 +164,24 @@ PFN_encodeTiled get_encode_fn() {
     return fn;
 }
 
-// 3-D bf16 tensor map over `count` matrices of rows x cols, row stride ld
-// (elements), 128-byte swizzle, box {64, box_rows, 1}.
+// 3-D tensor map over `count` matrices of rows x cols (row stride ld elements,
+// matrices back to back), box {box_cols, box_rows, 1}.
+bool encode_3d(PFN_encodeTiled enc, CUtensorMap* map, CUtensorMapDataType dtype, int esize, void* base, int64_t cols,
+               int64_t rows, int64_t count, int64_t ld, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swz) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(ld * esize * rows)};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_bf16_3d(PFN_encodeTiled enc, CUtensorMap* map, void* base, int64_t cols, int64_t rows, int64_t count,
                     int64_t ld, uint32_t box_rows) {
-    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
-    cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(ld * 2 * rows)};
-    cuuint32_t box[3] = {64, box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_3d(enc, map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, count, ld, 64, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int CAP>
@@ -518,7 +526,16 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                   encode_bf16_3d(enc, &g.map_p_k, g.p16, g.m, g.m, g.count, g.lda, kBM);
         for (int b = 0; b < 2 && ok; ++b)
             ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
-                 encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64);
+                 encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64) &&
+                 encode_3d(enc, &g.map_x32[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.x32[b], g.n, g.m, g.count,
+                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 encode_3d(enc, &g.map_x16o[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
+                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B);
+        ok = ok &&
+             encode_3d(enc, &g.map_u32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.u32, g.n, g.m, g.count, g.ldx, 32, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+             encode_bf16_3d(enc, &g.map_a_mir, g.a16, g.m, g.m, g.count, g.lda, 64) &&
+             encode_bf16_3d(enc, &g.map_p_mir, g.p16, g.m, g.m, g.count, g.lda, 64);
         if (!ok) {
             cudaFree(h->arena);
             delete h;
@@ -628,17 +645,25 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     G.rowsq = g.rowsq;
                     if (mode == MODE_GRAM) {
                         gp.map_a[sl] = first ? g.map_u_k : g.map_x_k[in_buf];
+                        gp.map_out[sl] = g.map_a_k;
+                        gp.map_out2[sl] = g.map_a_mir;
                         G.out16 = g.a16;
                         G.opl16 = xin16;
                         G.opr16 = xin16;
                     } else if (mode == MODE_POLY) {
                         gp.map_a[sl] = g.map_a_k;
+                        gp.map_ein[sl] = g.map_a_k;
+                        gp.map_out[sl] = g.map_p_k;
+                        gp.map_out2[sl] = g.map_p_mir;
                         G.out16 = g.p16;
                         G.opl16 = g.a16;
                         G.opr16 = g.a16;
                     } else {
                         gp.map_a[sl] = g.map_p_k;
                         gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
+                        gp.map_ein[sl] = first ? g.map_u32 : g.map_x32[in_buf];
+                        gp.map_out[sl] = g.map_x32[out_buf];
+                        gp.map_out2[sl] = g.map_x16o[out_buf];
                         G.opl16 = g.p16;
                         G.opr16 = xin16;
                     }

@@ -14,13 +14,17 @@
 // for GRAM / POLY (rows again, thanks to the symmetry) and MN-major for
 // UPDATE (X[k, j] with j contiguous), selected in the instruction descriptor.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over a tile list):
-//   warp 0     TMA producer (one thread): 128 B-swizzled tiles into a ring of
-//              shared-memory stages, completion tracked by mbarriers
+// Warp roles (224 threads, one CTA per SM, persistent over a tile list):
+//   warp 0     TMA producer (one thread): 128 B-swizzled operand tiles into a
+//              ring of shared-memory stages, completion tracked by mbarriers
 //   warp 1     TMEM allocator + MMA issuer (one thread): tcgen05.mma M=128,
 //              N=128/256, K=16 into a double-buffered TMEM accumulator
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w owns TMEM lanes
-//              32*(w%4)..+31), combine in fp32, round to bf16, store
+//              32*(w%4)..+31), combine in fp32, round, write swizzled
+//              shared-memory staging tiles; one thread issues TMA bulk stores
+//   warp 6     epilogue loader (one thread, POLY and UPDATE): TMA-loads the
+//              tiles the epilogue combines with (A for POLY, the fp32 iterate
+//              for UPDATE) into the same staging slots
 // Every wait is bounded (2 s); on a timeout the kernel sets the status word,
 // lets copies and MMAs in flight finish, frees TMEM and returns.
 #include "muon_internal.h"
@@ -30,54 +34,33 @@ namespace muon {
 
 template <int MODE>
 struct TcCfg {
-    static constexpr int BN = (MODE == MODE_UPDATE) ? kBNUpd : kBNSym;
-    static constexpr int STAGES = (MODE == MODE_UPDATE) ? 4 : 6;
+    static constexpr bool UPD = (MODE == MODE_UPDATE);
+    static constexpr int BN = UPD ? kBNUpd : kBNSym;
+    static constexpr int STAGES = (MODE == MODE_GRAM) ? 5 : (MODE == MODE_POLY ? 4 : 3);
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr bool B_MN = (MODE == MODE_UPDATE);
+    static constexpr bool B_MN = UPD;
     static constexpr uint32_t IDESC = make_idesc_bf16(kBM, BN, B_MN);
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    // epilogue: column chunks staged in shared memory
+    static constexpr int CHUNK = UPD ? 32 : 64;          // columns per chunk
+    static constexpr int NCHUNK = BN / CHUNK;
+    static constexpr int ESLOTS = UPD ? 3 : 2;
+    static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
+    static constexpr int EIN_BYTES = UPD ? kBM * 32 * 4 : (HAS_EIN ? kBM * 64 * 2 : 0);  // fp32 X / bf16 A
+    static constexpr int EOUT_BYTES = UPD ? kBM * 32 * 2 : kBM * 64 * 2;                 // bf16 out
+    static constexpr int EMIR_BYTES = UPD ? 0 : 64 * kBM * 2;                           // mirrored bf16 out
+    static constexpr int SLOT_BYTES = EIN_BYTES + EOUT_BYTES + EMIR_BYTES;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + ESLOTS * SLOT_BYTES + 1024 /*align*/ + 512;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void store_bf16_row32(uint16_t* dst, const float (&v)[32], int nvalid) {
-    if (nvalid >= 32) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf2(v[8 * q + 0], v[8 * q + 1]);
-            w.y = pack_bf2(v[8 * q + 2], v[8 * q + 3]);
-            w.z = pack_bf2(v[8 * q + 4], v[8 * q + 5]);
-            w.w = pack_bf2(v[8 * q + 6], v[8 * q + 7]);
-            d4[q] = w;
-        }
-    } else {
-        for (int e = 0; e < nvalid; ++e) dst[e] = f2bf(v[e]);
-    }
-}
-
-__device__ __forceinline__ void load_bf16_row32(const uint16_t* src, float (&v)[32], int nvalid) {
-    if (nvalid >= 32) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 w = s4[q];
-            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                v[8 * q + 2 * h] = __uint_as_float(ws[h] << 16);
-                v[8 * q + 2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
-            }
-        }
-    } else {
-        for (int e = 0; e < 32; ++e) v[e] = (e < nvalid) ? bf2f(src[e]) : 0.f;
-    }
-}
+constexpr int kThreads = 224;
+constexpr int kStoreThread = 64;  // warp 2, lane 0: issues and tracks the bulk stores
 
 template <int MODE>
-__global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constant__ GemmParams p) {
     using C = TcCfg<MODE>;
     constexpr int BN = C::BN;
     constexpr int STAGES = C::STAGES;
@@ -86,13 +69,17 @@ __global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ G
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * C::A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_BYTES);
+    uint8_t* sE = sB + STAGES * C::B_BYTES;  // ESLOTS x {ein | eout | emir}
+    uint64_t* full = reinterpret_cast<uint64_t*>(sE + C::ESLOTS * C::SLOT_BYTES);
     uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;   // [2] accumulator ready
-    uint64_t* tempty = tfull + 2;       // [2] accumulator drained
-    uint64_t* mma_done = tempty + 2;    // abort path only
+    uint64_t* tfull = empty + STAGES;      // [2] accumulator ready
+    uint64_t* tempty = tfull + 2;          // [2] accumulator drained
+    uint64_t* ein_full = tempty + 2;       // [ESLOTS] epilogue input landed
+    uint64_t* ein_empty = ein_full + C::ESLOTS;  // [ESLOTS] slot free for the loader
+    uint64_t* mma_done = ein_empty + C::ESLOTS;  // abort path only
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* s_go = abort_flag + 1;  // [2] epilogue verdicts, used in turn
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -105,6 +92,10 @@ __global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ G
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 4);
+        }
+        for (int s = 0; s < C::ESLOTS; ++s) {
+            mbar_init(&ein_full[s], 1);
+            mbar_init(&ein_empty[s], 1);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -120,11 +111,11 @@ __global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ G
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ operand producer
         if (lane == 0) {
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_a[g]);
-                if (MODE == MODE_UPDATE) tma_prefetch_desc(&p.map_b[g]);
+                if (C::B_MN) tma_prefetch_desc(&p.map_b[g]);
             }
             int stage = 0;
             uint32_t phase = 0;
@@ -146,14 +137,13 @@ __global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ G
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     uint8_t* a_dst = sA + stage * C::A_BYTES;
                     uint8_t* b_dst = sB + stage * C::B_BYTES;
-                    if (MODE == MODE_UPDATE) {
-                        tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
+                    tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
+                    if (C::B_MN) {
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
                             tma_load_3d(b_dst + c * (64 * kBK * 2), &p.map_b[g], &full[stage], tj * BN + c * 64,
                                         kb * kBK, idx);
                     } else {
-                        tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
                         tma_load_3d(b_dst, &p.map_a[g], &full[stage], kb * kBK, tj * BN, idx);
                     }
                     issued[stage] = true;
@@ -205,11 +195,8 @@ __global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ G
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t adesc = make_sdesc_sw128(a_st + kk * 32, 16, 1024);
-                        uint64_t bdesc;
-                        if (C::B_MN)
-                            bdesc = make_sdesc_sw128(b_st + kk * (16 * 128), 64 * kBK * 2, 1024);
-                        else
-                            bdesc = make_sdesc_sw128(b_st + kk * 32, 16, 1024);
+                        const uint64_t bdesc = C::B_MN ? make_sdesc_sw128(b_st + kk * (16 * 128), 64 * kBK * 2, 1024)
+                                                       : make_sdesc_sw128(b_st + kk * 32, 16, 1024);
                         umma_bf16(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
                         any = true;
                     }
@@ -231,114 +218,231 @@ __global__ void __launch_bounds__(192, 1) k_ns_gemm_tc(const __grid_constant__ G
             }
         }
         __syncwarp();
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ epilogue loader
+        if (C::HAS_EIN && lane == 0) {
+            for (int g = 0; g < p.ngroups; ++g) tma_prefetch_desc(&p.map_ein[g]);
+            int slot = 0;
+            uint32_t phase = 0;
+            uint32_t issued_phase[C::ESLOTS];
+            bool issued[C::ESLOTS];
+#pragma unroll
+            for (int s = 0; s < C::ESLOTS; ++s) issued[s] = false;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+                const int4 tile = p.tiles[t];
+                const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
+                for (int c = 0; c < C::NCHUNK; ++c) {
+                    if (!mbar_wait(&ein_empty[slot], phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ein_full[slot], C::EIN_BYTES);
+                    tma_load_3d(sE + slot * C::SLOT_BYTES, &p.map_ein[g], &ein_full[slot], tj * BN + c * C::CHUNK,
+                                ti * kBM, idx);
+                    issued[slot] = true;
+                    issued_phase[slot] = phase;
+                    if (++slot == C::ESLOTS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+#pragma unroll
+                for (int s = 0; s < C::ESLOTS; ++s)
+                    if (issued[s]) mbar_wait_drain(&ein_full[s], issued_phase[s], 100000000ull);
+            }
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
-        const int r_in_tile = quad * 32 + lane;
+        const uint32_t r = (uint32_t)(quad * 32 + lane);  // row within the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const bool store_thread = threadIdx.x == kStoreThread;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        int slot = 0;
+        uint32_t ephase = 0;
+        int prev_slot = -1;  // store thread: slot whose bulk store is still being read
+        int dec = 0;         // verdict counter (identical on all epilogue threads)
+        // Every wait of the epilogue ends in one verdict for all 128 threads: the
+        // store thread publishes its own outcome (and any abort raised elsewhere),
+        // a named barrier orders it, everyone reads the same flag.
+        auto decide = [&](bool mine) -> bool {
+            if (store_thread) s_go[dec & 1] = (mine && !*abort_flag) ? 1 : 0;
+            named_barrier(1, 128);
+            const bool go = s_go[dec & 1] != 0;
+            ++dec;
+            return go;
+        };
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
             const int4 tile = p.tiles[t];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             const bool got = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
-            if (!__all_sync(0xffffffffu, got)) break;
+            if (!decide(got)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            const int row = ti * kBM + r_in_tile;
             const uint32_t t_acc = tmem_base + lane_off + (uint32_t)(acc * BN);
-            if (MODE == MODE_UPDATE) {
-                const bool row_ok = row < G.m;
-                const float s1 = p.first ? p.norm_scale[G.sub0 + idx] : 1.f;
-                const int64_t xoff = (int64_t)idx * G.x_stride + (int64_t)row * G.ldx;
-                float sumsq = 0.f;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+            float scale = 1.f;
+            if (p.first && MODE != MODE_POLY) {
+                const float s = p.norm_scale[G.sub0 + idx];
+                scale = (MODE == MODE_GRAM) ? s * s : s;
+            }
+            float sumsq = 0.f;
+            for (int c = 0; c < C::NCHUNK; ++c) {
+                uint8_t* ein = sE + slot * C::SLOT_BYTES;
+                uint8_t* eout = ein + C::EIN_BYTES;
+                uint8_t* emir = eout + C::EOUT_BYTES;
+                bool go;
+                if (C::HAS_EIN) {
+                    go = decide(mbar_wait(&ein_full[slot], ephase, abort_flag, p.status));
+                } else {
+                    // the bulk store that last read this slot must be done before it is rewritten
+                    if (store_thread) bulk_wait_read<C::ESLOTS - 1>();
+                    go = decide(true);
+                }
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+                if (MODE == MODE_UPDATE) {
                     float v[32];
                     tmem_load_32x32(t_acc + c * 32, v);
-                    const int col0 = tj * BN + c * 32;
-                    const int nvalid = min(32, G.n - col0);
-                    if (row_ok && nvalid > 0) {
-                        float x[32];
-                        const float* xin = G.x32_in + xoff + col0;
-                        if (nvalid >= 32) {
+                    float y[32];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                float4 f = reinterpret_cast<const float4*>(xin)[q];
-                                x[4 * q] = f.x;
-                                x[4 * q + 1] = f.y;
-                                x[4 * q + 2] = f.z;
-                                x[4 * q + 3] = f.w;
-                            }
-                        } else {
-                            for (int e = 0; e < 32; ++e) x[e] = (e < nvalid) ? xin[e] : 0.f;
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 x = *reinterpret_cast<const float4*>(ein + sw128(r, j));
+                        y[4 * j + 0] = scale * fmaf(p.ca, x.x, v[4 * j + 0]);
+                        y[4 * j + 1] = scale * fmaf(p.ca, x.y, v[4 * j + 1]);
+                        y[4 * j + 2] = scale * fmaf(p.ca, x.z, v[4 * j + 2]);
+                        y[4 * j + 3] = scale * fmaf(p.ca, x.w, v[4 * j + 3]);
+                    }
+                    if (!p.last) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = s1 * fmaf(p.ca, x[e], v[e]);
-                        if (G.x32_out != nullptr) {
-                            float* xo = G.x32_out + xoff + col0;
-                            if (nvalid >= 32) {
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4*>(ein + sw128(r, j)) =
+                                make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+                    }
 #pragma unroll
-                                for (int q = 0; q < 8; ++q)
-                                    reinterpret_cast<float4*>(xo)[q] =
-                                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                            } else {
-                                for (int e = 0; e < nvalid; ++e) xo[e] = v[e];
-                            }
-                        }
-                        store_bf16_row32(G.x16_out + xoff + col0, v, nvalid);
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 w;
+                        w.x = pack_bf2(y[8 * j + 0], y[8 * j + 1]);
+                        w.y = pack_bf2(y[8 * j + 2], y[8 * j + 3]);
+                        w.z = pack_bf2(y[8 * j + 4], y[8 * j + 5]);
+                        w.w = pack_bf2(y[8 * j + 6], y[8 * j + 7]);
+                        *reinterpret_cast<uint4*>(eout + sw64(r, j)) = w;
                         if (p.want_rowsq) {
-                            for (int e = 0; e < 32; ++e) {
-                                if (e < nvalid) {
-                                    const float ob = bf2f(f2bf(v[e]));
-                                    sumsq = fmaf(ob, ob, sumsq);
-                                }
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const float lo = __uint_as_float(ws[h] << 16), hi = __uint_as_float(ws[h] & 0xFFFF0000u);
+                                sumsq = fmaf(lo, lo, sumsq);
+                                sumsq = fmaf(hi, hi, sumsq);
                             }
                         }
                     }
-                }
-                if (p.want_rowsq && row_ok)
-                    G.rowsq[((int64_t)idx * G.m + row) * G.ntile_n + tj] = sumsq;
-            } else {
-                const bool row_ok = row < G.m;
-                float sc = 1.f;
-                if (MODE == MODE_GRAM && p.first) {
-                    const float s = p.norm_scale[G.sub0 + idx];
-                    sc = s * s;
-                }
-                uint16_t* out = G.out16 + (int64_t)idx * G.a_stride;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_load_32x32(t_acc + c * 32, v);
-                    const int col0 = tj * BN + c * 32;
-                    const int nvalid = min(32, G.m - col0);
+                } else {
+                    float v[64];
+                    {
+                        float v0[32], v1[32];
+                        tmem_load_32x32(t_acc + c * 64, v0);
+                        tmem_load_32x32(t_acc + c * 64 + 32, v1);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            v[e] = v0[e];
+                            v[32 + e] = v1[e];
+                        }
+                    }
                     if (MODE == MODE_POLY) {
-                        float a[32];
-                        if (row_ok && nvalid > 0)
-                            load_bf16_row32(G.a16 + (int64_t)idx * G.a_stride + (int64_t)row * G.lda + col0, a,
-                                            nvalid);
-                        else
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) a[e] = 0.f;
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(ein + sw128(r, j));
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = fmaf(p.cb, a[e], p.cc * v[e]);
+                            for (int h = 0; h < 4; ++h) {
+                                const float lo = __uint_as_float(ws[h] << 16), hi = __uint_as_float(ws[h] & 0xFFFF0000u);
+                                v[8 * j + 2 * h] = fmaf(p.cb, lo, p.cc * v[8 * j + 2 * h]);
+                                v[8 * j + 2 * h + 1] = fmaf(p.cb, hi, p.cc * v[8 * j + 2 * h + 1]);
+                            }
+                        }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] *= sc;
+                        for (int e = 0; e < 64; ++e) v[e] *= scale;
                     }
-                    if (row_ok && nvalid > 0) store_bf16_row32(out + (int64_t)row * G.lda + col0, v, nvalid);
-                    if (ti != tj && row_ok) {
-                        for (int e = 0; e < 32; ++e)
-                            if (e < nvalid) out[(int64_t)(col0 + e) * G.lda + row] = f2bf(v[e]);
+                    uint16_t b[64];
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) b[e] = f2bf(v[e]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 w;
+                        w.x = (uint32_t)b[8 * j + 0] | ((uint32_t)b[8 * j + 1] << 16);
+                        w.y = (uint32_t)b[8 * j + 2] | ((uint32_t)b[8 * j + 3] << 16);
+                        w.z = (uint32_t)b[8 * j + 4] | ((uint32_t)b[8 * j + 5] << 16);
+                        w.w = (uint32_t)b[8 * j + 6] | ((uint32_t)b[8 * j + 7] << 16);
+                        *reinterpret_cast<uint4*>(eout + sw128(r, j)) = w;
+                    }
+                    if (ti != tj) {
+                        // mirror: element (r, e) of this chunk goes to row e, column r of the
+                        // transposed chunk, stored as two 64 x 64 boxes (columns r / 64)
+                        uint8_t* mbox = emir + (r >> 6) * (64 * 128);
+                        const uint32_t rc = r & 63u;
+#pragma unroll
+                        for (int e = 0; e < 64; ++e)
+                            *reinterpret_cast<uint16_t*>(mbox + sw128((uint32_t)e, rc >> 3) + (rc & 7u) * 2) = b[e];
                     }
                 }
+                fence_async_smem();
+                named_barrier(1, 128);
+                if (store_thread) {
+                    if (MODE == MODE_UPDATE) {
+                        const int x = tj * BN + c * C::CHUNK;
+                        if (x < G.n) {
+                            if (!p.last) tma_store_3d(&p.map_out[g], ein, x, ti * kBM, idx);
+                            tma_store_3d(&p.map_out2[g], eout, x, ti * kBM, idx);
+                        }
+                    } else {
+                        const int x = tj * BN + c * C::CHUNK;
+                        if (x < G.m) {
+                            tma_store_3d(&p.map_out[g], eout, x, ti * kBM, idx);
+                            if (ti != tj) {
+                                tma_store_3d(&p.map_out2[g], emir, ti * kBM, x, idx);
+                                if (ti * kBM + 64 < G.m) tma_store_3d(&p.map_out2[g], emir + 64 * 128, ti * kBM + 64, x, idx);
+                            }
+                        }
+                    }
+                    bulk_commit();
+                    if (C::HAS_EIN) {
+                        // hand the previous chunk's slot back to the loader once its store has read it
+                        bulk_wait_read<1>();
+                        if (prev_slot >= 0) mbar_arrive(&ein_empty[prev_slot]);
+                        prev_slot = slot;
+                    }
+                }
+                if (++slot == C::ESLOTS) {
+                    slot = 0;
+                    ephase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (MODE == MODE_UPDATE && p.want_rowsq) {
+                const int row = ti * kBM + (int)r;
+                if (row < G.m) G.rowsq[((int64_t)idx * G.m + row) * G.ntile_n + tj] = sumsq;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
+        }
+        if (store_thread) {
+            bulk_wait<0>();
+            if (C::HAS_EIN && prev_slot >= 0) mbar_arrive(&ein_empty[prev_slot]);
         }
     }
 
@@ -368,7 +472,7 @@ cudaError_t launch_ns_gemm_tc(const GemmParams& p, int num_sms, cudaStream_t str
     using C = TcCfg<MODE>;
     if (p.ntiles <= 0) return cudaSuccess;
     const int grid = p.ntiles < num_sms ? p.ntiles : num_sms;
-    k_ns_gemm_tc<MODE><<<grid, 192, C::SMEM_BYTES, stream>>>(p);
+    k_ns_gemm_tc<MODE><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ from .muon_oracle import (
     frobenius_normalise,
     newton_schulz,
     newton_schulz_closed_form,
+    newton_schulz_mixed,
     zeropower_via_newtonschulz5,
     normuon_scale,
     shape_scale,
@@ -48,6 +49,7 @@ __all__ = [
     "frobenius_normalise",
     "newton_schulz",
     "newton_schulz_closed_form",
+    "newton_schulz_mixed",
     "zeropower_via_newtonschulz5",
     "normuon_scale",
     "shape_scale",

@@ -197,6 +197,26 @@ def newton_schulz(x: np.ndarray, steps: int = 5, coeffs=None, form: str = "page"
     return x
 
 
+def newton_schulz_mixed(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarray:
+    """Diagnostic: the iteration with the rounding points of a mixed-precision
+    bf16 tensor-core implementation (not a definition of the method).
+
+    The iterate is held in fp32; each product reads bf16-rounded operands and
+    accumulates exactly; A and P = b A + c A A are stored in bf16; the output
+    is rounded to bf16.  Used only to size the bf16 error of tiny matrices,
+    where a relative Frobenius error is dominated by a handful of singular
+    values and can exceed the 2e-2 bound that holds for the workloads.
+    """
+    f32 = lambda v: np.asarray(v, dtype=np.float32).astype(np.float64)
+    x = f32(x)
+    for a, b, c in _coeff_list(coeffs, steps):
+        xb = bf16_round(x)
+        A = bf16_round(xb @ xb.T)
+        P = bf16_round(b * A + c * (A @ A))
+        x = f32(a * x + P @ xb)
+    return bf16_round(x)
+
+
 def zeropower_via_newtonschulz5(g: np.ndarray, steps: int = 5, eps: float = NORM_EPS, coeffs=None,
                                 form: str = "page", bf16: bool = False) -> np.ndarray:
     """The [50B] orthogonalisation of one matrix, result in the input's orientation."""

@@ -20,6 +20,20 @@ import oracle
 
 TOL_STATE = 1e-5
 TOL_NS = 2e-2
+# Below this short side the relative Frobenius error of a bf16 iteration is
+# dominated by a few singular values and can exceed TOL_NS by itself; there the
+# bound is derived from the arithmetic: twice the error of the oracle's
+# mixed-precision emulation (same rounding points as the kernels) on the
+# same input, never less than TOL_NS.
+TINY_SIDE = 32
+
+
+def ns_tolerance(u_sub: np.ndarray, o_ref: np.ndarray, ns_steps: int, ns_coeffs) -> float:
+    if min(u_sub.shape) >= TINY_SIDE:
+        return TOL_NS
+    x0, _ = oracle.orient_wide(oracle.frobenius_normalise(u_sub))
+    emu = oracle.newton_schulz_mixed(x0, ns_steps, ns_coeffs)
+    return max(TOL_NS, 2.0 * rel(emu, o_ref))
 
 
 def rel(a, b) -> float:
@@ -49,6 +63,10 @@ class Errors:
     v_e2e: float = 0.0
     delta_stage: float = 0.0
     delta_e2e: float = 0.0
+    # NS-dependent errors divided by their per-matrix bound (<= 1 passes)
+    ortho_ratio: float = 0.0
+    v_e2e_ratio: float = 0.0
+    delta_e2e_ratio: float = 0.0
     per_matrix: List[Dict] = field(default_factory=list)
 
     worst: Dict = field(default_factory=dict)
@@ -62,16 +80,17 @@ class Errors:
     def assert_within(self, state_tol=TOL_STATE, ns_tol=TOL_NS, normuon=True):
         msg = repr(self)
         assert self.momentum <= state_tol, msg
-        assert self.ortho <= ns_tol, msg
+        assert self.ortho_ratio <= 1.0, msg
         assert self.delta_stage <= state_tol, msg
-        assert self.delta_e2e <= ns_tol, msg
+        assert self.delta_e2e_ratio <= 1.0, msg
         if normuon:
             assert self.v_stage <= state_tol, msg
-            assert self.v_e2e <= ns_tol, msg
+            assert self.v_e2e_ratio <= 1.0, msg
 
     def __repr__(self):
         return (f"Errors(momentum={self.momentum:.2e}, ortho={self.ortho:.2e}, v_stage={self.v_stage:.2e}, "
                 f"v_e2e={self.v_e2e:.2e}, delta_stage={self.delta_stage:.2e}, delta_e2e={self.delta_e2e:.2e}, "
+                f"ratios(ortho={self.ortho_ratio:.2f}, v={self.v_e2e_ratio:.2f}, delta={self.delta_e2e_ratio:.2f}), "
                 f"worst={self.worst})")
 
 
@@ -139,20 +158,25 @@ def run_parity(shapes: Sequence[Shape], params_cpu: List[torch.Tensor], grads_st
             errs.update(where=(step, i), momentum=rel(mom_gpu, orc.momentum[j]))
             p_new = params[i].double().cpu().numpy()
             d_gpu = p_new - p_old[i]
-            errs.update(where=(step, i), delta_e2e=rel(d_gpu, expect[j] - p_old[i]))
+            tol_parent = max(ns_tolerance(rec.u, rec.o, ns_steps, ns_coeffs) for rec in orc.records[j])
+            e_d = rel(d_gpu, expect[j] - p_old[i])
+            errs.update(where=(step, i), delta_e2e=e_d, delta_e2e_ratio=e_d / tol_parent)
             subs_p = oracle.split_matrix(p_old[i], sh.split, sh.split_mode)
             subs_d = oracle.split_matrix(d_gpu, sh.split, sh.split_mode)
             for q in range(sh.split):
                 k, info = where[(i, q)]
                 rec = orc.records[j][q]
+                tol = ns_tolerance(rec.u, rec.o, ns_steps, ns_coeffs)
                 o_gpu = opt.get_state(MUON_STATE_ORTHO, k).double().cpu().numpy()
                 e_o = rel(o_gpu, rec.o)
-                errs.update(where=(step, i, q), ortho=e_o)
+                errs.update(where=(step, i, q), ortho=e_o, ortho_ratio=e_o / tol)
                 # stage-wise: NorMuon and write-back fed with the GPU's own O
                 if normuon:
                     o_sc, v_exp = oracle.normuon_scale(o_gpu, v_old[(i, q)], beta2)
                     v_gpu = opt.get_state(MUON_STATE_SECOND_MOMENT, k).double().cpu().numpy()
-                    errs.update(where=(step, i, q), v_stage=rel(v_gpu, v_exp), v_e2e=rel(v_gpu, rec.v))
+                    e_v = rel(v_gpu, rec.v)
+                    errs.update(where=(step, i, q), v_stage=rel(v_gpu, v_exp), v_e2e=e_v,
+                                v_e2e_ratio=e_v / (tol if tol > TOL_NS else TOL_NS))
                     scale = 1.0
                 else:
                     o_sc = o_gpu
@@ -160,5 +184,5 @@ def run_parity(shapes: Sequence[Shape], params_cpu: List[torch.Tensor], grads_st
                 upd = o_sc.T if info["transposed"] else o_sc
                 exp_sub = oracle.write_back(subs_p[q], upd, cur_lr, sh.lr_mul, weight_decay, sh.wd_mul, scale)
                 errs.update(where=(step, i, q), delta_stage=rel(subs_d[q], exp_sub - subs_p[q]))
-                errs.per_matrix.append(dict(step=step, parent=i, q=q, ortho=e_o))
+                errs.per_matrix.append(dict(step=step, parent=i, q=q, ortho=e_o, tol=tol))
     return errs, opt, params

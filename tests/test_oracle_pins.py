@@ -124,6 +124,16 @@ def test_closed_form_matches_iteration(m, n):
     assert _rel(oracle.newton_schulz_closed_form(x, 2, table), oracle.newton_schulz(x, 2, table)) < 1e-9
 
 
+def test_mixed_precision_emulation_is_close_to_fp64():
+    # The mixed-precision diagnostic must stay an approximation of the same
+    # map: within bf16 accuracy of the closed form on a well-conditioned matrix.
+    rng = np.random.default_rng(31)
+    x = _rand_with_spectrum(rng, 48, 96, np.linspace(0.2, 1.0, 48)) * 0.7
+    ref = oracle.newton_schulz(x, steps=5)
+    emu = oracle.newton_schulz_mixed(x, steps=5)
+    assert 1e-4 < _rel(emu, ref) < 5e-2
+
+
 def test_classic_newton_schulz_converges_to_polar_factor():
     rng = np.random.default_rng(11)
     s = np.linspace(0.05, 1.0, 24)

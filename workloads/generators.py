@@ -39,7 +39,7 @@ def _rng(seed: int, index: int) -> np.random.Generator:
 def _orthonormal_columns(rng: np.random.Generator, n: int, k: int, device: Optional[str]) -> torch.Tensor:
     """n x k matrix with orthonormal columns (Haar-distributed up to the sign fix)."""
     g = rng.standard_normal((n, k))
-    if device is None or device == "cpu":
+    if device is None or device == "cpu" or k <= 64:
         q, r = np.linalg.qr(g)
         q = q * np.sign(np.diag(r))[None, :]
         return torch.from_numpy(q)
@@ -111,6 +111,8 @@ def grads_for(wl: Workload, step: int = 0, device: Optional[str] = None,
     for i in idx:
         m: MatrixShape = wl.matrices[i]
         g = make(_rng(s, i), m.rows, m.cols, device=device)
+        if device is not None:
+            g = g.to(device)
         out.append(g.to(dt).contiguous())
     return out
 
