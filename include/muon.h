@@ -196,6 +196,35 @@ int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void*
 /* Overwrites one state array (MOMENTUM or SECOND_MOMENT) from `src`. */
 int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src, void* stream);
 
+/* ---- allocation-free entry point ------------------------------------------
+ *
+ * No counterpart on the pages: this call exists for callers that cannot call
+ * cudaMalloc where they run the step -- frameworks whose device memory belongs
+ * to their own pool or arena, code where an allocation would synchronise the
+ * device or is not allowed (a latency-critical loop, a host callback), and
+ * users with a device-memory budget fixed at load time.
+ *
+ * For ONE matrix, dense row-major rows x cols: updates `momentum` (fp32, in
+ * place) with the gradient `grad` (bf16 or fp32 per grad_dtype) exactly as
+ * muon_step does (lerp or mul/add form), forms the Nesterov direction u and
+ * writes x0 = u / (||u||_F + 1e-7) (fp32) -- steps S1, S2 and S4 in the
+ * matrix's own orientation.  All pointers are device pointers.  Work is
+ * enqueued on `stream`; nothing is allocated.
+ *
+ * Scratch: the per-tile partial sums of u^2 and the scale live in one static
+ * device array of MUON_NOALLOC_MAX_TILES + 64 floats (about 256 KB) that every
+ * GPU loading the library holds until the process exits.  Matrices needing
+ * more than MUON_NOALLOC_MAX_TILES tiles of 64 x 64 are rejected with
+ * MUON_ERR_SHAPE.  All calls share the array; calls whose work overlaps on
+ * the GPU race, so order them on one stream.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make it before any stream capture.  Returns MUON_OK, MUON_ERR_ARG,
+ * MUON_ERR_SHAPE or MUON_ERR_CUDA. */
+#define MUON_NOALLOC_MAX_TILES 65536
+int muon_nesterov_normalize_noalloc(const void* grad, int32_t grad_dtype, float* momentum, float* x0,
+                                    int64_t rows, int64_t cols, float mu, int32_t lerp_form,
+                                    int32_t nesterov, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

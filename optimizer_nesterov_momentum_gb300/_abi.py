@@ -60,7 +60,10 @@ EXPORTED = (
     "muon_get_stage_times",
     "muon_get_state",
     "muon_set_state",
+    "muon_nesterov_normalize_noalloc",
 )
+
+MUON_NOALLOC_MAX_TILES = 65536
 
 
 class muon_shape(ctypes.Structure):
@@ -125,6 +128,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_get_stage_times.argtypes = [c_void_p, POINTER(c_float)]
     lib.muon_get_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
     lib.muon_set_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.muon_nesterov_normalize_noalloc.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_int64,
+                                                    c_float, c_int32, c_int32, c_void_p]
     for name in EXPORTED:
         if name not in ("muon_config_default", "muon_error_string", "muon_last_error"):
             getattr(lib, name).restype = c_int32
@@ -221,3 +226,13 @@ def muon_get_state(h, which: int, index: int, dst_ptr: int, stream: int) -> None
 
 def muon_set_state(h, which: int, index: int, src_ptr: int, stream: int) -> None:
     _check(load_library().muon_set_state(h, which, index, c_void_p(src_ptr), c_void_p(stream)), h)
+
+
+def muon_nesterov_normalize_noalloc(grad_ptr: int, grad_dtype: int, momentum_ptr: int, x0_ptr: int, rows: int,
+                                    cols: int, mu: float, lerp_form: bool, nesterov: bool, stream: int) -> None:
+    """Allocation-free momentum + Nesterov + normalisation of one dense matrix (see include/muon.h)."""
+    rc = load_library().muon_nesterov_normalize_noalloc(
+        c_void_p(grad_ptr), grad_dtype, c_void_p(momentum_ptr), c_void_p(x0_ptr), rows, cols, mu, int(lerp_form),
+        int(nesterov), c_void_p(stream))
+    if rc < 0:
+        raise MuonError(rc, muon_error_string(rc))
