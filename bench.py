@@ -68,7 +68,7 @@ def work_model(wl, grad_bytes):
         "gram_flops": gram, "poly_flops": poly, "update_flops": upd,
         "ns_flops": ns * (gram + poly + upd),
         "ns_flops_dense": ns * sum(4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3 for r, c in wl.sub_shapes()),
-        "momentum_bytes": elems * (grad_bytes + 4 + 4 + 4 + 2),   # g, buf r/w, u fp32 + bf16
+        "momentum_bytes": elems * (grad_bytes + 4 + 4 + 2 + 2),   # g, buf r/w, u as bf16 hi + lo
         "apply_bytes": elems * (2 + 4 + 4),                        # O bf16, p r/w
     }
 

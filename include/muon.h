@@ -187,7 +187,8 @@ int muon_get_stage_times(muon_handle h, float* out);
 #define MUON_STATE_ORTHO 2         /* per split matrix: last Newton-Schulz output O, wide
                                       orientation m x n, dense, raw bf16 (2 bytes each) */
 #define MUON_STATE_DIRECTION 3     /* per split matrix: last Nesterov direction u, wide
-                                      orientation m x n, fp32 */
+                                      orientation m x n, fp32, DEVICE destination only
+                                      (rebuilt on the device from its bf16 hi + lo pair) */
 
 /* Copies one state array into `dst` (host or device memory; cudaMemcpyDefault)
  * on `stream`.  Layouts as listed above. */

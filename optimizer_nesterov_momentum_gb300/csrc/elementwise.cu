@@ -14,6 +14,8 @@
 //                 O read in the wide orientation and written back in the
 //                 caller's orientation
 // Reductions are two-stage with a fixed order, so results are reproducible.
+#include <algorithm>
+
 #include "muon_internal.h"
 #include "ptx_sm103.cuh"
 
@@ -82,6 +84,21 @@ __device__ __forceinline__ void store8_bf16(uint16_t* dst, const float (&v)[8]) 
     *reinterpret_cast<uint4*>(dst) = w;
 }
 
+// u as two bf16 halves: hi = bf16(u), lo = bf16(u - hi); hi + lo keeps ~16 mantissa bits
+__device__ __forceinline__ void store8_hilo(uint16_t* hi, uint16_t* lo, const float (&v)[8]) {
+    float l[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) l[e] = v[e] - bf2f(f2bf(v[e]));
+    store8_bf16(hi, v);
+    store8_bf16(lo, l);
+}
+
+__device__ __forceinline__ void store1_hilo(uint16_t* hi, uint16_t* lo, float v) {
+    const uint16_t h = f2bf(v);
+    *hi = h;
+    *lo = f2bf(v - bf2f(h));
+}
+
 __device__ __forceinline__ void load8_bf16(const uint16_t* src, float (&v)[8]) {
     const uint4 w = *reinterpret_cast<const uint4*>(src);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -104,7 +121,7 @@ __device__ __forceinline__ float momentum_elem(float g, float& b, float mu, int 
 }
 
 template <int CAP, bool GRAD_F32>
-__global__ void __launch_bounds__(256, 5) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
+__global__ void __launch_bounds__(256) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float su[kTile][kTile + 1];
     __shared__ float red[8];
     const int4 tile = p.tiles[blockIdx.x];
@@ -115,30 +132,6 @@ __global__ void __launch_bounds__(256, 5) k_momentum(const __grid_constant__ Ele
     const void* gbase = p.ptr.grad[d.parent];
     float sumsq = 0.f;
 
-    // all loads of both row passes first (independent 16-byte loads in flight)
-    float g[2][8], b[2][8];
-    bool act[2];
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-        const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
-        act[pass] = r < d.rows && c < d.cols;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) g[pass][e] = b[pass][e] = 0.f;
-        if (act[pass]) {
-            const int64_t goff = d.grad_off + (int64_t)r * d.ld + c;
-            const float* bptr = d.mom + (int64_t)r * d.ld_mom + c;
-            if (d.vec) {
-                load_grad8<GRAD_F32>(gbase, goff, g[pass]);
-                load8_f32(bptr, b[pass]);
-            } else {
-                for (int e = 0; e < 8 && c + e < d.cols; ++e) {
-                    g[pass][e] = load_grad1<GRAD_F32>(gbase, goff + e);
-                    b[pass][e] = bptr[e];
-                }
-            }
-        }
-    }
-
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
         const int rl = pass * 32 + tr, cl = tc * 8;
@@ -146,18 +139,21 @@ __global__ void __launch_bounds__(256, 5) k_momentum(const __grid_constant__ Ele
         float u[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) u[e] = 0.f;
-        if (act[pass]) {
+        if (r < d.rows && c < d.cols) {
+            const int64_t goff = d.grad_off + (int64_t)r * d.ld + c;
             float* bptr = d.mom + (int64_t)r * d.ld_mom + c;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) u[e] = momentum_elem(g[pass][e], b[pass][e], mu, p.lerp_form, p.nesterov);
             if (d.vec) {
-                store8_f32(bptr, b[pass]);
+                float g[8], b[8];
+                load_grad8<GRAD_F32>(gbase, goff, g);
+                load8_f32(bptr, b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) u[e] = momentum_elem(g[e], b[e], mu, p.lerp_form, p.nesterov);
+                store8_f32(bptr, b);
             } else {
-                for (int e = 0; e < 8; ++e) {
-                    if (c + e < d.cols)
-                        bptr[e] = b[pass][e];
-                    else
-                        u[e] = 0.f;
+                for (int e = 0; e < 8 && c + e < d.cols; ++e) {
+                    float b = bptr[e];
+                    u[e] = momentum_elem(load_grad1<GRAD_F32>(gbase, goff + e), b, mu, p.lerp_form, p.nesterov);
+                    bptr[e] = b;
                 }
             }
 #pragma unroll
@@ -165,13 +161,9 @@ __global__ void __launch_bounds__(256, 5) k_momentum(const __grid_constant__ Ele
             if (!d.transposed) {
                 const int64_t xo = (int64_t)r * d.ldx + c;
                 if (d.vec) {
-                    store8_f32(d.u32 + xo, u);
-                    store8_bf16(d.u16 + xo, u);
+                    store8_hilo(d.u16 + xo, d.ulo16 + xo, u);
                 } else {
-                    for (int e = 0; e < 8 && c + e < d.cols; ++e) {
-                        d.u32[xo + e] = u[e];
-                        d.u16[xo + e] = f2bf(u[e]);
-                    }
+                    for (int e = 0; e < 8 && c + e < d.cols; ++e) store1_hilo(d.u16 + xo + e, d.ulo16 + xo + e, u[e]);
                 }
             }
         }
@@ -193,13 +185,9 @@ __global__ void __launch_bounds__(256, 5) k_momentum(const __grid_constant__ Ele
                 for (int e = 0; e < 8; ++e) v[e] = su[i][tc * 8 + e];
                 const int64_t xo = (int64_t)wr * d.ldx + wc;
                 if (wc + 8 <= d.rows) {
-                    store8_f32(d.u32 + xo, v);
-                    store8_bf16(d.u16 + xo, v);
+                    store8_hilo(d.u16 + xo, d.ulo16 + xo, v);
                 } else {
-                    for (int e = 0; e < 8 && wc + e < d.rows; ++e) {
-                        d.u32[xo + e] = v[e];
-                        d.u16[xo + e] = f2bf(v[e]);
-                    }
+                    for (int e = 0; e < 8 && wc + e < d.rows; ++e) store1_hilo(d.u16 + xo + e, d.ulo16 + xo + e, v[e]);
                 }
             }
         }
@@ -334,6 +322,23 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
             for (int e = 0; e < 8 && c + e < d.cols; ++e) pp[e] = out[e];
         }
     }
+}
+
+// u = hi + lo of one matrix into a dense fp32 m x n array (state access)
+__global__ void k_combine_hilo(float* dst, const uint16_t* hi, const uint16_t* lo, int m, int n, int ld) {
+    const int64_t total = (int64_t)m * n;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / n, j = e % n;
+        dst[e] = bf2f(hi[i * ld + j]) + bf2f(lo[i * ld + j]);
+    }
+}
+
+cudaError_t launch_combine_hilo(float* dst, const uint16_t* hi, const uint16_t* lo, int m, int n, int ld,
+                                cudaStream_t s) {
+    const int64_t total = (int64_t)m * n;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    k_combine_hilo<<<blocks, 256, 0, s>>>(dst, hi, lo, m, n, ld);
+    return cudaGetLastError();
 }
 
 __global__ void k_set_hparams(float* hp, float lr, float mu, float beta2, float wd) {

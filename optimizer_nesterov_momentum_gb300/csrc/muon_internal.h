@@ -3,9 +3,9 @@
 // Layout of the device state for one handle:
 //   * momentum arena: one dense fp32 [rows x cols] block per parameter (S1).
 //   * per split matrix ("sub"), in the wide orientation m x n (m <= n):
-//       u32 / u16   Nesterov direction, fp32 and its bf16 copy (S2)
-//       x32 / x16   Newton-Schulz iterate, fp32 master + bf16 tensor-core operand,
-//                   two buffers used in turn (S5-S7)
+//       u16 / ulo16 Nesterov direction as a pair of bf16 arrays, u = hi + lo (S2)
+//       x16 / xlo16 Newton-Schulz iterate as hi + lo; the hi half is the
+//                   tensor-core operand; two buffers used in turn (S5-S7)
 //       a16 / p16   A = X X^T and P = b A + c A A, bf16, m x m (S5, S6)
 //       rowsq       per (row, 256-column tile) sums of O^2 from the last iteration (S8)
 //       v           second moment, fp32 [m] (S8)
@@ -52,8 +52,8 @@ struct SubDesc {
     int32_t k1_tile0, k1_ntiles;  // range of this sub's elementwise tiles
     float lr_mul, wd_mul, shape_scale;
     // wide-orientation arenas of this sub
-    float* u32;
-    uint16_t* u16;
+    uint16_t* u16;        // hi half of u (bf16(u))
+    uint16_t* ulo16;      // lo half of u (bf16(u - hi))
     const uint16_t* o16;  // final Newton-Schulz output (bf16), m x n, row stride ldx
     float* rowsq;         // m x ntile_n
     float* v;             // m
@@ -85,9 +85,9 @@ struct GemmGroup {
     int32_t sub0;            // sub index of the group's first matrix (subs are group-ordered)
     int64_t x_stride;        // elements between matrices in x / u arenas (m * ldx)
     int64_t a_stride;        // elements between matrices in a / p arenas (m * lda)
-    const float* x32_in;     // update: fp32 iterate read by the a*X term
-    float* x32_out;          // update: next fp32 iterate (nullptr on the last iteration)
-    uint16_t* x16_out;       // update: next bf16 iterate / final O
+    const uint16_t* xlo_in;  // update: lo half of the iterate read by the a*X term (hi: opr16)
+    uint16_t* xlo_out;       // update: lo half of the next iterate (nullptr on the last iteration)
+    uint16_t* x16_out;       // update: hi half of the next iterate / final O
     const uint16_t* a16;     // poly epilogue: A (also simt operand)
     uint16_t* out16;         // gram: A, poly: P
     float* rowsq;            // update, last iteration: per-row sums of O^2 (m * ntile_n per matrix)
@@ -98,9 +98,10 @@ struct GemmGroup {
 struct GemmParams {
     CUtensorMap map_a[kMaxGroupsPerLaunch];     // left operand (K-major)
     CUtensorMap map_b[kMaxGroupsPerLaunch];     // right operand of the update (MN-major X)
-    CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, update fp32 X tile
-    CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: bf16 tile; update: fp32 X'
-    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored bf16 tile; update: bf16 X'
+    CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, update hi half of X
+    CUtensorMap map_ein2[kMaxGroupsPerLaunch];  // epilogue input: update lo half of X
+    CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: bf16 tile; update: hi half of X'
+    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored bf16 tile; update: lo half of X'
     GemmGroup grp[kMaxGroupsPerLaunch];
     const int4* tiles;       // {group slot, index in group, tile row, tile col}
     int32_t ntiles;

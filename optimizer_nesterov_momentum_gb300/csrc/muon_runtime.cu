@@ -33,6 +33,7 @@ cudaError_t launch_apply(const ElemParams<CAP>&, cudaStream_t);
 cudaError_t launch_norm_scale(const NormParams&, cudaStream_t);
 cudaError_t launch_lane_stats(const LaneParams&, cudaStream_t);
 cudaError_t launch_set_hparams(float*, float, float, float, float, cudaStream_t);
+cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
 template <int MODE>
 cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
@@ -55,20 +56,20 @@ struct Group {
     int32_t count = 0;
     int32_t ldx = 0, lda = 0, ntile_n = 0;
     int32_t sub0 = 0;
-    // device arenas (count matrices back to back)
-    float* u32 = nullptr;
+    // device arenas (count matrices back to back); u and X are hi + lo bf16 pairs
     uint16_t* u16 = nullptr;
-    float* x32[2] = {nullptr, nullptr};
+    uint16_t* ulo16 = nullptr;
     uint16_t* x16[2] = {nullptr, nullptr};
+    uint16_t* xlo16[2] = {nullptr, nullptr};
     uint16_t* a16 = nullptr;
     uint16_t* p16 = nullptr;
     float* rowsq = nullptr;
     float* v = nullptr;
     float* lane = nullptr;
-    // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), fp32 iterate
-    // boxes (32 x 128), bf16 iterate output boxes (32 x 128), mirror boxes of A / P
+    // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), 32 x 128 boxes of
+    // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
-    CUtensorMap map_u32, map_x32[2], map_x16o[2], map_a_mir, map_p_mir;
+    CUtensorMap map_u_hi, map_u_lo, map_x_hi[2], map_x_lo[2], map_a_mir, map_p_mir;
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
@@ -422,7 +423,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->n_elem_tiles = (int32_t)elem_tiles.size();
     const size_t o_norm_part = take(sizeof(float) * elem_tiles.size());
     const size_t o_mom = take(sizeof(float) * (size_t)mom_total);
-    std::vector<size_t> go_u32, go_u16, go_x32[2], go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane;
+    std::vector<size_t> go_ulo, go_u16, go_xlo[2], go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane;
     for (auto& g : h->groups) g.count = 0;
     for (int sidx = 0; sidx < nsubs; ++sidx) h->groups[sub_group[order[sidx]]].count++;
     {
@@ -434,10 +435,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     }
     for (auto& g : h->groups) {
         const size_t xe = (size_t)g.count * g.m * g.ldx, ae = (size_t)g.count * g.m * g.lda;
-        go_u32.push_back(take(xe * 4));
+        go_ulo.push_back(take(xe * 2));
         go_u16.push_back(take(xe * 2));
         for (int b = 0; b < 2; ++b) {
-            go_x32[b].push_back(take(xe * 4));
+            go_xlo[b].push_back(take(xe * 2));
             go_x16[b].push_back(take(xe * 2));
         }
         go_a16.push_back(take(ae * 2));
@@ -509,10 +510,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->d_gemm_tiles = reinterpret_cast<int4*>(base + o_gtiles);
     for (size_t gi = 0; gi < h->groups.size(); ++gi) {
         Group& g = h->groups[gi];
-        g.u32 = reinterpret_cast<float*>(base + go_u32[gi]);
+        g.ulo16 = reinterpret_cast<uint16_t*>(base + go_ulo[gi]);
         g.u16 = reinterpret_cast<uint16_t*>(base + go_u16[gi]);
         for (int b = 0; b < 2; ++b) {
-            g.x32[b] = reinterpret_cast<float*>(base + go_x32[b][gi]);
+            g.xlo16[b] = reinterpret_cast<uint16_t*>(base + go_xlo[b][gi]);
             g.x16[b] = reinterpret_cast<uint16_t*>(base + go_x16[b][gi]);
         }
         g.a16 = reinterpret_cast<uint16_t*>(base + go_a16[gi]);
@@ -527,13 +528,15 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         for (int b = 0; b < 2 && ok; ++b)
             ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
                  encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64) &&
-                 encode_3d(enc, &g.map_x32[b], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.x32[b], g.n, g.m, g.count,
-                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-                 encode_3d(enc, &g.map_x16o[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
+                 encode_3d(enc, &g.map_x_hi[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
+                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                 encode_3d(enc, &g.map_x_lo[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.xlo16[b], g.n, g.m, g.count,
                            g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
-             encode_3d(enc, &g.map_u32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.u32, g.n, g.m, g.count, g.ldx, 32, kBM,
-                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+             encode_3d(enc, &g.map_u_hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_3d(enc, &g.map_u_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.ulo16, g.n, g.m, g.count, g.ldx, 32,
+                       kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_bf16_3d(enc, &g.map_a_mir, g.a16, g.m, g.m, g.count, g.lda, 64) &&
              encode_bf16_3d(enc, &g.map_p_mir, g.p16, g.m, g.m, g.count, g.lda, 64);
         if (!ok) {
@@ -574,8 +577,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         d.wd_mul = h->wd_mul[pd.parent];
         d.shape_scale = (float)std::sqrt(std::max(1.0, (double)pd.rows / (double)pd.cols));
         const int64_t xo = (int64_t)gi * g.m * g.ldx;
-        d.u32 = g.u32 + xo;
         d.u16 = g.u16 + xo;
+        d.ulo16 = g.ulo16 + xo;
         d.o16 = g.x16[last_buf] + xo;
         d.rowsq = g.rowsq + (int64_t)gi * g.m * g.ntile_n;
         d.v = g.v + (int64_t)gi * g.m;
@@ -638,8 +641,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     G.x_stride = (int64_t)g.m * g.ldx;
                     G.a_stride = (int64_t)g.m * g.lda;
                     const uint16_t* xin16 = first ? g.u16 : g.x16[in_buf];
-                    G.x32_in = first ? g.u32 : g.x32[in_buf];
-                    G.x32_out = last ? nullptr : g.x32[out_buf];
+                    G.xlo_in = first ? g.ulo16 : g.xlo16[in_buf];
+                    G.xlo_out = last ? nullptr : g.xlo16[out_buf];
                     G.x16_out = g.x16[out_buf];
                     G.a16 = g.a16;
                     G.rowsq = g.rowsq;
@@ -661,9 +664,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     } else {
                         gp.map_a[sl] = g.map_p_k;
                         gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
-                        gp.map_ein[sl] = first ? g.map_u32 : g.map_x32[in_buf];
-                        gp.map_out[sl] = g.map_x32[out_buf];
-                        gp.map_out2[sl] = g.map_x16o[out_buf];
+                        gp.map_ein[sl] = first ? g.map_u_hi : g.map_x_hi[in_buf];
+                        gp.map_ein2[sl] = first ? g.map_u_lo : g.map_x_lo[in_buf];
+                        gp.map_out[sl] = g.map_x_hi[out_buf];
+                        gp.map_out2[sl] = g.map_x_lo[out_buf];
                         G.opl16 = g.p16;
                         G.opr16 = xin16;
                     }
@@ -876,8 +880,14 @@ int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void*
         MUON_CUDA(h, cudaMemcpy2DAsync(dst, sizeof(uint16_t) * d.n, d.o16, sizeof(uint16_t) * d.ldx,
                                        sizeof(uint16_t) * d.n, d.m, cudaMemcpyDefault, s));
     } else if (which == MUON_STATE_DIRECTION) {
-        MUON_CUDA(h, cudaMemcpy2DAsync(dst, sizeof(float) * d.n, d.u32, sizeof(float) * d.ldx, sizeof(float) * d.n,
-                                       d.m, cudaMemcpyDefault, s));
+        // u is stored as a bf16 hi + lo pair: combine it on the device into the caller's array
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, dst) != cudaSuccess ||
+            (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)) {
+            cudaGetLastError();
+            return fail(h, MUON_ERR_ARG, "MUON_STATE_DIRECTION needs a device destination");
+        }
+        MUON_CUDA(h, launch_combine_hilo(static_cast<float*>(dst), d.u16, d.ulo16, d.m, d.n, d.ldx, s));
     } else {
         return fail(h, MUON_ERR_ARG, "bad state selector %d", which);
     }

@@ -77,9 +77,11 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
                 G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = f2bf(fmaf(p.cb, a, p.cc * acc[r][c]));
             } else {
                 const int64_t off = (int64_t)idx * G.x_stride + (int64_t)i * G.ldx + j;
-                const float y = s * fmaf(p.ca, G.x32_in[off], acc[r][c]);
-                if (G.x32_out) G.x32_out[off] = y;
-                G.x16_out[off] = f2bf(y);
+                const float x = bf2f(R[(int64_t)i * ldr + j]) + bf2f(G.xlo_in[off]);  // hi + lo
+                const float y = s * fmaf(p.ca, x, acc[r][c]);
+                const uint16_t hi = f2bf(y);
+                G.x16_out[off] = hi;
+                if (G.xlo_out) G.xlo_out[off] = f2bf(y - bf2f(hi));
             }
         }
     }

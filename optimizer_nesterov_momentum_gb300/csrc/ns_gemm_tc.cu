@@ -23,8 +23,11 @@
 //              32*(w%4)..+31), combine in fp32, round, write swizzled
 //              shared-memory staging tiles; one thread issues TMA bulk stores
 //   warp 6     epilogue loader (one thread, POLY and UPDATE): TMA-loads the
-//              tiles the epilogue combines with (A for POLY, the fp32 iterate
-//              for UPDATE) into the same staging slots
+//              tiles the epilogue combines with (A for POLY; the hi and lo
+//              halves of the iterate for UPDATE) into the same staging slots
+// The iterate X is held as two bf16 arrays, X = hi + lo (about 16 mantissa
+// bits): hi is the tensor-core operand, and the UPDATE epilogue rebuilds X
+// from both halves for the a*X term and splits the result the same way.
 // Every wait is bounded (2 s); on a timeout the kernel sets the status word,
 // lets copies and MMAs in flight finish, frees TMEM and returns.
 #include "muon_internal.h"
@@ -46,10 +49,11 @@ struct TcCfg {
     // epilogue: column chunks staged in shared memory
     static constexpr int CHUNK = UPD ? 32 : 64;          // columns per chunk
     static constexpr int NCHUNK = BN / CHUNK;
-    static constexpr int ESLOTS = UPD ? 3 : 2;
+    static constexpr int ESLOTS = UPD ? 4 : 2;
     static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
-    static constexpr int EIN_BYTES = UPD ? kBM * 32 * 4 : (HAS_EIN ? kBM * 64 * 2 : 0);  // fp32 X / bf16 A
-    static constexpr int EOUT_BYTES = UPD ? kBM * 32 * 2 : kBM * 64 * 2;                 // bf16 out
+    static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // one bf16 half, 32 cols
+    static constexpr int EIN_BYTES = UPD ? 2 * HALF_BYTES : (HAS_EIN ? kBM * 64 * 2 : 0);  // X hi|lo / A
+    static constexpr int EOUT_BYTES = UPD ? 0 : kBM * 64 * 2;                           // UPDATE: in place
     static constexpr int EMIR_BYTES = UPD ? 0 : 64 * kBM * 2;                           // mirrored bf16 out
     static constexpr int SLOT_BYTES = EIN_BYTES + EOUT_BYTES + EMIR_BYTES;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + ESLOTS * SLOT_BYTES + 1024 /*align*/ + 512;
@@ -221,7 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
     } else if (warp == 6) {
         // ------------------------------------------------------------ epilogue loader
         if (C::HAS_EIN && lane == 0) {
-            for (int g = 0; g < p.ngroups; ++g) tma_prefetch_desc(&p.map_ein[g]);
+            for (int g = 0; g < p.ngroups; ++g) {
+                tma_prefetch_desc(&p.map_ein[g]);
+                if (C::UPD) tma_prefetch_desc(&p.map_ein2[g]);
+            }
             int slot = 0;
             uint32_t phase = 0;
             uint32_t issued_phase[C::ESLOTS];
@@ -238,8 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         break;
                     }
                     mbar_arrive_expect_tx(&ein_full[slot], C::EIN_BYTES);
-                    tma_load_3d(sE + slot * C::SLOT_BYTES, &p.map_ein[g], &ein_full[slot], tj * BN + c * C::CHUNK,
-                                ti * kBM, idx);
+                    uint8_t* dst = sE + slot * C::SLOT_BYTES;
+                    tma_load_3d(dst, &p.map_ein[g], &ein_full[slot], tj * BN + c * C::CHUNK, ti * kBM, idx);
+                    if (C::UPD)
+                        tma_load_3d(dst + C::HALF_BYTES, &p.map_ein2[g], &ein_full[slot], tj * BN + c * C::CHUNK,
+                                    ti * kBM, idx);
                     issued[slot] = true;
                     issued_phase[slot] = phase;
                     if (++slot == C::ESLOTS) {
@@ -314,38 +324,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                 if (MODE == MODE_UPDATE) {
                     float v[32];
                     tmem_load_32x32(t_acc + c * 32, v);
-                    float y[32];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 x = *reinterpret_cast<const float4*>(ein + sw128(r, j));
-                        y[4 * j + 0] = scale * fmaf(p.ca, x.x, v[4 * j + 0]);
-                        y[4 * j + 1] = scale * fmaf(p.ca, x.y, v[4 * j + 1]);
-                        y[4 * j + 2] = scale * fmaf(p.ca, x.z, v[4 * j + 2]);
-                        y[4 * j + 3] = scale * fmaf(p.ca, x.w, v[4 * j + 3]);
-                    }
-                    if (!p.last) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<float4*>(ein + sw128(r, j)) =
-                                make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
-                    }
+                    uint8_t* hib = ein;                  // hi half, rows of 64 bytes, 64-byte swizzle
+                    uint8_t* lob = ein + C::HALF_BYTES;  // lo half, same layout
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        uint4 w;
-                        w.x = pack_bf2(y[8 * j + 0], y[8 * j + 1]);
-                        w.y = pack_bf2(y[8 * j + 2], y[8 * j + 3]);
-                        w.z = pack_bf2(y[8 * j + 4], y[8 * j + 5]);
-                        w.w = pack_bf2(y[8 * j + 6], y[8 * j + 7]);
-                        *reinterpret_cast<uint4*>(eout + sw64(r, j)) = w;
-                        if (p.want_rowsq) {
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        const uint4 hw = *reinterpret_cast<const uint4*>(hib + sw64(r, j));
+                        const uint4 lw = *reinterpret_cast<const uint4*>(lob + sw64(r, j));
+                        const uint32_t hs[4] = {hw.x, hw.y, hw.z, hw.w};
+                        const uint32_t ls[4] = {lw.x, lw.y, lw.z, lw.w};
+                        uint32_t ho[4], lo[4];
 #pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const float lo = __uint_as_float(ws[h] << 16), hi = __uint_as_float(ws[h] & 0xFFFF0000u);
-                                sumsq = fmaf(lo, lo, sumsq);
-                                sumsq = fmaf(hi, hi, sumsq);
+                        for (int h = 0; h < 4; ++h) {
+                            const float x0 = __uint_as_float(hs[h] << 16) + __uint_as_float(ls[h] << 16);
+                            const float x1 = __uint_as_float(hs[h] & 0xFFFF0000u) + __uint_as_float(ls[h] & 0xFFFF0000u);
+                            const float y0 = scale * fmaf(p.ca, x0, v[8 * j + 2 * h]);
+                            const float y1 = scale * fmaf(p.ca, x1, v[8 * j + 2 * h + 1]);
+                            const uint16_t b0 = f2bf(y0), b1 = f2bf(y1);
+                            ho[h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                            lo[h] = pack_bf2(y0 - bf2f(b0), y1 - bf2f(b1));
+                            if (p.want_rowsq) {
+                                const float o0 = bf2f(b0), o1 = bf2f(b1);
+                                sumsq = fmaf(o0, o0, sumsq);
+                                sumsq = fmaf(o1, o1, sumsq);
                             }
                         }
+                        *reinterpret_cast<uint4*>(hib + sw64(r, j)) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                        if (!p.last) *reinterpret_cast<uint4*>(lob + sw64(r, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 } else {
                     float v[64];
@@ -403,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     if (MODE == MODE_UPDATE) {
                         const int x = tj * BN + c * C::CHUNK;
                         if (x < G.n) {
-                            if (!p.last) tma_store_3d(&p.map_out[g], ein, x, ti * kBM, idx);
-                            tma_store_3d(&p.map_out2[g], eout, x, ti * kBM, idx);
+                            tma_store_3d(&p.map_out[g], ein, x, ti * kBM, idx);
+                            if (!p.last) tma_store_3d(&p.map_out2[g], ein + C::HALF_BYTES, x, ti * kBM, idx);
                         }
                     } else {
                         const int x = tj * BN + c * C::CHUNK;
