@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
     float before = 0.f, after = 0.f;
     for (int i = threadIdx.x; i < d.m; i += 256) {
         float rs = 0.f;
-        for (int t = 0; t < d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n + t];
+        for (int t = 0; t < 2 * d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n * 2 + t];
         const float r = rs * inv_n;
         const float v0 = d.v[i];
         const float v1 = fmaf(1.f - beta2, r - v0, v0);  // v.lerp_(r, 1 - beta2)

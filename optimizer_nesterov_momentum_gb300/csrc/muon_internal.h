@@ -7,7 +7,8 @@
 //       x16 / xlo16 Newton-Schulz iterate as hi + lo; the hi half is the
 //                   tensor-core operand; two buffers used in turn (S5-S7)
 //       a16 / p16   A = X X^T and P = b A + c A A, bf16, m x m (S5, S6)
-//       rowsq       per (row, 256-column tile) sums of O^2 from the last iteration (S8)
+//       rowsq       per (row, 256-column tile, column half) sums of O^2 from the
+//                   last iteration (S8)
 //       v           second moment, fp32 [m] (S8)
 //       lane        per-lane update factor lr*lr_mul*gamma/sqrt(v) (S9)
 //   Matrices with the same (m, n) form a group and sit back to back in each
@@ -23,7 +24,7 @@ constexpr int kMaxGroupsPerLaunch = 8;
 constexpr int kTile = 64;            // edge of the elementwise tiles (K1 / K5)
 constexpr int kBM = 128;             // Newton-Schulz tile rows (TMEM lanes)
 constexpr int kBK = 64;              // k-block: 64 bf16 = one 128-byte swizzle row
-constexpr int kBNSym = 128;          // Gram / polynomial tile columns
+constexpr int kBNSym = 256;          // Gram / polynomial tile columns
 constexpr int kBNUpd = 256;          // update tile columns
 constexpr float kNormEps = 1e-7f;
 constexpr float kVFloor = 1e-10f;
@@ -48,14 +49,14 @@ struct SubDesc {
     int32_t vec;         // 8-wide vector access is legal (cols, ld, offsets multiples of 8)
     int32_t m, n;        // wide shape
     int32_t ldx;         // row stride of the wide arenas
-    int32_t ntile_n;     // 256-column tiles per row (rowsq entries per row)
+    int32_t ntile_n;     // 256-column tiles per row (2 rowsq entries each)
     int32_t k1_tile0, k1_ntiles;  // range of this sub's elementwise tiles
     float lr_mul, wd_mul, shape_scale;
     // wide-orientation arenas of this sub
     uint16_t* u16;        // hi half of u (bf16(u))
     uint16_t* ulo16;      // lo half of u (bf16(u - hi))
     const uint16_t* o16;  // final Newton-Schulz output (bf16), m x n, row stride ldx
-    float* rowsq;         // m x ntile_n
+    float* rowsq;         // m x ntile_n x 2
     float* v;             // m
     float* lane;          // m
 };
@@ -90,7 +91,7 @@ struct GemmGroup {
     uint16_t* x16_out;       // update: hi half of the next iterate / final O
     const uint16_t* a16;     // poly epilogue: A (also simt operand)
     uint16_t* out16;         // gram: A, poly: P
-    float* rowsq;            // update, last iteration: per-row sums of O^2 (m * ntile_n per matrix)
+    float* rowsq;            // update, last iteration: per-row sums of O^2 (m * ntile_n * 2 per matrix)
     const uint16_t* opl16;   // simt: left operand base (gram: X, poly: A, update: P)
     const uint16_t* opr16;   // simt: right operand base (gram: X, poly: A, update: X)
 };

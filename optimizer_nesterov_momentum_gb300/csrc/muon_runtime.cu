@@ -443,7 +443,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         }
         go_a16.push_back(take(ae * 2));
         go_p16.push_back(take(ae * 2));
-        go_rowsq.push_back(take((size_t)g.count * g.m * g.ntile_n * 4));
+        go_rowsq.push_back(take((size_t)g.count * g.m * g.ntile_n * 2 * 4));
         go_v.push_back(take((size_t)g.count * g.m * 4));
         go_lane.push_back(take((size_t)g.count * g.m * 4));
     }
@@ -471,9 +471,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             const Group& g = h->groups[g0 + sl];
             const int tm = (g.m + kBM - 1) / kBM;
             const int tn = (g.n + kBNUpd - 1) / kBNUpd;
+            const int ts = (g.m + kBNSym - 1) / kBNSym;  // 256-column blocks of A / P
             for (int idx = 0; idx < g.count; ++idx) {
+                // symmetric 128 x 256 tiles that reach the diagonal or lie above it
                 for (int ti = 0; ti < tm; ++ti)
-                    for (int tj = ti; tj < tm; ++tj) {
+                    for (int tj = 0; tj < ts; ++tj) {
+                        if ((tj * kBNSym + kBNSym - 1) / kBM < ti) continue;
                         gram.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
                         poly.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
                     }
@@ -580,7 +583,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         d.u16 = g.u16 + xo;
         d.ulo16 = g.ulo16 + xo;
         d.o16 = g.x16[last_buf] + xo;
-        d.rowsq = g.rowsq + (int64_t)gi * g.m * g.ntile_n;
+        d.rowsq = g.rowsq + (int64_t)gi * g.m * g.ntile_n * 2;
         d.v = g.v + (int64_t)gi * g.m;
         d.lane = g.lane + (int64_t)gi * g.m;
         h->subs.push_back(d);

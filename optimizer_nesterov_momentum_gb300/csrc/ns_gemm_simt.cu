@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(256) k_rowsq_simt(const __grid_constant__ Gemm
         const float v = bf2f(o[j]);
         s = fmaf(v, v, s);
     }
-    G.rowsq[((int64_t)idx * G.m + row) * G.ntile_n + t] = s;
+    float* out = G.rowsq + (((int64_t)idx * G.m + row) * G.ntile_n + t) * 2;  // (row, tile, half) layout
+    out[0] = s;
+    out[1] = 0.f;
 }
 
 template <int MODE>

@@ -8,21 +8,26 @@
 //   MODE_POLY    P = b A + c A A          (A symmetric, so A A = sum_k A[i,k] A[j,k])
 //   MODE_UPDATE  X' = s1 (a X + P X)      (s1 = s on the first iteration)
 //
-// A and P are symmetric: GRAM and POLY only compute tiles on and above the
-// diagonal and store each tile twice (itself and its mirror).  The left
+// A and P are symmetric: GRAM and POLY compute 128 x 256 tiles that reach the
+// diagonal or lie above it, and store every 128 x 128 block above the
+// diagonal twice (itself and its mirror) and the diagonal block once; the
+// 64-column chunks of a tile that fall below the diagonal are neither
+// staged nor stored.  The left
 // operand is always K-major (rows of X, A or P); the right operand is K-major
 // for GRAM / POLY (rows again, thanks to the symmetry) and MN-major for
 // UPDATE (X[k, j] with j contiguous), selected in the instruction descriptor.
 //
-// Warp roles (224 threads, one CTA per SM, persistent over a tile list):
+// Warp roles (352 threads, one CTA per SM, persistent over a tile list):
 //   warp 0     TMA producer (one thread): 128 B-swizzled operand tiles into a
 //              ring of shared-memory stages, completion tracked by mbarriers
 //   warp 1     TMEM allocator + MMA issuer (one thread): tcgen05.mma M=128,
 //              N=128/256, K=16 into a double-buffered TMEM accumulator
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w owns TMEM lanes
-//              32*(w%4)..+31), combine in fp32, round, write swizzled
-//              shared-memory staging tiles; one thread issues TMA bulk stores
-//   warp 6     epilogue loader (one thread, POLY and UPDATE): TMA-loads the
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//              32*(w%4)..+31; warps 2-5 take the first half of every column
+//              chunk, warps 6-9 the second), combine in fp32, round, write
+//              swizzled shared-memory staging tiles; one thread issues TMA
+//              bulk stores
+//   warp 10    epilogue loader (one thread, POLY and UPDATE): TMA-loads the
 //              tiles the epilogue combines with (A for POLY; the hi and lo
 //              halves of the iterate for UPDATE) into the same staging slots
 // The iterate X is held as two bf16 arrays, X = hi + lo (about 16 mantissa
@@ -38,8 +43,9 @@ namespace muon {
 template <int MODE>
 struct TcCfg {
     static constexpr bool UPD = (MODE == MODE_UPDATE);
+    static constexpr bool SYM = !UPD;
     static constexpr int BN = UPD ? kBNUpd : kBNSym;
-    static constexpr int STAGES = (MODE == MODE_GRAM) ? 5 : (MODE == MODE_POLY ? 4 : 3);
+    static constexpr int STAGES = (MODE == MODE_GRAM) ? 4 : 3;
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -49,18 +55,30 @@ struct TcCfg {
     // epilogue: column chunks staged in shared memory
     static constexpr int CHUNK = UPD ? 32 : 64;          // columns per chunk
     static constexpr int NCHUNK = BN / CHUNK;
-    static constexpr int ESLOTS = UPD ? 4 : 2;
+    static constexpr int ESLOTS = (MODE == MODE_GRAM) ? 1 : (UPD ? 4 : 2);
     static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
     static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // one bf16 half, 32 cols
     static constexpr int EIN_BYTES = UPD ? 2 * HALF_BYTES : (HAS_EIN ? kBM * 64 * 2 : 0);  // X hi|lo / A
     static constexpr int EOUT_BYTES = UPD ? 0 : kBM * 64 * 2;                           // UPDATE: in place
-    static constexpr int EMIR_BYTES = UPD ? 0 : 64 * kBM * 2;                           // mirrored bf16 out
+    // mirrored bf16 out: its own buffer for GRAM; POLY reuses its input buffer
+    static constexpr int EMIR_BYTES = (MODE == MODE_GRAM) ? 64 * kBM * 2 : 0;
     static constexpr int SLOT_BYTES = EIN_BYTES + EOUT_BYTES + EMIR_BYTES;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + ESLOTS * SLOT_BYTES + 1024 /*align*/ + 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // the loader gets a slot back only after the next chunk's store is issued,
+    // so a loaded epilogue input needs at least two slots to make progress
+    static_assert(!HAS_EIN || ESLOTS >= 2, "an epilogue with inputs needs two or more slots");
 };
 
-constexpr int kThreads = 224;
+// A 64-column chunk of a symmetric tile is live unless its 128-column block
+// lies left of (below) the diagonal block of the tile's rows.
+__device__ __forceinline__ bool sym_chunk_live(int ti, int tj, int c) {
+    return ((tj * kBNSym + c * 64) >> 7) >= ti;
+}
+
+constexpr int kThreads = 352;
+constexpr int kEpiThreads = 256;  // warps 2-9
+constexpr int kLoaderWarp = 10;
 constexpr int kStoreThread = 64;  // warp 2, lane 0: issues and tracks the bulk stores
 
 template <int MODE>
@@ -95,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], kEpiThreads / 32);
         }
         for (int s = 0; s < C::ESLOTS; ++s) {
             mbar_init(&ein_full[s], 1);
@@ -148,7 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                             tma_load_3d(b_dst + c * (64 * kBK * 2), &p.map_b[g], &full[stage], tj * BN + c * 64,
                                         kb * kBK, idx);
                     } else {
-                        tma_load_3d(b_dst, &p.map_a[g], &full[stage], kb * kBK, tj * BN, idx);
+#pragma unroll
+                        for (int h = 0; h < BN / kBM; ++h)
+                            tma_load_3d(b_dst + h * (kBM * kBK * 2), &p.map_a[g], &full[stage], kb * kBK,
+                                        tj * BN + h * kBM, idx);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             }
         }
         __syncwarp();
-    } else if (warp == 6) {
+    } else if (warp == kLoaderWarp) {
         // ------------------------------------------------------------ epilogue loader
         if (C::HAS_EIN && lane == 0) {
             for (int g = 0; g < p.ngroups; ++g) {
@@ -240,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                 const int4 tile = p.tiles[t];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 for (int c = 0; c < C::NCHUNK; ++c) {
+                    if (C::SYM && !sym_chunk_live(ti, tj, c)) continue;
                     if (!mbar_wait(&ein_empty[slot], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -268,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;                  // which half of each column chunk
         const uint32_t r = (uint32_t)(quad * 32 + lane);  // row within the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const bool store_thread = threadIdx.x == kStoreThread;
@@ -277,12 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         uint32_t ephase = 0;
         int prev_slot = -1;  // store thread: slot whose bulk store is still being read
         int dec = 0;         // verdict counter (identical on all epilogue threads)
-        // Every wait of the epilogue ends in one verdict for all 128 threads: the
+        // Every wait of the epilogue ends in one verdict for all epilogue threads: the
         // store thread publishes its own outcome (and any abort raised elsewhere),
         // a named barrier orders it, everyone reads the same flag.
         auto decide = [&](bool mine) -> bool {
             if (store_thread) s_go[dec & 1] = (mine && !*abort_flag) ? 1 : 0;
-            named_barrier(1, 128);
+            named_barrier(1, kEpiThreads);
             const bool go = s_go[dec & 1] != 0;
             ++dec;
             return go;
@@ -306,9 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             }
             float sumsq = 0.f;
             for (int c = 0; c < C::NCHUNK; ++c) {
+                if (C::SYM && !sym_chunk_live(ti, tj, c)) continue;  // below the diagonal: nothing to do
                 uint8_t* ein = sE + slot * C::SLOT_BYTES;
                 uint8_t* eout = ein + C::EIN_BYTES;
-                uint8_t* emir = eout + C::EOUT_BYTES;
+                uint8_t* emir = (MODE == MODE_POLY) ? ein : eout + C::EOUT_BYTES;
+                const int col0 = tj * BN + c * C::CHUNK;
+                const bool mirror = C::SYM && (col0 >> 7) > ti;  // strictly above the diagonal block
                 bool go;
                 if (C::HAS_EIN) {
                     go = decide(mbar_wait(&ein_full[slot], ephase, abort_flag, p.status));
@@ -322,12 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     break;
                 }
                 if (MODE == MODE_UPDATE) {
-                    float v[32];
-                    tmem_load_32x32(t_acc + c * 32, v);
+                    float v[16];
+                    tmem_load_32x16(t_acc + c * 32 + half * 16, v);
                     uint8_t* hib = ein;                  // hi half, rows of 64 bytes, 64-byte swizzle
                     uint8_t* lob = ein + C::HALF_BYTES;  // lo half, same layout
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const uint32_t j = (uint32_t)(half * 2 + jj);
                         const uint4 hw = *reinterpret_cast<const uint4*>(hib + sw64(r, j));
                         const uint4 lw = *reinterpret_cast<const uint4*>(lob + sw64(r, j));
                         const uint32_t hs[4] = {hw.x, hw.y, hw.z, hw.w};
@@ -337,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         for (int h = 0; h < 4; ++h) {
                             const float x0 = __uint_as_float(hs[h] << 16) + __uint_as_float(ls[h] << 16);
                             const float x1 = __uint_as_float(hs[h] & 0xFFFF0000u) + __uint_as_float(ls[h] & 0xFFFF0000u);
-                            const float y0 = scale * fmaf(p.ca, x0, v[8 * j + 2 * h]);
-                            const float y1 = scale * fmaf(p.ca, x1, v[8 * j + 2 * h + 1]);
+                            const float y0 = scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]);
+                            const float y1 = scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]);
                             const uint16_t b0 = f2bf(y0), b1 = f2bf(y1);
                             ho[h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                             lo[h] = pack_bf2(y0 - bf2f(b0), y1 - bf2f(b1));
@@ -352,57 +379,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         if (!p.last) *reinterpret_cast<uint4*>(lob + sw64(r, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 } else {
-                    float v[64];
-                    {
-                        float v0[32], v1[32];
-                        tmem_load_32x32(t_acc + c * 64, v0);
-                        tmem_load_32x32(t_acc + c * 64 + 32, v1);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            v[e] = v0[e];
-                            v[32 + e] = v1[e];
-                        }
-                    }
+                    float v[32];
+                    tmem_load_32x32(t_acc + c * 64 + half * 32, v);
                     if (MODE == MODE_POLY) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(ein + sw128(r, j));
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(ein + sw128(r, (uint32_t)(half * 4 + jj)));
                             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 const float lo = __uint_as_float(ws[h] << 16), hi = __uint_as_float(ws[h] & 0xFFFF0000u);
-                                v[8 * j + 2 * h] = fmaf(p.cb, lo, p.cc * v[8 * j + 2 * h]);
-                                v[8 * j + 2 * h + 1] = fmaf(p.cb, hi, p.cc * v[8 * j + 2 * h + 1]);
+                                v[8 * jj + 2 * h] = fmaf(p.cb, lo, p.cc * v[8 * jj + 2 * h]);
+                                v[8 * jj + 2 * h + 1] = fmaf(p.cb, hi, p.cc * v[8 * jj + 2 * h + 1]);
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) v[e] *= scale;
+                        for (int e = 0; e < 32; ++e) v[e] *= scale;
                     }
-                    uint16_t b[64];
+                    uint16_t b[32];
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) b[e] = f2bf(v[e]);
+                    for (int e = 0; e < 32; ++e) b[e] = f2bf(v[e]);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int jj = 0; jj < 4; ++jj) {
                         uint4 w;
-                        w.x = (uint32_t)b[8 * j + 0] | ((uint32_t)b[8 * j + 1] << 16);
-                        w.y = (uint32_t)b[8 * j + 2] | ((uint32_t)b[8 * j + 3] << 16);
-                        w.z = (uint32_t)b[8 * j + 4] | ((uint32_t)b[8 * j + 5] << 16);
-                        w.w = (uint32_t)b[8 * j + 6] | ((uint32_t)b[8 * j + 7] << 16);
-                        *reinterpret_cast<uint4*>(eout + sw128(r, j)) = w;
+                        w.x = (uint32_t)b[8 * jj + 0] | ((uint32_t)b[8 * jj + 1] << 16);
+                        w.y = (uint32_t)b[8 * jj + 2] | ((uint32_t)b[8 * jj + 3] << 16);
+                        w.z = (uint32_t)b[8 * jj + 4] | ((uint32_t)b[8 * jj + 5] << 16);
+                        w.w = (uint32_t)b[8 * jj + 6] | ((uint32_t)b[8 * jj + 7] << 16);
+                        *reinterpret_cast<uint4*>(eout + sw128(r, (uint32_t)(half * 4 + jj))) = w;
                     }
-                    if (ti != tj) {
+                    if (mirror) {
+                        // POLY writes the mirror over its input chunk: every row must be read first
+                        if (MODE == MODE_POLY) named_barrier(1, kEpiThreads);
                         // mirror: element (r, e) of this chunk goes to row e, column r of the
                         // transposed chunk, stored as two 64 x 64 boxes (columns r / 64)
                         uint8_t* mbox = emir + (r >> 6) * (64 * 128);
                         const uint32_t rc = r & 63u;
 #pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            *reinterpret_cast<uint16_t*>(mbox + sw128((uint32_t)e, rc >> 3) + (rc & 7u) * 2) = b[e];
+                        for (int e = 0; e < 32; ++e) {
+                            const uint32_t me = (uint32_t)(half * 32 + e);
+                            *reinterpret_cast<uint16_t*>(mbox + sw128(me, rc >> 3) + (rc & 7u) * 2) = b[e];
+                        }
                     }
                 }
                 fence_async_smem();
-                named_barrier(1, 128);
+                named_barrier(1, kEpiThreads);
                 if (store_thread) {
                     if (MODE == MODE_UPDATE) {
                         const int x = tj * BN + c * C::CHUNK;
@@ -411,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                             if (!p.last) tma_store_3d(&p.map_out2[g], ein + C::HALF_BYTES, x, ti * kBM, idx);
                         }
                     } else {
-                        const int x = tj * BN + c * C::CHUNK;
-                        if (x < G.m) {
-                            tma_store_3d(&p.map_out[g], eout, x, ti * kBM, idx);
-                            if (ti != tj) {
-                                tma_store_3d(&p.map_out2[g], emir, ti * kBM, x, idx);
-                                if (ti * kBM + 64 < G.m) tma_store_3d(&p.map_out2[g], emir + 64 * 128, ti * kBM + 64, x, idx);
+                        if (col0 < G.m) {
+                            tma_store_3d(&p.map_out[g], eout, col0, ti * kBM, idx);
+                            if (mirror) {
+                                tma_store_3d(&p.map_out2[g], emir, ti * kBM, col0, idx);
+                                if (ti * kBM + 64 < G.m)
+                                    tma_store_3d(&p.map_out2[g], emir + 64 * 128, ti * kBM + 64, col0, idx);
                             }
                         }
                     }
@@ -436,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             if (!ok) break;
             if (MODE == MODE_UPDATE && p.want_rowsq) {
                 const int row = ti * kBM + (int)r;
-                if (row < G.m) G.rowsq[((int64_t)idx * G.m + row) * G.ntile_n + tj] = sumsq;
+                if (row < G.m) G.rowsq[(((int64_t)idx * G.m + row) * G.ntile_n + tj) * 2 + half] = sumsq;
             }
             tc_fence_before();
             __syncwarp();
