@@ -29,7 +29,10 @@
 //              bulk stores
 //   warp 10    epilogue loader (one thread, POLY and UPDATE): TMA-loads the
 //              tiles the epilogue combines with (A for POLY; the hi and lo
-//              halves of the iterate for UPDATE) into the same staging slots
+//              halves of the iterate for UPDATE) into an input ring whose
+//              slots come back as soon as every epilogue thread has read its
+//              part into registers; results go to a separate, double-buffered
+//              output staging area that the bulk stores read from
 // The iterate X is held as two bf16 arrays, X = hi + lo (about 16 mantissa
 // bits): hi is the tensor-core operand, and the UPDATE epilogue rebuilds X
 // from both halves for the a*X term and splits the result the same way.
@@ -52,22 +55,20 @@ struct TcCfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr bool B_MN = UPD;
     static constexpr uint32_t IDESC = make_idesc_bf16(kBM, BN, B_MN);
-    // epilogue: column chunks staged in shared memory
+    // epilogue: column chunks; an input ring (TMA-loaded operands of the
+    // combine) and a double-buffered output staging area (read by TMA stores)
     static constexpr int CHUNK = UPD ? 32 : 64;          // columns per chunk
     static constexpr int NCHUNK = BN / CHUNK;
-    static constexpr int ESLOTS = (MODE == MODE_GRAM) ? 1 : (UPD ? 4 : 2);
     static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
-    static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // one bf16 half, 32 cols
-    static constexpr int EIN_BYTES = UPD ? 2 * HALF_BYTES : (HAS_EIN ? kBM * 64 * 2 : 0);  // X hi|lo / A
-    static constexpr int EOUT_BYTES = UPD ? 0 : kBM * 64 * 2;                           // UPDATE: in place
-    // mirrored bf16 out: its own buffer for GRAM; POLY reuses its input buffer
-    static constexpr int EMIR_BYTES = (MODE == MODE_GRAM) ? 64 * kBM * 2 : 0;
-    static constexpr int SLOT_BYTES = EIN_BYTES + EOUT_BYTES + EMIR_BYTES;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + ESLOTS * SLOT_BYTES + 1024 /*align*/ + 512;
+    static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // bf16 128 x 32
+    static constexpr int ISLOTS = UPD ? 3 : (HAS_EIN ? 1 : 0);
+    static constexpr int IN_BYTES = UPD ? 2 * HALF_BYTES : kBM * 64 * 2;              // X hi|lo / A chunk
+    static constexpr int OSLOTS = (MODE == MODE_GRAM) ? 1 : 2;
+    static constexpr int OUT_BYTES = UPD ? 2 * HALF_BYTES : 2 * kBM * 64 * 2;         // X' hi|lo / out|mirror
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + ISLOTS * IN_BYTES + OSLOTS * OUT_BYTES + 1024 /*align*/ + 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    // the loader gets a slot back only after the next chunk's store is issued,
-    // so a loaded epilogue input needs at least two slots to make progress
-    static_assert(!HAS_EIN || ESLOTS >= 2, "an epilogue with inputs needs two or more slots");
+    static_assert(!HAS_EIN || ISLOTS >= 1, "an epilogue with inputs needs an input slot");
 };
 
 // A 64-column chunk of a symmetric tile is live unless its 128-column block
@@ -91,14 +92,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * C::A_BYTES;
-    uint8_t* sE = sB + STAGES * C::B_BYTES;  // ESLOTS x {ein | eout | emir}
-    uint64_t* full = reinterpret_cast<uint64_t*>(sE + C::ESLOTS * C::SLOT_BYTES);
+    uint8_t* sI = sB + STAGES * C::B_BYTES;     // ISLOTS x IN_BYTES: epilogue inputs
+    uint8_t* sO = sI + C::ISLOTS * C::IN_BYTES;  // OSLOTS x OUT_BYTES: epilogue outputs
+    uint64_t* full = reinterpret_cast<uint64_t*>(sO + C::OSLOTS * C::OUT_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;      // [2] accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] accumulator drained
-    uint64_t* ein_full = tempty + 2;       // [ESLOTS] epilogue input landed
-    uint64_t* ein_empty = ein_full + C::ESLOTS;  // [ESLOTS] slot free for the loader
-    uint64_t* mma_done = ein_empty + C::ESLOTS;  // abort path only
+    uint64_t* ein_full = tempty + 2;       // [ISLOTS] epilogue input landed
+    uint64_t* ein_empty = ein_full + 4;    // [ISLOTS] input read by every epilogue thread
+    uint64_t* mma_done = ein_empty + 4;    // abort path only
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_go = abort_flag + 1;  // [2] epilogue verdicts, used in turn
@@ -115,9 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], kEpiThreads / 32);
         }
-        for (int s = 0; s < C::ESLOTS; ++s) {
+        for (int s = 0; s < C::ISLOTS; ++s) {
             mbar_init(&ein_full[s], 1);
-            mbar_init(&ein_empty[s], 1);
+            mbar_init(&ein_empty[s], kEpiThreads);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -252,10 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             }
             int slot = 0;
             uint32_t phase = 0;
-            uint32_t issued_phase[C::ESLOTS];
-            bool issued[C::ESLOTS];
+            uint32_t issued_phase[C::ISLOTS > 0 ? C::ISLOTS : 1];
+            bool issued[C::ISLOTS > 0 ? C::ISLOTS : 1];
 #pragma unroll
-            for (int s = 0; s < C::ESLOTS; ++s) issued[s] = false;
+            for (int s = 0; s < C::ISLOTS; ++s) issued[s] = false;
             bool ok = true;
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
                 const int4 tile = p.tiles[t];
@@ -266,15 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&ein_full[slot], C::EIN_BYTES);
-                    uint8_t* dst = sE + slot * C::SLOT_BYTES;
+                    mbar_arrive_expect_tx(&ein_full[slot], C::IN_BYTES);
+                    uint8_t* dst = sI + slot * C::IN_BYTES;
                     tma_load_3d(dst, &p.map_ein[g], &ein_full[slot], tj * BN + c * C::CHUNK, ti * kBM, idx);
                     if (C::UPD)
                         tma_load_3d(dst + C::HALF_BYTES, &p.map_ein2[g], &ein_full[slot], tj * BN + c * C::CHUNK,
                                     ti * kBM, idx);
                     issued[slot] = true;
                     issued_phase[slot] = phase;
-                    if (++slot == C::ESLOTS) {
+                    if (++slot == C::ISLOTS) {
                         slot = 0;
                         phase ^= 1u;
                     }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             }
             if (!ok) {
 #pragma unroll
-                for (int s = 0; s < C::ESLOTS; ++s)
+                for (int s = 0; s < C::ISLOTS; ++s)
                     if (issued[s]) mbar_wait_drain(&ein_full[s], issued_phase[s], 100000000ull);
             }
         }
@@ -296,9 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         const bool store_thread = threadIdx.x == kStoreThread;
         int acc = 0;
         uint32_t acc_phase = 0;
-        int slot = 0;
-        uint32_t ephase = 0;
-        int prev_slot = -1;  // store thread: slot whose bulk store is still being read
+        int islot = 0;       // input ring position
+        uint32_t iphase = 0;
+        int ochunk = 0;      // chunks staged so far (output buffer = ochunk % OSLOTS)
         int dec = 0;         // verdict counter (identical on all epilogue threads)
         // Every wait of the epilogue ends in one verdict for all epilogue threads: the
         // store thread publishes its own outcome (and any abort raised elsewhere),
@@ -330,35 +332,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             float sumsq = 0.f;
             for (int c = 0; c < C::NCHUNK; ++c) {
                 if (C::SYM && !sym_chunk_live(ti, tj, c)) continue;  // below the diagonal: nothing to do
-                uint8_t* ein = sE + slot * C::SLOT_BYTES;
-                uint8_t* eout = ein + C::EIN_BYTES;
-                uint8_t* emir = (MODE == MODE_POLY) ? ein : eout + C::EOUT_BYTES;
+                uint8_t* ein = sI + islot * C::IN_BYTES;
+                uint8_t* obuf = sO + (ochunk % C::OSLOTS) * C::OUT_BYTES;
                 const int col0 = tj * BN + c * C::CHUNK;
                 const bool mirror = C::SYM && (col0 >> 7) > ti;  // strictly above the diagonal block
-                bool go;
-                if (C::HAS_EIN) {
-                    go = decide(mbar_wait(&ein_full[slot], ephase, abort_flag, p.status));
-                } else {
-                    // the bulk store that last read this slot must be done before it is rewritten
-                    if (store_thread) bulk_wait_read<C::ESLOTS - 1>();
-                    go = decide(true);
-                }
-                if (!go) {
+                // the bulk store that last read this output buffer must be done with it
+                if (store_thread) bulk_wait_read<C::OSLOTS - 1>();
+                bool landed = true;
+                if (C::HAS_EIN) landed = mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
+                if (!decide(landed)) {
                     ok = false;
                     break;
                 }
                 if (MODE == MODE_UPDATE) {
                     float v[16];
                     tmem_load_32x16(t_acc + c * 32 + half * 16, v);
-                    uint8_t* hib = ein;                  // hi half, rows of 64 bytes, 64-byte swizzle
-                    uint8_t* lob = ein + C::HALF_BYTES;  // lo half, same layout
+                    // inputs: hi and lo halves of X, rows of 64 bytes, 64-byte swizzle
+                    uint4 hw[2], lw[2];
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
                         const uint32_t j = (uint32_t)(half * 2 + jj);
-                        const uint4 hw = *reinterpret_cast<const uint4*>(hib + sw64(r, j));
-                        const uint4 lw = *reinterpret_cast<const uint4*>(lob + sw64(r, j));
-                        const uint32_t hs[4] = {hw.x, hw.y, hw.z, hw.w};
-                        const uint32_t ls[4] = {lw.x, lw.y, lw.z, lw.w};
+                        hw[jj] = *reinterpret_cast<const uint4*>(ein + sw64(r, j));
+                        lw[jj] = *reinterpret_cast<const uint4*>(ein + C::HALF_BYTES + sw64(r, j));
+                    }
+                    mbar_arrive(&ein_empty[islot]);  // this thread is done with the input slot
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const uint32_t j = (uint32_t)(half * 2 + jj);
+                        const uint32_t hs[4] = {hw[jj].x, hw[jj].y, hw[jj].z, hw[jj].w};
+                        const uint32_t ls[4] = {lw[jj].x, lw[jj].y, lw[jj].z, lw[jj].w};
                         uint32_t ho[4], lo[4];
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
@@ -375,17 +377,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                                 sumsq = fmaf(o1, o1, sumsq);
                             }
                         }
-                        *reinterpret_cast<uint4*>(hib + sw64(r, j)) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-                        if (!p.last) *reinterpret_cast<uint4*>(lob + sw64(r, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        *reinterpret_cast<uint4*>(obuf + sw64(r, j)) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                        if (!p.last)
+                            *reinterpret_cast<uint4*>(obuf + C::HALF_BYTES + sw64(r, j)) =
+                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     }
                 } else {
                     float v[32];
                     tmem_load_32x32(t_acc + c * 64 + half * 32, v);
                     if (MODE == MODE_POLY) {
+                        uint4 aw[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            aw[jj] = *reinterpret_cast<const uint4*>(ein + sw128(r, (uint32_t)(half * 4 + jj)));
+                        mbar_arrive(&ein_empty[islot]);  // this thread is done with the input slot
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(ein + sw128(r, (uint32_t)(half * 4 + jj)));
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                            const uint32_t ws[4] = {aw[jj].x, aw[jj].y, aw[jj].z, aw[jj].w};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 const float lo = __uint_as_float(ws[h] << 16), hi = __uint_as_float(ws[h] & 0xFFFF0000u);
@@ -400,6 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     uint16_t b[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) b[e] = f2bf(v[e]);
+                    uint8_t* eout = obuf;                  // 128 x 64 bf16, 128-byte swizzle
+                    uint8_t* emir = obuf + kBM * 64 * 2;  // transposed chunk: two 64 x 64 boxes
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
                         uint4 w;
@@ -410,10 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         *reinterpret_cast<uint4*>(eout + sw128(r, (uint32_t)(half * 4 + jj))) = w;
                     }
                     if (mirror) {
-                        // POLY writes the mirror over its input chunk: every row must be read first
-                        if (MODE == MODE_POLY) named_barrier(1, kEpiThreads);
-                        // mirror: element (r, e) of this chunk goes to row e, column r of the
-                        // transposed chunk, stored as two 64 x 64 boxes (columns r / 64)
+                        // element (r, e) of this chunk goes to row e, column r of the transposed
+                        // chunk, stored as two 64 x 64 boxes (columns r / 64)
                         uint8_t* mbox = emir + (r >> 6) * (64 * 128);
                         const uint32_t rc = r & 63u;
 #pragma unroll
@@ -427,32 +435,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                 named_barrier(1, kEpiThreads);
                 if (store_thread) {
                     if (MODE == MODE_UPDATE) {
-                        const int x = tj * BN + c * C::CHUNK;
-                        if (x < G.n) {
-                            tma_store_3d(&p.map_out[g], ein, x, ti * kBM, idx);
-                            if (!p.last) tma_store_3d(&p.map_out2[g], ein + C::HALF_BYTES, x, ti * kBM, idx);
+                        if (col0 < G.n) {
+                            tma_store_3d(&p.map_out[g], obuf, col0, ti * kBM, idx);
+                            if (!p.last) tma_store_3d(&p.map_out2[g], obuf + C::HALF_BYTES, col0, ti * kBM, idx);
                         }
-                    } else {
-                        if (col0 < G.m) {
-                            tma_store_3d(&p.map_out[g], eout, col0, ti * kBM, idx);
-                            if (mirror) {
-                                tma_store_3d(&p.map_out2[g], emir, ti * kBM, col0, idx);
-                                if (ti * kBM + 64 < G.m)
-                                    tma_store_3d(&p.map_out2[g], emir + 64 * 128, ti * kBM + 64, col0, idx);
-                            }
+                    } else if (col0 < G.m) {
+                        tma_store_3d(&p.map_out[g], obuf, col0, ti * kBM, idx);
+                        if (mirror) {
+                            uint8_t* emir = obuf + kBM * 64 * 2;
+                            tma_store_3d(&p.map_out2[g], emir, ti * kBM, col0, idx);
+                            if (ti * kBM + 64 < G.m) tma_store_3d(&p.map_out2[g], emir + 64 * 128, ti * kBM + 64, col0, idx);
                         }
                     }
                     bulk_commit();
-                    if (C::HAS_EIN) {
-                        // hand the previous chunk's slot back to the loader once its store has read it
-                        bulk_wait_read<1>();
-                        if (prev_slot >= 0) mbar_arrive(&ein_empty[prev_slot]);
-                        prev_slot = slot;
-                    }
                 }
-                if (++slot == C::ESLOTS) {
-                    slot = 0;
-                    ephase ^= 1u;
+                ++ochunk;
+                if (C::HAS_EIN && ++islot == C::ISLOTS) {
+                    islot = 0;
+                    iphase ^= 1u;
                 }
             }
             if (!ok) break;
@@ -466,10 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if (store_thread) {
-            bulk_wait<0>();
-            if (C::HAS_EIN && prev_slot >= 0) mbar_arrive(&ein_empty[prev_slot]);
-        }
+        if (store_thread) bulk_wait<0>();
     }
 
     tc_fence_before();

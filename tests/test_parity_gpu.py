@@ -107,6 +107,10 @@ def test_per_iteration_coefficients_and_step_counts():
     errs.assert_within()
     errs, _, _ = run_parity(shapes, params, grads, ns_steps=1)
     errs.assert_within()
+    # a coefficient table whose middle iteration has no linear term (a = 0)
+    table0 = [(3.4445, -4.7750, 2.0315), (0.0, 1.2, -0.4), (2.0, -1.5, 0.5)]
+    errs, _, _ = run_parity(shapes, params, grads, ns_steps=3, ns_coeffs=table0)
+    errs.assert_within()
 
 
 def test_lr_schedule_through_device_scalars():
