@@ -33,8 +33,12 @@ from .muon_oracle import (
     shape_scale,
     write_back,
 )
+from .schedules import lr_multiplier, scheduled_lr, scheduled_momentum
 
 __all__ = [
+    "lr_multiplier",
+    "scheduled_lr",
+    "scheduled_momentum",
     "NS_COEFFS",
     "NORM_EPS",
     "V_FLOOR",
