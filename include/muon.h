@@ -127,14 +127,53 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
  * captured with).  The caller keeps the buffers alive until the work is done. */
 int muon_step(muon_handle h, float* const* params, const void* const* grads, void* stream);
 
-/* Zeroes the momentum and second-moment buffers on `stream` (the reset() the
- * FixMuonLR record adds to clear state dirtied by warm-up / graph capture). */
+/* Zeroes the momentum and second-moment buffers and the schedule's step
+ * counter on `stream` (the reset() the FixMuonLR record adds to clear state
+ * dirtied by warm-up / graph capture). */
 int muon_reset(muon_handle h, void* stream);
 
 /* Sets the device-resident scalars read by later steps (stream-ordered, so a
  * captured step graph follows schedule updates made between replays). */
 int muon_set_hparams(muon_handle h, float lr, float momentum, float beta2,
                      float weight_decay, void* stream);
+
+/* Step-indexed schedules evaluated on the device.
+ *
+ * Learning rate (FlexAttention record write-up, hyper-parameter table: a
+ * constant phase and a linear warmdown to 0; FixMuonLR write-up, change 3: a
+ * linear cool-down to an absolute floor that stays flat through the
+ * extension steps):  lr(s) = lr_base * m(s), with m(s) = 1 for
+ * s <= cooldown_start, lr_floor for s >= cooldown_end, and the straight line
+ * between them in between.
+ * Momentum (FlexAttention record write-up, section on the optimizer split):
+ * mu(s) = momentum_start + (momentum_end - momentum_start) * min(s / momentum_warmup, 1)
+ * (momentum_end throughout when momentum_warmup == 0).
+ * s counts steps from 0.  Layout: 40 bytes, offsets 0, 4, 8, 16, 24, 28, 32. */
+typedef struct {
+    float lr_base;           /* lr at multiplier 1 */
+    float lr_floor;          /* multiplier from cooldown_end on (0: decay to zero), >= 0 */
+    int64_t cooldown_start;  /* last step at multiplier 1 (>= -1) */
+    int64_t cooldown_end;    /* first step at lr_floor (> cooldown_start) */
+    float momentum_start;    /* mu at step 0 */
+    float momentum_end;      /* mu from step momentum_warmup on */
+    int64_t momentum_warmup; /* steps of linear warm-up (>= 0) */
+} muon_schedule;
+
+/* Installs `sched` (copied) and sets the device step counter to `start_step`
+ * (>= 0; e.g. when resuming), both stream-ordered on `stream`.  From then on
+ * every muon_step first runs one single-thread kernel that writes lr(s) and
+ * mu(s) into the device scalars (overriding muon_set_hparams for those two)
+ * and advances s, so a graph captured after this call follows the schedule on
+ * every replay with no host call.  sched == NULL removes the schedule (later
+ * steps launch no schedule kernel; graphs captured before keep theirs).
+ * muon_reset sets s back to 0.  MUON_ERR_ARG for a non-finite or negative
+ * lr_base / lr_floor, cooldown_end <= cooldown_start, cooldown_start < -1,
+ * momentum_warmup < 0 or start_step < 0. */
+int muon_set_schedule(muon_handle h, const muon_schedule* sched, int64_t start_step, void* stream);
+
+/* Synchronises `stream` and reads the device step counter: the schedule index
+ * the next muon_step will use (0 when no schedule was ever installed). */
+int muon_get_step(muon_handle h, int64_t* step, void* stream);
 
 /* Synchronises `stream`, reads and clears the device status word.
  * Returns MUON_OK, MUON_ERR_TIMEOUT, or MUON_ERR_CUDA. */

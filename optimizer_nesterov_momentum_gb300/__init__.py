@@ -126,6 +126,26 @@ class Muon:
                     stream=None) -> None:
         _abi.muon_set_hparams(self.handle, lr, momentum, beta2, weight_decay, _stream_ptr(stream))
 
+    def set_schedule(self, lr_base: float, cooldown_start: int, cooldown_end: int, lr_floor: float = 0.0,
+                     momentum_start: float = 0.95, momentum_end: float = 0.95, momentum_warmup: int = 0,
+                     start_step: int = 0, stream=None) -> None:
+        """Installs a device-side step schedule (see muon_set_schedule in include/muon.h).
+
+        Every later step writes lr(s) and mu(s) on the device before it runs,
+        so a CUDA graph captured afterwards follows the schedule by itself.
+        """
+        sc = _abi.muon_schedule(lr_base, lr_floor, cooldown_start, cooldown_end, momentum_start, momentum_end,
+                                momentum_warmup)
+        _abi.muon_set_schedule(self.handle, sc, start_step, _stream_ptr(stream))
+
+    def clear_schedule(self, start_step: int = 0, stream=None) -> None:
+        """Removes the step schedule; later steps use the muon_set_hparams scalars."""
+        _abi.muon_set_schedule(self.handle, None, start_step, _stream_ptr(stream))
+
+    def schedule_step(self, stream=None) -> int:
+        """Schedule index the next step will use (synchronises ``stream``)."""
+        return _abi.muon_get_step(self.handle, _stream_ptr(stream))
+
     def sync_status(self, stream=None) -> None:
         _abi.muon_sync_status(self.handle, _stream_ptr(stream))
 

@@ -48,6 +48,8 @@ EXPORTED = (
     "muon_step",
     "muon_reset",
     "muon_set_hparams",
+    "muon_set_schedule",
+    "muon_get_step",
     "muon_sync_status",
     "muon_destroy",
     "muon_error_string",
@@ -68,6 +70,18 @@ MUON_NOALLOC_MAX_TILES = 65536
 
 class muon_shape(ctypes.Structure):
     _fields_ = [("rows", c_int64), ("cols", c_int64), ("ld", c_int64), ("split", c_int32), ("flags", c_int32)]
+
+
+class muon_schedule(ctypes.Structure):
+    _fields_ = [
+        ("lr_base", c_float),
+        ("lr_floor", c_float),
+        ("cooldown_start", c_int64),
+        ("cooldown_end", c_int64),
+        ("momentum_start", c_float),
+        ("momentum_end", c_float),
+        ("momentum_warmup", c_int64),
+    ]
 
 
 class muon_config(ctypes.Structure):
@@ -168,6 +182,17 @@ def muon_reset(h, stream: int) -> None:
 
 def muon_set_hparams(h, lr, momentum, beta2, weight_decay, stream: int) -> None:
     _check(load_library().muon_set_hparams(h, lr, momentum, beta2, weight_decay, c_void_p(stream)), h)
+
+
+def muon_set_schedule(h, sched, start_step: int, stream: int) -> None:
+    ref = ctypes.byref(sched) if sched is not None else None
+    _check(load_library().muon_set_schedule(h, ref, c_int64(start_step), c_void_p(stream)), h)
+
+
+def muon_get_step(h, stream: int) -> int:
+    out = c_int64()
+    _check(load_library().muon_get_step(h, ctypes.byref(out), c_void_p(stream)), h)
+    return out.value
 
 
 def muon_sync_status(h, stream: int) -> int:

@@ -348,6 +348,27 @@ __global__ void k_set_hparams(float* hp, float lr, float mu, float beta2, float 
     hp[HP_WD] = wd;
 }
 
+// Installs a schedule (by value) and its starting step.
+__global__ void k_schedule_set(DevSchedule* dst, DevSchedule val) { *dst = val; }
+
+// Start of a scheduled step: lr and mu of step s into the device scalars, then
+// s <- s + 1.  Evaluated in double, stored as fp32.
+__global__ void k_schedule_advance(float* hp, DevSchedule* sc) {
+    const int64_t s = sc->step;
+    double mult;
+    if (s <= sc->cooldown_start)
+        mult = 1.0;
+    else if (s >= sc->cooldown_end)
+        mult = (double)sc->lr_floor;
+    else
+        mult = (double)sc->lr_floor + (1.0 - (double)sc->lr_floor) * ((double)(sc->cooldown_end - s) /
+                                                                      (double)(sc->cooldown_end - sc->cooldown_start));
+    const double frac = sc->momentum_warmup == 0 ? 1.0 : fmin((double)s / (double)sc->momentum_warmup, 1.0);
+    hp[HP_LR] = (float)((double)sc->lr_base * mult);
+    hp[HP_MU] = (float)((double)sc->momentum_start + ((double)sc->momentum_end - (double)sc->momentum_start) * frac);
+    sc->step = s + 1;
+}
+
 // ------------------------------------------------------------------ launchers
 template <int CAP>
 cudaError_t launch_momentum(const ElemParams<CAP>& p, bool grad_f32, cudaStream_t s) {
@@ -380,6 +401,16 @@ cudaError_t launch_lane_stats(const LaneParams& p, cudaStream_t s) {
 
 cudaError_t launch_set_hparams(float* hp, float lr, float mu, float beta2, float wd, cudaStream_t s) {
     k_set_hparams<<<1, 1, 0, s>>>(hp, lr, mu, beta2, wd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_schedule_set(DevSchedule* dst, const DevSchedule& val, cudaStream_t s) {
+    k_schedule_set<<<1, 1, 0, s>>>(dst, val);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_schedule_advance(float* hp, DevSchedule* sc, cudaStream_t s) {
+    k_schedule_advance<<<1, 1, 0, s>>>(hp, sc);
     return cudaGetLastError();
 }
 

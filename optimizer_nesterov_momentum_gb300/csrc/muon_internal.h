@@ -32,6 +32,13 @@ constexpr float kVFloor = 1e-10f;
 // device hyper-parameter slots (muon_set_hparams)
 enum { HP_LR = 0, HP_MU = 1, HP_BETA2 = 2, HP_WD = 3, HP_COUNT = 4 };
 
+// Device copy of a step schedule (see muon_schedule in muon.h) and its counter.
+struct DevSchedule {
+    int64_t step;             // schedule index of the next step
+    int64_t cooldown_start, cooldown_end, momentum_warmup;
+    float lr_base, lr_floor, momentum_start, momentum_end;
+};
+
 // bits of the device status word
 enum { STATUS_TIMEOUT = 1 };
 

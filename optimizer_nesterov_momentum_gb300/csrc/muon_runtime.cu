@@ -33,6 +33,8 @@ cudaError_t launch_apply(const ElemParams<CAP>&, cudaStream_t);
 cudaError_t launch_norm_scale(const NormParams&, cudaStream_t);
 cudaError_t launch_lane_stats(const LaneParams&, cudaStream_t);
 cudaError_t launch_set_hparams(float*, float, float, float, float, cudaStream_t);
+cudaError_t launch_schedule_set(DevSchedule*, const DevSchedule&, cudaStream_t);
+cudaError_t launch_schedule_advance(float*, DevSchedule*, cudaStream_t);
 cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
 template <int MODE>
@@ -104,6 +106,8 @@ struct muon_s {
     size_t arena_bytes = 0;
     float* hp = nullptr;
     int* status = nullptr;
+    DevSchedule* sched = nullptr;  // step schedule + counter (zero at create)
+    bool schedule_on = false;      // muon_step starts with the schedule kernel
     float* norm_scale = nullptr;
     float* norm_part = nullptr;
     float* momentum = nullptr;
@@ -218,10 +222,12 @@ cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* gra
 
 int launches_per_step(const muon_s* h) {
     // k_momentum, k_norm_scale, k_lane_stats, k_apply + the Newton-Schulz products
-    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) return 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps;
+    // (+ k_schedule_advance while a schedule is installed)
+    const int sched = h->schedule_on ? 1 : 0;
+    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) return sched + 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps;
     const int per_iter = 3 * (int)h->groups.size();
     const int rowsq = h->cfg.normuon ? (int)h->groups.size() : 0;  // extra pass after the last update
-    return 4 + per_iter * h->cfg.ns_steps + rowsq;
+    return sched + 4 + per_iter * h->cfg.ns_steps + rowsq;
 }
 
 cudaError_t mark(muon_s* h, int stage, cudaStream_t s) {
@@ -405,6 +411,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     const int nsubs = (int)pend.size();
     const size_t o_hp = take(sizeof(float) * HP_COUNT);
     const size_t o_status = take(sizeof(int));
+    const size_t o_sched = take(sizeof(DevSchedule));
     const size_t o_norm_scale = take(sizeof(float) * nsubs);
     // elementwise tiles
     std::vector<int4> elem_tiles;
@@ -505,6 +512,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     }
     h->hp = reinterpret_cast<float*>(base + o_hp);
     h->status = reinterpret_cast<int*>(base + o_status);
+    h->sched = reinterpret_cast<DevSchedule*>(base + o_sched);
     h->norm_scale = reinterpret_cast<float*>(base + o_norm_scale);
     h->norm_part = reinterpret_cast<float*>(base + o_norm_part);
     h->momentum = reinterpret_cast<float*>(base + o_mom);
@@ -702,6 +710,7 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
     MUON_CUDA(h, cudaSetDevice(h->device));
     h->n_recorded = 0;
     MUON_CUDA(h, mark(h, MUON_STAGE_MOMENTUM, s));
+    if (h->schedule_on) MUON_CUDA(h, launch_schedule_advance(h->hp, h->sched, s));
     MUON_CUDA(h, run_elem_any(h, params, grads, false, s));
     NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale};
     MUON_CUDA(h, mark(h, MUON_STAGE_NORM, s));
@@ -745,6 +754,48 @@ int muon_reset(muon_handle h, void* stream) {
     for (size_t i = 0; i < h->shapes.size(); ++i) mom_floats += round_up(h->shapes[i].rows * h->shapes[i].cols, 64);
     MUON_CUDA(h, cudaMemsetAsync(h->momentum, 0, sizeof(float) * (size_t)mom_floats, s));
     for (const Group& g : h->groups) MUON_CUDA(h, cudaMemsetAsync(g.v, 0, sizeof(float) * (size_t)g.count * g.m, s));
+    MUON_CUDA(h, cudaMemsetAsync(&h->sched->step, 0, sizeof(int64_t), s));
+    return MUON_OK;
+}
+
+int muon_set_schedule(muon_handle h, const muon_schedule* sched, int64_t start_step, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (start_step < 0) return fail(h, MUON_ERR_ARG, "start_step must be >= 0");
+    DevSchedule d;
+    memset(&d, 0, sizeof(d));
+    d.step = start_step;
+    if (sched) {
+        const muon_schedule& q = *sched;
+        if (!std::isfinite(q.lr_base) || q.lr_base < 0.f || !std::isfinite(q.lr_floor) || q.lr_floor < 0.f)
+            return fail(h, MUON_ERR_ARG, "lr_base and lr_floor must be finite and >= 0");
+        if (q.cooldown_start < -1 || q.cooldown_end <= q.cooldown_start)
+            return fail(h, MUON_ERR_ARG, "need -1 <= cooldown_start < cooldown_end");
+        if (q.momentum_warmup < 0) return fail(h, MUON_ERR_ARG, "momentum_warmup must be >= 0");
+        if (!std::isfinite(q.momentum_start) || !std::isfinite(q.momentum_end))
+            return fail(h, MUON_ERR_ARG, "momentum_start / momentum_end must be finite");
+        d.cooldown_start = q.cooldown_start;
+        d.cooldown_end = q.cooldown_end;
+        d.momentum_warmup = q.momentum_warmup;
+        d.lr_base = q.lr_base;
+        d.lr_floor = q.lr_floor;
+        d.momentum_start = q.momentum_start;
+        d.momentum_end = q.momentum_end;
+    }
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    MUON_CUDA(h, launch_schedule_set(h->sched, d, static_cast<cudaStream_t>(stream)));
+    h->schedule_on = sched != nullptr;
+    return MUON_OK;
+}
+
+int muon_get_step(muon_handle h, int64_t* step, void* stream) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (!step) return fail(h, MUON_ERR_ARG, "step is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_CUDA(h, cudaSetDevice(h->device));
+    MUON_CUDA(h, cudaStreamSynchronize(s));
+    MUON_CUDA(h, cudaMemcpy(step, &h->sched->step, sizeof(int64_t), cudaMemcpyDeviceToHost));
     return MUON_OK;
 }
 

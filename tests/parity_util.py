@@ -106,14 +106,17 @@ def run_parity(shapes: Sequence[Shape], params_cpu: List[torch.Tensor], grads_st
                *, lr=0.02, momentum=0.95, beta2=0.95, weight_decay=0.0, ns_steps=5, nesterov=True,
                lerp_form=True, normuon=True, grad_dtype="bf16", gemm_engine="tcgen05", ns_coeffs=None,
                ns_impl="iterate", check_parents: Optional[Sequence[int]] = None, opt=None,
-               lr_schedule: Optional[Sequence[float]] = None) -> Errors:
+               lr_schedule: Optional[Sequence[float]] = None, device_schedule: Optional[dict] = None) -> Errors:
     """Steps the GPU optimizer over ``grads_steps`` and compares every step.
 
     The oracle keeps its own momentum and second moment (they are compared
     end to end); the parameters are re-synced from the GPU before each step so
     that per-step updates are compared.  ``check_parents`` restricts the
     oracle to a sample of the parameters (each parameter is an independent
-    unit of the step).
+    unit of the step).  ``device_schedule`` (keyword arguments of
+    ``Muon.set_schedule``) installs a device-side step schedule; the oracle
+    then takes each step's lr and momentum from ``oracle.scheduled_lr`` /
+    ``oracle.scheduled_momentum``.
     """
     from optimizer_nesterov_momentum_gb300 import (MUON_STATE_MOMENTUM, MUON_STATE_ORTHO,
                                                    MUON_STATE_SECOND_MOMENT)
@@ -136,7 +139,16 @@ def run_parity(shapes: Sequence[Shape], params_cpu: List[torch.Tensor], grads_st
 
     params = [p.cuda() for p in params_cpu]
     errs = Errors()
+    if device_schedule is not None:
+        opt.set_schedule(**device_schedule)
     for step, grads_cpu in enumerate(grads_steps):
+        if device_schedule is not None:
+            d = device_schedule
+            s_idx = d.get("start_step", 0) + step
+            orc.cfg.lr = oracle.scheduled_lr(s_idx, d["lr_base"], d["cooldown_start"], d["cooldown_end"],
+                                             d.get("lr_floor", 0.0))
+            orc.cfg.momentum = oracle.scheduled_momentum(s_idx, d.get("momentum_start", 0.95),
+                                                         d.get("momentum_end", 0.95), d.get("momentum_warmup", 0))
         if lr_schedule is not None:
             opt.set_hparams(lr_schedule[step], momentum, beta2, weight_decay)
             orc.cfg.lr = lr_schedule[step]

@@ -43,6 +43,8 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(_abi.muon_shape) == 32
     assert _abi.muon_config.lr_mul.offset == 48
     assert ctypes.sizeof(_abi.muon_config) == 72
+    assert ctypes.sizeof(_abi.muon_schedule) == 40
+    assert [getattr(_abi.muon_schedule, f).offset for f, _ in _abi.muon_schedule._fields_] == [0, 4, 8, 16, 24, 28, 32]
 
 
 def test_config_default(lib):
@@ -106,6 +108,11 @@ def test_calls_on_invalid_handles(lib):
     bogus = ctypes.c_void_p(0x1234)
     assert lib.muon_step(bogus, None, None, None) == A.MUON_ERR_ARG
     assert lib.muon_sync_status(bogus, None) == A.MUON_ERR_ARG
+    sc = A.muon_schedule(0.03, 0.3, 10, 20, 0.85, 0.95, 5)
+    assert lib.muon_set_schedule(None, ctypes.byref(sc), ctypes.c_int64(0), None) == A.MUON_ERR_ARG
+    assert lib.muon_set_schedule(bogus, None, ctypes.c_int64(0), None) == A.MUON_ERR_ARG
+    step = ctypes.c_int64()
+    assert lib.muon_get_step(bogus, ctypes.byref(step), None) == A.MUON_ERR_ARG
     n = ctypes.c_int32()
     assert lib.muon_num_matrices(bogus, ctypes.byref(n)) == A.MUON_ERR_ARG
 

@@ -120,6 +120,85 @@ def test_lr_schedule_through_device_scalars():
     errs.assert_within()
 
 
+SCHED = dict(lr_base=0.03, cooldown_start=1, cooldown_end=4, lr_floor=0.3,
+             momentum_start=0.85, momentum_end=0.95, momentum_warmup=3)
+
+
+def test_device_schedule_cooldown_and_momentum_warmup():
+    """Six steps cross the whole cool-down and the momentum warm-up on the device."""
+    shapes = [Shape(128, 384), Shape(256, 256), Shape(384, 128, split=2)]
+    params, grads = _inputs(shapes, 6, seed=21)
+    errs, opt, _ = run_parity(shapes, params, grads, lr=0.5, momentum=0.5, device_schedule=SCHED)
+    errs.assert_within()
+    assert opt.schedule_step() == 6
+    # resuming mid-schedule: steps 2..4 only
+    params, grads = _inputs(shapes, 3, seed=22)
+    errs, opt, _ = run_parity(shapes, params, grads, device_schedule=dict(SCHED, start_step=2))
+    errs.assert_within()
+    assert opt.schedule_step() == 5
+
+
+def test_device_schedule_counter_reset_and_removal():
+    shapes = [Shape(64, 192)]
+    params, grads = _inputs(shapes, 1, seed=23)
+    opt = make_optimizer(shapes, lr=0.03)
+    base = opt.launch_count()
+    opt.set_schedule(**SCHED, start_step=7)
+    assert opt.launch_count() == base + 1
+    assert opt.schedule_step() == 7
+    p = [params[0].cuda()]
+    opt.step(p, [grads[0][0].cuda()])
+    assert opt.schedule_step() == 8
+    opt.reset()
+    assert opt.schedule_step() == 0
+    opt.clear_schedule(start_step=3)
+    assert opt.launch_count() == base
+    opt.step(p, [grads[0][0].cuda()])
+    assert opt.schedule_step() == 3  # no schedule kernel, counter untouched
+    from optimizer_nesterov_momentum_gb300 import MuonError
+    with pytest.raises(MuonError):
+        opt.set_schedule(0.03, cooldown_start=5, cooldown_end=5)
+    with pytest.raises(MuonError):
+        opt.set_schedule(0.03, cooldown_start=1, cooldown_end=4, momentum_warmup=-1)
+
+
+def test_device_schedule_followed_by_graph_replays():
+    """A graph captured once follows the schedule on every replay, bitwise like eager steps."""
+    shapes = [Shape(128, 384), Shape(384, 128), Shape(128, 512, split=4)]
+    params, grads = _inputs(shapes, 5, seed=24)
+    eager = make_optimizer(shapes, lr=0.5)
+    graphed = make_optimizer(shapes, lr=0.5)
+    eager.set_schedule(**SCHED)
+    graphed.set_schedule(**SCHED)
+    pe = [p.cuda() for p in params]
+    pg = [p.cuda() for p in params]
+    gbuf = [g.cuda() for g in grads[0]]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graphed.step(pg, gbuf)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        graphed.step(pg, gbuf)
+    graphed.reset()
+    for p, p0 in zip(pg, params):
+        p.copy_(p0.cuda())
+    for k in range(5):
+        for dst, src in zip(gbuf, grads[k]):
+            dst.copy_(src.cuda())
+        graph.replay()
+        eager.step(pe, gbuf)
+    torch.cuda.synchronize()
+    assert graphed.schedule_step() == 5 and eager.schedule_step() == 5
+    for a, b in zip(pe, pg):
+        assert torch.equal(a, b)
+    # and the eager run itself follows the oracle schedule
+    params2 = [p.clone() for p in params]
+    errs, _, _ = run_parity(shapes, params2, grads, device_schedule=SCHED)
+    errs.assert_within()
+
+
 def test_zero_gradient_keeps_params_and_is_finite():
     shapes = [Shape(64, 192), Shape(192, 64)]
     opt = make_optimizer(shapes, lr=0.03)
