@@ -34,8 +34,15 @@ from .muon_oracle import (
     write_back,
 )
 from .schedules import lr_multiplier, scheduled_lr, scheduled_momentum
+from .adam_oracle import ADAM_BETAS, ADAM_EPS, AdamConfig, AdamOracle, adam_moments, adam_param_update
 
 __all__ = [
+    "ADAM_BETAS",
+    "ADAM_EPS",
+    "AdamConfig",
+    "AdamOracle",
+    "adam_moments",
+    "adam_param_update",
     "lr_multiplier",
     "scheduled_lr",
     "scheduled_momentum",

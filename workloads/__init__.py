@@ -7,6 +7,7 @@ the CUDA path consume exactly the bits produced here.
 """
 
 from .shapes import MatrixShape, WORKLOADS, workload
+from .adam import ADAM_WORKLOADS, AdamTensor, AdamWorkload, adam_grads_for, adam_params_for, adam_workload
 from .generators import (
     lowrank_plus_noise,
     power_law_spectrum,
@@ -18,6 +19,12 @@ from .generators import (
 )
 
 __all__ = [
+    "ADAM_WORKLOADS",
+    "AdamTensor",
+    "AdamWorkload",
+    "adam_grads_for",
+    "adam_params_for",
+    "adam_workload",
     "MatrixShape",
     "WORKLOADS",
     "workload",
