@@ -56,6 +56,7 @@ def work_model(wl, grad_bytes):
     """Algorithmic flops / bytes of one step of workload ``wl``."""
     ns = wl.ns_steps
     gram = poly = upd = 0
+    gram_b = poly_b = upd_b = upd_last_b = 0
     elems = 0
     for (r, c) in wl.sub_shapes():
         m, n = min(r, c), max(r, c)
@@ -63,9 +64,16 @@ def work_model(wl, grad_bytes):
         poly += m * m * (m + 1)          # upper triangle of A A
         upd += 2 * m * m * n             # P X
         elems += r * c
+        # HBM bytes per launch: bf16 operands / results; the iterate is a hi + lo pair
+        gram_b += 2 * m * n + 2 * m * m            # read X hi, write A
+        poly_b += 2 * m * m + 2 * m * m            # read A, write P
+        upd_b += 2 * m * m + 4 * 2 * m * n         # read P, X hi, X lo; write X' hi, lo
+        upd_last_b += 2 * m * m + 3 * 2 * m * n    # last iteration writes no lo half
     return {
         "elems": elems,
         "gram_flops": gram, "poly_flops": poly, "update_flops": upd,
+        "gram_bytes": gram_b, "poly_bytes": poly_b,
+        "update_bytes": ((ns - 1) * upd_b + upd_last_b) / ns,   # mean per launch
         "ns_flops": ns * (gram + poly + upd),
         "ns_flops_dense": ns * sum(4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3 for r, c in wl.sub_shapes()),
         "momentum_bytes": elems * (grad_bytes + 4 + 4 + 2 + 2),   # g, buf r/w, u as bf16 hi + lo
@@ -197,6 +205,49 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------- our arm
 
+def adam_measure(args, dev, hbm):
+    """Graph-replayed fused Adam step on the GPT-2 embedding / head / scalar groups."""
+    import torch
+
+    from optimizer_nesterov_momentum_gb300 import AdamGroup, AdamTensorSpec
+    from workloads import adam_grads_for, adam_params_for, adam_workload
+
+    wl = adam_workload("gpt2-124m-adam")
+    grp = AdamGroup([AdamTensorSpec(t.numel, t.lr, t.weight_decay) for t in wl.tensors], grad_dtype=wl.grad_dtype)
+    params = [p.reshape(-1).to(dev) for p in adam_params_for(wl)]
+    bank = [[g.reshape(-1).to(dev) for g in adam_grads_for(wl, k)] for k in range(2)]
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            grp.step(params, bank[k % 2])
+    torch.cuda.current_stream().wait_stream(stream)
+    graphs = []
+    for k in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            grp.step(params, bank[k])
+        graphs.append(g)
+    for k in range(3):
+        graphs[k % 2].replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for k in range(args.steps):
+        graphs[k % 2].replay()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    nbytes = wl.numel * (2 + 3 * 4 + 3 * 4)   # g bf16; p, m, v read and written
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    launches = grp.launch_count()
+    grp.close()
+    return {"workload": wl.name, "description": wl.description, "elements": wl.numel, "ms": ms,
+            "bound": "hbm", "achieved": gbs, "unit": "GB/s", "peak": hbm, "frac": gbs / hbm,
+            "algorithmic_per_step": nbytes, "gpu_launches": launches * args.steps,
+            "launch": "cuda graph of muon_adam_step", "l2": "inputs larger than L2 (2.0 GB per step)"}
+
+
 def run_ours(args):
     import torch
 
@@ -323,11 +374,19 @@ def run_ours(args):
                      "achieved": model["apply_bytes"] / (stage_ms["apply"] * 1e-3) / 1e9, "unit": "GB/s",
                      "algorithmic_per_launch": model["apply_bytes"]}
     for name in ("gram", "poly", "update"):
+        # a product is bound by whichever of its flops (at the tensor peak) and its
+        # HBM bytes (at the copy peak) takes longer; both fractions are reported
         per_launch_ms = stage_ms[name] / nsi
-        flops = model[f"{name}_flops"]
-        kern[name] = {"ms": stage_ms[name], "ms_per_launch": per_launch_ms, "bound": "tensor",
-                      "achieved": flops / (per_launch_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                      "algorithmic_per_launch": flops}
+        flops, nbytes = model[f"{name}_flops"], model[f"{name}_bytes"]
+        tflops = flops / (per_launch_ms * 1e-3) / 1e12
+        gbs = nbytes / (per_launch_ms * 1e-3) / 1e9
+        hbm_bound = nbytes / hbm > flops / 1e3 / tc_peak
+        kern[name] = {"ms": stage_ms[name], "ms_per_launch": per_launch_ms,
+                      "bound": "hbm" if hbm_bound else "tensor",
+                      "achieved": gbs if hbm_bound else tflops, "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                      "algorithmic_per_launch": nbytes if hbm_bound else flops,
+                      "tflops": tflops, "frac_tensor": tflops / tc_peak,
+                      "gbs": gbs, "frac_hbm": gbs / hbm, "bytes_per_launch": nbytes, "flops_per_launch": flops}
     for name in ("norm_scale", "lane_stats"):
         kern[name] = {"ms": stage_ms[name]}
     for k, v in kern.items():
@@ -348,6 +407,8 @@ def run_ours(args):
                 "frac": d["frac"], "traffic": traffic, "kernel": dom,
                 "peak_source": f"{peak_src} ({'hbm_gbs' if d['unit'] == 'GB/s' else 'bf16_tflops_sustained'})",
                 "share_of_step": d["ms"] / total_stage}
+
+    adam = None if args.no_adam else adam_measure(args, dev, hbm)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -374,6 +435,7 @@ def run_ours(args):
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps,
             "clocks": clocks,
+            "next_rows": {"adam": adam},
         }
         print(json.dumps(line), flush=True)
     opt.close()
@@ -390,6 +452,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-adam", action="store_true", help="skip the Adam-group measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

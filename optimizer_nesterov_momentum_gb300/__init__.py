@@ -27,7 +27,10 @@ from ._abi import (  # noqa: F401  (re-exported names of the C ABI)
     load_library,
 )
 
-__all__ = ["Muon", "MatrixSpec", "MuonError", "load_library"]
+from .adam import MUON_ADAM_M, MUON_ADAM_V, AdamGroup, AdamTensorSpec  # noqa: E402
+
+__all__ = ["Muon", "MatrixSpec", "MuonError", "load_library", "AdamGroup", "AdamTensorSpec", "MUON_ADAM_M",
+           "MUON_ADAM_V"]
 
 
 @dataclass(frozen=True)

@@ -63,7 +63,23 @@ EXPORTED = (
     "muon_get_state",
     "muon_set_state",
     "muon_nesterov_normalize_noalloc",
+    # include/muon_adam.h
+    "muon_adam_config_default",
+    "muon_adam_create",
+    "muon_adam_step",
+    "muon_adam_reset",
+    "muon_adam_set_lr_scale",
+    "muon_adam_set_schedule",
+    "muon_adam_get_step",
+    "muon_adam_set_step",
+    "muon_adam_get_state",
+    "muon_adam_set_state",
+    "muon_adam_launch_count",
+    "muon_adam_last_error",
+    "muon_adam_destroy",
 )
+
+MUON_ADAM_MAX_TENSORS = 1024
 
 MUON_NOALLOC_MAX_TILES = 65536
 
@@ -82,6 +98,14 @@ class muon_schedule(ctypes.Structure):
         ("momentum_end", c_float),
         ("momentum_warmup", c_int64),
     ]
+
+
+class muon_adam_tensor(ctypes.Structure):
+    _fields_ = [("numel", c_int64), ("lr", c_float), ("weight_decay", c_float)]
+
+
+class muon_adam_config(ctypes.Structure):
+    _fields_ = [("beta1", c_float), ("beta2", c_float), ("eps", c_float), ("grad_dtype", c_int32)]
 
 
 class muon_config(ctypes.Structure):
@@ -138,6 +162,24 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_matrix_info.argtypes = [c_void_p, c_int32, POINTER(c_int64)]
     lib.muon_workspace_bytes.argtypes = [c_void_p, POINTER(c_int64)]
     lib.muon_launch_count.argtypes = [c_void_p, POINTER(c_int32)]
+    lib.muon_set_schedule.argtypes = [c_void_p, POINTER(muon_schedule), c_int64, c_void_p]
+    lib.muon_get_step.argtypes = [c_void_p, POINTER(c_int64), c_void_p]
+    lib.muon_adam_config_default.argtypes = [POINTER(muon_adam_config)]
+    lib.muon_adam_config_default.restype = None
+    lib.muon_adam_create.argtypes = [POINTER(muon_adam_tensor), c_int32, POINTER(muon_adam_config), c_int32,
+                                     POINTER(c_void_p)]
+    lib.muon_adam_step.argtypes = [c_void_p, POINTER(c_void_p), POINTER(c_void_p), c_void_p]
+    lib.muon_adam_reset.argtypes = [c_void_p, c_void_p]
+    lib.muon_adam_set_lr_scale.argtypes = [c_void_p, c_float, c_void_p]
+    lib.muon_adam_set_schedule.argtypes = [c_void_p, POINTER(muon_schedule), c_int64, c_void_p]
+    lib.muon_adam_get_step.argtypes = [c_void_p, POINTER(c_int64), c_void_p]
+    lib.muon_adam_set_step.argtypes = [c_void_p, c_int64, c_void_p]
+    lib.muon_adam_get_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.muon_adam_set_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.muon_adam_launch_count.argtypes = [c_void_p, POINTER(c_int32)]
+    lib.muon_adam_last_error.argtypes = [c_void_p]
+    lib.muon_adam_last_error.restype = c_char_p
+    lib.muon_adam_destroy.argtypes = [c_void_p]
     lib.muon_set_profiling.argtypes = [c_void_p, c_int32]
     lib.muon_get_stage_times.argtypes = [c_void_p, POINTER(c_float)]
     lib.muon_get_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
@@ -145,7 +187,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_nesterov_normalize_noalloc.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_int64,
                                                     c_float, c_int32, c_int32, c_void_p]
     for name in EXPORTED:
-        if name not in ("muon_config_default", "muon_error_string", "muon_last_error"):
+        if name not in ("muon_config_default", "muon_error_string", "muon_last_error", "muon_adam_config_default",
+                        "muon_adam_last_error"):
             getattr(lib, name).restype = c_int32
     _lib = lib
     return lib
@@ -261,3 +304,75 @@ def muon_nesterov_normalize_noalloc(grad_ptr: int, grad_dtype: int, momentum_ptr
         int(nesterov), c_void_p(stream))
     if rc < 0:
         raise MuonError(rc, muon_error_string(rc))
+
+
+# ---------------------------------------------------------------- include/muon_adam.h
+
+
+def _adam_check(rc: int, handle=None) -> int:
+    if rc < 0:
+        lib = load_library()
+        msg = lib.muon_adam_last_error(handle).decode() or lib.muon_error_string(rc).decode()
+        raise MuonError(rc, msg)
+    return rc
+
+
+def muon_adam_config_default() -> muon_adam_config:
+    cfg = muon_adam_config()
+    load_library().muon_adam_config_default(ctypes.byref(cfg))
+    return cfg
+
+
+def muon_adam_create(tensors, cfg: muon_adam_config, device: int):
+    arr = (muon_adam_tensor * len(tensors))(*tensors)
+    out = c_void_p()
+    _adam_check(load_library().muon_adam_create(arr, len(tensors), ctypes.byref(cfg), device, ctypes.byref(out)))
+    return out
+
+
+def muon_adam_step(h, params, grads, stream: int) -> None:
+    n = len(params)
+    pa = (c_void_p * n)(*params)
+    ga = (c_void_p * n)(*grads)
+    _adam_check(load_library().muon_adam_step(h, pa, ga, c_void_p(stream)), h)
+
+
+def muon_adam_reset(h, stream: int) -> None:
+    _adam_check(load_library().muon_adam_reset(h, c_void_p(stream)), h)
+
+
+def muon_adam_set_lr_scale(h, scale: float, stream: int) -> None:
+    _adam_check(load_library().muon_adam_set_lr_scale(h, scale, c_void_p(stream)), h)
+
+
+def muon_adam_set_schedule(h, sched, start_step: int, stream: int) -> None:
+    ref = ctypes.byref(sched) if sched is not None else None
+    _adam_check(load_library().muon_adam_set_schedule(h, ref, c_int64(start_step), c_void_p(stream)), h)
+
+
+def muon_adam_get_step(h, stream: int) -> int:
+    out = c_int64()
+    _adam_check(load_library().muon_adam_get_step(h, ctypes.byref(out), c_void_p(stream)), h)
+    return out.value
+
+
+def muon_adam_set_step(h, t: int, stream: int) -> None:
+    _adam_check(load_library().muon_adam_set_step(h, c_int64(t), c_void_p(stream)), h)
+
+
+def muon_adam_get_state(h, which: int, index: int, dst_ptr: int, stream: int) -> None:
+    _adam_check(load_library().muon_adam_get_state(h, which, index, c_void_p(dst_ptr), c_void_p(stream)), h)
+
+
+def muon_adam_set_state(h, which: int, index: int, src_ptr: int, stream: int) -> None:
+    _adam_check(load_library().muon_adam_set_state(h, which, index, c_void_p(src_ptr), c_void_p(stream)), h)
+
+
+def muon_adam_launch_count(h) -> int:
+    out = c_int32()
+    _adam_check(load_library().muon_adam_launch_count(h, ctypes.byref(out)), h)
+    return out.value
+
+
+def muon_adam_destroy(h) -> None:
+    _adam_check(load_library().muon_adam_destroy(h), h)

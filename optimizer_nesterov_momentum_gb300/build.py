@@ -41,7 +41,7 @@ def _needs_rebuild(objs):
     if not os.path.exists(LIB_PATH):
         return True
     lib_t = os.path.getmtime(LIB_PATH)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "muon.h")]
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
     return any(os.path.getmtime(d) > lib_t for d in deps)
 
 

@@ -29,7 +29,7 @@ Stochastic Optimization", Algorithm 1), with the step counter t starting at 1:
 from __future__ import annotations
 
 from dataclasses import dataclass
-from typing import List, Sequence
+from typing import List, Optional, Sequence
 
 import numpy as np
 
@@ -75,19 +75,24 @@ class AdamOracle:
         self.v = [np.zeros(n) for n in self.numels]
         self.t = 0
 
-    def step(self, params: Sequence[np.ndarray], grads: Sequence[np.ndarray], lrs: Sequence[float]) -> List[np.ndarray]:
+    def step(self, params: Sequence[np.ndarray], grads: Sequence[np.ndarray], lrs: Sequence[float],
+             weight_decays: Optional[Sequence[float]] = None) -> List[np.ndarray]:
         """One step for every tensor; ``lrs`` are the learning rates of this step.
 
-        Arrays are flattened; the new parameters are returned (inputs untouched).
+        ``weight_decays`` gives each tensor its own L2 coefficient (the
+        library Adam's per-group ``weight_decay``); by default every tensor
+        uses ``cfg.weight_decay``.  Arrays are flattened; the new parameters
+        are returned (inputs untouched).
         """
         c = self.cfg
         self.t += 1
         out = []
         for i, (p, g, lr) in enumerate(zip(params, grads, lrs)):
+            wd = c.weight_decay if weight_decays is None else float(weight_decays[i])
             p = np.asarray(p, dtype=np.float64).reshape(-1)
             g = np.asarray(g, dtype=np.float64).reshape(-1)
-            if c.weight_decay != 0.0:
-                g = g + c.weight_decay * p
+            if wd != 0.0:
+                g = g + wd * p
             self.m[i], self.v[i] = adam_moments(self.m[i], self.v[i], g, c.beta1, c.beta2)
             out.append(adam_param_update(p, self.m[i], self.v[i], self.t, lr, c.beta1, c.beta2, c.eps))
         return out

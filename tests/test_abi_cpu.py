@@ -1,5 +1,5 @@
 """The C-ABI library on the host: it loads, exports every entry point that
-include/muon.h declares, and rejects bad arguments before any device work.
+include/*.h declare, and rejects bad arguments before any device work.
 No kernel runs here (there is no GPU in the build container)."""
 
 import ctypes
@@ -20,8 +20,11 @@ def lib():
 
 
 def _declared_entry_points():
-    with open(os.path.join(ROOT, "include", "muon.h")) as f:
-        text = f.read()
+    text = ""
+    for name in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if name.endswith(".h"):
+            with open(os.path.join(ROOT, "include", name)) as f:
+                text += f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(muon_[a-z_]+)\s*\(", text)))
 
@@ -45,6 +48,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(_abi.muon_config) == 72
     assert ctypes.sizeof(_abi.muon_schedule) == 40
     assert [getattr(_abi.muon_schedule, f).offset for f, _ in _abi.muon_schedule._fields_] == [0, 4, 8, 16, 24, 28, 32]
+    assert ctypes.sizeof(_abi.muon_adam_tensor) == 16 and ctypes.sizeof(_abi.muon_adam_config) == 16
 
 
 def test_config_default(lib):
@@ -115,6 +119,33 @@ def test_calls_on_invalid_handles(lib):
     assert lib.muon_get_step(bogus, ctypes.byref(step), None) == A.MUON_ERR_ARG
     n = ctypes.c_int32()
     assert lib.muon_num_matrices(bogus, ctypes.byref(n)) == A.MUON_ERR_ARG
+
+
+def test_adam_rejects_bad_arguments_on_the_host(lib):
+    A = __import__("optimizer_nesterov_momentum_gb300._abi", fromlist=["x"])
+    cfg = A.muon_adam_config_default()
+    assert (cfg.beta1, cfg.beta2, cfg.grad_dtype) == (pytest.approx(0.9), pytest.approx(0.95), A.MUON_GRAD_BF16)
+    assert cfg.eps == pytest.approx(1e-8)
+    good = (A.muon_adam_tensor * 1)(A.muon_adam_tensor(10, 0.1, 0.0))
+    out = ctypes.c_void_p()
+    assert lib.muon_adam_create(good, 1, ctypes.byref(cfg), 0, None) == A.MUON_ERR_ARG
+    assert lib.muon_adam_create(good, 0, ctypes.byref(cfg), 0, ctypes.byref(out)) == A.MUON_ERR_ARG
+    assert lib.muon_adam_create(good, A.MUON_ADAM_MAX_TENSORS + 1, ctypes.byref(cfg), 0, ctypes.byref(out)) == A.MUON_ERR_ARG
+    bad = A.muon_adam_config_default()
+    bad.beta1 = 1.0
+    assert lib.muon_adam_create(good, 1, ctypes.byref(bad), 0, ctypes.byref(out)) == A.MUON_ERR_ARG
+    bad = A.muon_adam_config_default()
+    bad.grad_dtype = 7
+    assert lib.muon_adam_create(good, 1, ctypes.byref(bad), 0, ctypes.byref(out)) == A.MUON_ERR_ARG
+    for t in (A.muon_adam_tensor(0, 0.1, 0.0), A.muon_adam_tensor(4, -1.0, 0.0), A.muon_adam_tensor(4, float("nan"), 0.0)):
+        arr = (A.muon_adam_tensor * 1)(t)
+        assert lib.muon_adam_create(arr, 1, ctypes.byref(cfg), 0, ctypes.byref(out)) in (A.MUON_ERR_ARG, A.MUON_ERR_SHAPE)
+    assert lib.muon_adam_last_error(None).decode()
+    # no GPU here: a valid request fails at the device, loudly
+    assert lib.muon_adam_create(good, 1, ctypes.byref(cfg), 0, ctypes.byref(out)) == A.MUON_ERR_CUDA
+    assert lib.muon_adam_step(None, None, None, None) == A.MUON_ERR_ARG
+    assert lib.muon_adam_reset(ctypes.c_void_p(0x1234), None) == A.MUON_ERR_ARG
+    assert lib.muon_adam_destroy(None) == A.MUON_ERR_ARG
 
 
 def test_error_strings(lib):
