@@ -69,6 +69,7 @@ struct TcCfg {
         STAGES * STAGE_BYTES + ISLOTS * IN_BYTES + OSLOTS * OUT_BYTES + 1024 /*align*/ + 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(!HAS_EIN || ISLOTS >= 1, "an epilogue with inputs needs an input slot");
+    static_assert(OSLOTS >= 1 && OSLOTS <= 2, "two output-buffer mbarriers are reserved");
 };
 
 // A 64-column chunk of a symmetric tile is live unless its 128-column block
@@ -101,9 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
     uint64_t* ein_full = tempty + 2;       // [ISLOTS] epilogue input landed
     uint64_t* ein_empty = ein_full + 4;    // [ISLOTS] input read by every epilogue thread
     uint64_t* mma_done = ein_empty + 4;    // abort path only
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* obuf_free = mma_done + 1;    // [OSLOTS] output staging buffer read by its bulk store
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(obuf_free + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* s_go = abort_flag + 1;  // [2] epilogue verdicts, used in turn
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             mbar_init(&ein_empty[s], kEpiThreads);
         }
         mbar_init(mma_done, 1);
+        for (int b = 0; b < C::OSLOTS; ++b) mbar_init(&obuf_free[b], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -301,27 +303,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         int islot = 0;       // input ring position
         uint32_t iphase = 0;
         int ochunk = 0;      // chunks staged so far (output buffer = ochunk % OSLOTS)
-        int dec = 0;         // verdict counter (identical on all epilogue threads)
-        // Every wait of the epilogue ends in one verdict for all epilogue threads: the
-        // store thread publishes its own outcome (and any abort raised elsewhere),
-        // a named barrier orders it, everyone reads the same flag.
-        auto decide = [&](bool mine) -> bool {
-            if (store_thread) s_go[dec & 1] = (mine && !*abort_flag) ? 1 : 0;
-            named_barrier(1, kEpiThreads);
-            const bool go = s_go[dec & 1] != 0;
-            ++dec;
-            return go;
-        };
-        bool ok = true;
-        for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+        // The epilogue never leaves its loops early: after an abort every wait returns
+        // at once and the remaining tiles run through on scratch data, so all epilogue
+        // threads always meet at the same named barriers.  Each thread waits on the
+        // mbarriers itself; the one barrier per chunk orders the staging writes before
+        // the store thread's bulk stores.
+        for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
             const int4 tile = p.tiles[t];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
-            const bool got = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
-            if (!decide(got)) {
-                ok = false;
-                break;
-            }
+            mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
             tc_fence_after();
             const uint32_t t_acc = tmem_base + lane_off + (uint32_t)(acc * BN);
             float scale = 1.f;
@@ -333,21 +324,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             for (int c = 0; c < C::NCHUNK; ++c) {
                 if (C::SYM && !sym_chunk_live(ti, tj, c)) continue;  // below the diagonal: nothing to do
                 uint8_t* ein = sI + islot * C::IN_BYTES;
-                uint8_t* obuf = sO + (ochunk % C::OSLOTS) * C::OUT_BYTES;
+                const int ob = ochunk % C::OSLOTS;
+                uint8_t* obuf = sO + ob * C::OUT_BYTES;
                 const int col0 = tj * BN + c * C::CHUNK;
                 const bool mirror = C::SYM && (col0 >> 7) > ti;  // strictly above the diagonal block
                 // the bulk store that last read this output buffer must be done with it
-                if (store_thread) bulk_wait_read<C::OSLOTS - 1>();
-                bool landed = true;
-                if (C::HAS_EIN) landed = mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
-                if (!decide(landed)) {
-                    ok = false;
-                    break;
-                }
+                auto wait_obuf = [&]() {
+                    if (ochunk >= C::OSLOTS)
+                        mbar_wait(&obuf_free[ob], (uint32_t)((ochunk / C::OSLOTS - 1) & 1), abort_flag, p.status);
+                };
                 if (MODE == MODE_UPDATE) {
                     float v[16];
                     tmem_load_32x16(t_acc + c * 32 + half * 16, v);
                     // inputs: hi and lo halves of X, rows of 64 bytes, 64-byte swizzle
+                    mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
                     uint4 hw[2], lw[2];
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
@@ -356,12 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         lw[jj] = *reinterpret_cast<const uint4*>(ein + C::HALF_BYTES + sw64(r, j));
                     }
                     mbar_arrive(&ein_empty[islot]);  // this thread is done with the input slot
+                    uint32_t ho[2][4], lo[2][4];
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
-                        const uint32_t j = (uint32_t)(half * 2 + jj);
                         const uint32_t hs[4] = {hw[jj].x, hw[jj].y, hw[jj].z, hw[jj].w};
                         const uint32_t ls[4] = {lw[jj].x, lw[jj].y, lw[jj].z, lw[jj].w};
-                        uint32_t ho[4], lo[4];
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
                             const float x0 = __uint_as_float(hs[h] << 16) + __uint_as_float(ls[h] << 16);
@@ -369,23 +358,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                             const float y0 = scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]);
                             const float y1 = scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]);
                             const uint16_t b0 = f2bf(y0), b1 = f2bf(y1);
-                            ho[h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-                            lo[h] = pack_bf2(y0 - bf2f(b0), y1 - bf2f(b1));
+                            ho[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                            lo[jj][h] = pack_bf2(y0 - bf2f(b0), y1 - bf2f(b1));
                             if (p.want_rowsq) {
                                 const float o0 = bf2f(b0), o1 = bf2f(b1);
                                 sumsq = fmaf(o0, o0, sumsq);
                                 sumsq = fmaf(o1, o1, sumsq);
                             }
                         }
-                        *reinterpret_cast<uint4*>(obuf + sw64(r, j)) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                    }
+                    wait_obuf();
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const uint32_t j = (uint32_t)(half * 2 + jj);
+                        *reinterpret_cast<uint4*>(obuf + sw64(r, j)) = make_uint4(ho[jj][0], ho[jj][1], ho[jj][2], ho[jj][3]);
                         if (!p.last)
                             *reinterpret_cast<uint4*>(obuf + C::HALF_BYTES + sw64(r, j)) =
-                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                                make_uint4(lo[jj][0], lo[jj][1], lo[jj][2], lo[jj][3]);
                     }
                 } else {
                     float v[32];
                     tmem_load_32x32(t_acc + c * 64 + half * 32, v);
                     if (MODE == MODE_POLY) {
+                        mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
                         uint4 aw[4];
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj)
@@ -408,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     uint16_t b[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) b[e] = f2bf(v[e]);
+                    wait_obuf();
                     uint8_t* eout = obuf;                  // 128 x 64 bf16, 128-byte swizzle
                     uint8_t* emir = obuf + kBM * 64 * 2;  // transposed chunk: two 64 x 64 boxes
 #pragma unroll
@@ -448,6 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         }
                     }
                     bulk_commit();
+                    // once the store of chunk ochunk - (OSLOTS - 1) has read its buffer, chunk
+                    // ochunk + 1 (which uses that buffer) may be staged
+                    if (ochunk >= C::OSLOTS - 1) {
+                        bulk_wait_read<C::OSLOTS - 1>();
+                        mbar_arrive(&obuf_free[(ochunk - (C::OSLOTS - 1)) % C::OSLOTS]);
+                    }
                 }
                 ++ochunk;
                 if (C::HAS_EIN && ++islot == C::ISLOTS) {
@@ -455,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     iphase ^= 1u;
                 }
             }
-            if (!ok) break;
             if (MODE == MODE_UPDATE && p.want_rowsq) {
                 const int row = ti * kBM + (int)r;
                 if (row < G.m) G.rowsq[(((int64_t)idx * G.m + row) * G.ntile_n + tj) * 2 + half] = sumsq;
