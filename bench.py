@@ -56,7 +56,7 @@ def work_model(wl, grad_bytes):
     """Algorithmic flops / bytes of one step of workload ``wl``."""
     ns = wl.ns_steps
     gram = poly = upd = 0
-    gram_b = poly_b = upd_b = upd_last_b = 0
+    gram_b = poly_b = upd_first_b = upd_b = 0
     elems = 0
     for (r, c) in wl.sub_shapes():
         m, n = min(r, c), max(r, c)
@@ -64,16 +64,17 @@ def work_model(wl, grad_bytes):
         poly += m * m * (m + 1)          # upper triangle of A A
         upd += 2 * m * m * n             # P X
         elems += r * c
-        # HBM bytes per launch: bf16 operands / results; the iterate is a hi + lo pair
-        gram_b += 2 * m * n + 2 * m * m            # read X hi, write A
+        # HBM bytes per launch (2-byte elements): the first iteration works on u
+        # (bf16 hi + lo), later ones on the fp16 iterate
+        gram_b += 2 * m * n + 2 * m * m            # read X (u hi), write A
         poly_b += 2 * m * m + 2 * m * m            # read A, write P
-        upd_b += 2 * m * m + 4 * 2 * m * n         # read P, X hi, X lo; write X' hi, lo
-        upd_last_b += 2 * m * m + 3 * 2 * m * n    # last iteration writes no lo half
+        upd_first_b += 2 * m * m + 3 * 2 * m * n   # read P, u hi, u lo; write X1
+        upd_b += 2 * m * m + 2 * 2 * m * n         # read P, X; write X' 
     return {
         "elems": elems,
         "gram_flops": gram, "poly_flops": poly, "update_flops": upd,
         "gram_bytes": gram_b, "poly_bytes": poly_b,
-        "update_bytes": ((ns - 1) * upd_b + upd_last_b) / ns,   # mean per launch
+        "update_bytes": (upd_first_b + (ns - 1) * upd_b) / ns,   # mean per launch
         "ns_flops": ns * (gram + poly + upd),
         "ns_flops_dense": ns * sum(4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3 for r, c in wl.sub_shapes()),
         "momentum_bytes": elems * (grad_bytes + 4 + 4 + 2 + 2),   # g, buf r/w, u as bf16 hi + lo

@@ -99,13 +99,14 @@ __device__ __forceinline__ void store1_hilo(uint16_t* hi, uint16_t* lo, float v)
     *lo = f2bf(v - bf2f(h));
 }
 
-__device__ __forceinline__ void load8_bf16(const uint16_t* src, float (&v)[8]) {
+// eight fp16 values (the Newton-Schulz output O)
+__device__ __forceinline__ void load8_f16(const uint16_t* src, float (&v)[8]) {
     const uint4 w = *reinterpret_cast<const uint4*>(src);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-        v[2 * h] = __uint_as_float(ws[h] << 16);
-        v[2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+        v[2 * h] = h2f((uint16_t)(ws[h] & 0xFFFFu));
+        v[2 * h + 1] = h2f((uint16_t)(ws[h] >> 16));
     }
 }
 
@@ -265,9 +266,9 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
             if (!d.transposed) {
                 const uint16_t* src = d.o16 + (int64_t)r * d.ldx + c;
                 if (d.vec)
-                    load8_bf16(src, o[pass]);
+                    load8_f16(src, o[pass]);
                 else
-                    for (int e = 0; e < 8 && c + e < d.cols; ++e) o[pass][e] = bf2f(src[e]);
+                    for (int e = 0; e < 8 && c + e < d.cols; ++e) o[pass][e] = h2f(src[e]);
             }
         }
     }
@@ -284,9 +285,9 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
             if (wr < d.cols && wc < d.rows) {
                 const uint16_t* src = d.o16 + (int64_t)wr * d.ldx + wc;
                 if (wc + 8 <= d.rows)
-                    load8_bf16(src, v);
+                    load8_f16(src, v);
                 else
-                    for (int e = 0; e < 8 && wc + e < d.rows; ++e) v[e] = bf2f(src[e]);
+                    for (int e = 0; e < 8 && wc + e < d.rows; ++e) v[e] = h2f(src[e]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) so[i][tc * 8 + e] = v[e];

@@ -4,9 +4,10 @@
 //   * momentum arena: one dense fp32 [rows x cols] block per parameter (S1).
 //   * per split matrix ("sub"), in the wide orientation m x n (m <= n):
 //       u16 / ulo16 Nesterov direction as a pair of bf16 arrays, u = hi + lo (S2)
-//       x16 / xlo16 Newton-Schulz iterate as hi + lo; the hi half is the
-//                   tensor-core operand; two buffers used in turn (S5-S7)
-//       a16 / p16   A = X X^T and P = b A + c A A, bf16, m x m (S5, S6)
+//       x16         Newton-Schulz iterate after the first iteration, fp16 (the
+//                   tensor-core operand); two buffers used in turn (S5-S7)
+//       a16 / p16   A = X X^T and P = b A + c A A, m x m: bf16 in the first
+//                   iteration (on u), fp16 after (S5, S6)
 //       rowsq       per (row, 256-column tile, column half) sums of O^2 from the
 //                   last iteration (S8)
 //       v           second moment, fp32 [m] (S8)
@@ -62,7 +63,7 @@ struct SubDesc {
     // wide-orientation arenas of this sub
     uint16_t* u16;        // hi half of u (bf16(u))
     uint16_t* ulo16;      // lo half of u (bf16(u - hi))
-    const uint16_t* o16;  // final Newton-Schulz output (bf16), m x n, row stride ldx
+    const uint16_t* o16;  // final Newton-Schulz output (fp16), m x n, row stride ldx
     float* rowsq;         // m x ntile_n x 2
     float* v;             // m
     float* lane;          // m
@@ -93,9 +94,9 @@ struct GemmGroup {
     int32_t sub0;            // sub index of the group's first matrix (subs are group-ordered)
     int64_t x_stride;        // elements between matrices in x / u arenas (m * ldx)
     int64_t a_stride;        // elements between matrices in a / p arenas (m * lda)
-    const uint16_t* xlo_in;  // update: lo half of the iterate read by the a*X term (hi: opr16)
-    uint16_t* xlo_out;       // update: lo half of the next iterate (nullptr on the last iteration)
-    uint16_t* x16_out;       // update: hi half of the next iterate / final O
+    const uint16_t* xlo_in;  // first update: lo half of u read by the a*X term (hi: opr16); else nullptr
+    uint16_t* xlo_out;       // unused (kept zero)
+    uint16_t* x16_out;       // update: the next iterate / final O (fp16)
     const uint16_t* a16;     // poly epilogue: A (also simt operand)
     uint16_t* out16;         // gram: A, poly: P
     float* rowsq;            // update, last iteration: per-row sums of O^2 (m * ntile_n * 2 per matrix)
@@ -117,6 +118,7 @@ struct GemmParams {
     const float* norm_scale; // s per sub (first iteration), else nullptr
     float ca, cb, cc;        // (a, b, c) of this iteration
     int32_t first, last, want_rowsq;
+    int32_t f16;             // operands and results fp16 (iterations after the first); else bf16
     int* status;
 };
 

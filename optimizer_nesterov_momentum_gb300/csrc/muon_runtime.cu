@@ -37,7 +37,7 @@ cudaError_t launch_schedule_set(DevSchedule*, const DevSchedule&, cudaStream_t);
 cudaError_t launch_schedule_advance(float*, DevSchedule*, cudaStream_t);
 cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
-template <int MODE>
+template <int MODE, bool F16>
 cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
 template <int MODE>
 cudaError_t launch_ns_gemm_simt(const GemmParams&, int, int, cudaStream_t);
@@ -62,7 +62,6 @@ struct Group {
     uint16_t* u16 = nullptr;
     uint16_t* ulo16 = nullptr;
     uint16_t* x16[2] = {nullptr, nullptr};
-    uint16_t* xlo16[2] = {nullptr, nullptr};
     uint16_t* a16 = nullptr;
     uint16_t* p16 = nullptr;
     float* rowsq = nullptr;
@@ -71,7 +70,7 @@ struct Group {
     // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), 32 x 128 boxes of
     // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
-    CUtensorMap map_u_hi, map_u_lo, map_x_hi[2], map_x_lo[2], map_a_mir, map_p_mir;
+    CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
@@ -430,7 +429,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->n_elem_tiles = (int32_t)elem_tiles.size();
     const size_t o_norm_part = take(sizeof(float) * elem_tiles.size());
     const size_t o_mom = take(sizeof(float) * (size_t)mom_total);
-    std::vector<size_t> go_ulo, go_u16, go_xlo[2], go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane;
+    std::vector<size_t> go_ulo, go_u16, go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane;
     for (auto& g : h->groups) g.count = 0;
     for (int sidx = 0; sidx < nsubs; ++sidx) h->groups[sub_group[order[sidx]]].count++;
     {
@@ -445,7 +444,6 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         go_ulo.push_back(take(xe * 2));
         go_u16.push_back(take(xe * 2));
         for (int b = 0; b < 2; ++b) {
-            go_xlo[b].push_back(take(xe * 2));
             go_x16[b].push_back(take(xe * 2));
         }
         go_a16.push_back(take(ae * 2));
@@ -524,7 +522,6 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         g.ulo16 = reinterpret_cast<uint16_t*>(base + go_ulo[gi]);
         g.u16 = reinterpret_cast<uint16_t*>(base + go_u16[gi]);
         for (int b = 0; b < 2; ++b) {
-            g.xlo16[b] = reinterpret_cast<uint16_t*>(base + go_xlo[b][gi]);
             g.x16[b] = reinterpret_cast<uint16_t*>(base + go_x16[b][gi]);
         }
         g.a16 = reinterpret_cast<uint16_t*>(base + go_a16[gi]);
@@ -539,9 +536,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         for (int b = 0; b < 2 && ok; ++b)
             ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
                  encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64) &&
-                 encode_3d(enc, &g.map_x_hi[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
-                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
-                 encode_3d(enc, &g.map_x_lo[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.xlo16[b], g.n, g.m, g.count,
+                 encode_3d(enc, &g.map_x_o32[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
                            g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_u_hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32, kBM,
@@ -628,6 +623,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 gp.cc = h->coeffs[3 * it + 2];
                 gp.first = first;
                 gp.last = last;
+                gp.f16 = it > 0;
                 gp.want_rowsq = last && cfg.normuon;
                 gp.status = h->status;
                 if (mode == MODE_GRAM) {
@@ -652,8 +648,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     G.x_stride = (int64_t)g.m * g.ldx;
                     G.a_stride = (int64_t)g.m * g.lda;
                     const uint16_t* xin16 = first ? g.u16 : g.x16[in_buf];
-                    G.xlo_in = first ? g.ulo16 : g.xlo16[in_buf];
-                    G.xlo_out = last ? nullptr : g.xlo16[out_buf];
+                    G.xlo_in = first ? g.ulo16 : nullptr;  // the first update reads u as hi + lo
                     G.x16_out = g.x16[out_buf];
                     G.a16 = g.a16;
                     G.rowsq = g.rowsq;
@@ -675,10 +670,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     } else {
                         gp.map_a[sl] = g.map_p_k;
                         gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
-                        gp.map_ein[sl] = first ? g.map_u_hi : g.map_x_hi[in_buf];
-                        gp.map_ein2[sl] = first ? g.map_u_lo : g.map_x_lo[in_buf];
-                        gp.map_out[sl] = g.map_x_hi[out_buf];
-                        gp.map_out2[sl] = g.map_x_lo[out_buf];
+                        // first update: u hi | lo in 32-column boxes, X1 out in 32-column boxes;
+                        // later updates: the fp16 iterate in and out in 64-column boxes
+                        gp.map_ein[sl] = first ? g.map_u_hi : g.map_x_k[in_buf];
+                        gp.map_ein2[sl] = g.map_u_lo;
+                        gp.map_out[sl] = first ? g.map_x_o32[out_buf] : g.map_x_k[out_buf];
                         G.opl16 = g.p16;
                         G.opr16 = xin16;
                     }
@@ -722,9 +718,19 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                 const GemmParams& gp = h->gparams[((size_t)it * nch + c) * 3 + mode];
                 MUON_CUDA(h, mark(h, MUON_STAGE_GRAM + mode, s));
                 if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
-                    if (mode == MODE_GRAM) MUON_CUDA(h, launch_ns_gemm_tc<MODE_GRAM>(gp, h->num_sms, s));
-                    if (mode == MODE_POLY) MUON_CUDA(h, launch_ns_gemm_tc<MODE_POLY>(gp, h->num_sms, s));
-                    if (mode == MODE_UPDATE) MUON_CUDA(h, launch_ns_gemm_tc<MODE_UPDATE>(gp, h->num_sms, s));
+                    // the first iteration works on bf16 u; later ones on the fp16 iterate
+                    const bool f16 = it > 0;
+                    cudaError_t e = cudaSuccess;
+                    if (mode == MODE_GRAM)
+                        e = f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, s)
+                                : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, s);
+                    if (mode == MODE_POLY)
+                        e = f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
+                                : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s);
+                    if (mode == MODE_UPDATE)
+                        e = f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
+                                : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s);
+                    MUON_CUDA(h, e);
                 } else {
                     for (int sl = 0; sl < gp.ngroups; ++sl) {
                         const int cnt = h->groups[h->chunks[c].g0 + sl].count;

@@ -25,6 +25,9 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
     const uint16_t* L = G.opl16 + (int64_t)idx * ((MODE == MODE_GRAM) ? G.x_stride : G.a_stride);
     const uint16_t* R = G.opr16 + (int64_t)idx * ((MODE == MODE_POLY) ? G.a_stride : G.x_stride);
 
+    // operands: bf16 in the first iteration, fp16 after
+    auto dec = [&](uint16_t b) { return p.f16 ? h2f(b) : bf2f(b); };
+    auto enc = [&](float x) { return p.f16 ? f2h(x) : f2bf(x); };
     __shared__ float sl[16][65];
     __shared__ float sr[16][65];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -33,14 +36,14 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
         for (int e = threadIdx.x; e < 16 * 64; e += 256) {
             const int kk = e & 15, ii = e >> 4;
             const int i = ti * 64 + ii, k = k0 + kk;
-            sl[kk][ii] = (i < M && k < K) ? bf2f(L[(int64_t)i * ldl + k]) : 0.f;
+            sl[kk][ii] = (i < M && k < K) ? dec(L[(int64_t)i * ldl + k]) : 0.f;
             const int j = tj * 64 + ii;
             float r = 0.f;
             if (j < N && k < K) {
                 if (MODE == MODE_GRAM)
-                    r = bf2f(R[(int64_t)j * ldr + k]);  // X^T[k][j] = X[j][k]
+                    r = dec(R[(int64_t)j * ldr + k]);  // X^T[k][j] = X[j][k]
                 else
-                    r = bf2f(R[(int64_t)k * ldr + j]);  // A[k][j] (poly), X[k][j] (update)
+                    r = dec(R[(int64_t)k * ldr + j]);  // A[k][j] (poly), X[k][j] (update)
             }
             sr[kk][ii] = r;
         }
@@ -71,17 +74,16 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
             const int j = tj * 64 + tx * 4 + c;
             if (j >= N) continue;
             if (MODE == MODE_GRAM) {
-                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = f2bf(acc[r][c] * (s * s));
+                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(acc[r][c] * (s * s));
             } else if (MODE == MODE_POLY) {
-                const float a = bf2f(G.a16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j]);
-                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = f2bf(fmaf(p.cb, a, p.cc * acc[r][c]));
+                const float a = dec(G.a16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j]);
+                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(fmaf(p.cb, a, p.cc * acc[r][c]));
             } else {
                 const int64_t off = (int64_t)idx * G.x_stride + (int64_t)i * G.ldx + j;
-                const float x = bf2f(R[(int64_t)i * ldr + j]) + bf2f(G.xlo_in[off]);  // hi + lo
-                const float y = s * fmaf(p.ca, x, acc[r][c]);
-                const uint16_t hi = f2bf(y);
-                G.x16_out[off] = hi;
-                if (G.xlo_out) G.xlo_out[off] = f2bf(y - bf2f(hi));
+                // the first update reads u as hi + lo (bf16); later ones the fp16 iterate
+                const float x = p.f16 ? h2f(R[(int64_t)i * ldr + j])
+                                      : bf2f(R[(int64_t)i * ldr + j]) + bf2f(G.xlo_in[off]);
+                G.x16_out[off] = f2h(s * fmaf(p.ca, x, acc[r][c]));  // the next iterate is fp16
             }
         }
     }
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(256) k_rowsq_simt(const __grid_constant__ Gemm
     const uint16_t* o = G.x16_out + (int64_t)idx * G.x_stride + (int64_t)row * G.ldx;
     float s = 0.f;
     for (int j = t * kBNUpd; j < min(G.n, (t + 1) * kBNUpd); ++j) {
-        const float v = bf2f(o[j]);
+        const float v = h2f(o[j]);  // O is fp16
         s = fmaf(v, v, s);
     }
     float* out = G.rowsq + (((int64_t)idx * G.m + row) * G.ntile_n + t) * 2;  // (row, tile, half) layout

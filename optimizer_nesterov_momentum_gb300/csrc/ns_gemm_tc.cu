@@ -43,7 +43,9 @@
 
 namespace muon {
 
-template <int MODE>
+// F16: operands and results in fp16 (the iterations after the first); otherwise
+// bf16 operands (the first iteration, on the Nesterov direction u).
+template <int MODE, bool F16>
 struct TcCfg {
     static constexpr bool UPD = (MODE == MODE_UPDATE);
     static constexpr bool SYM = !UPD;
@@ -54,17 +56,20 @@ struct TcCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr bool B_MN = UPD;
-    static constexpr uint32_t IDESC = make_idesc_bf16(kBM, BN, B_MN);
+    static constexpr uint32_t IDESC = make_idesc_16bit(kBM, BN, B_MN, F16);
     // epilogue: column chunks; an input ring (TMA-loaded operands of the
-    // combine) and a double-buffered output staging area (read by TMA stores)
-    static constexpr int CHUNK = UPD ? 32 : 64;          // columns per chunk
+    // combine) and a double-buffered output staging area (read by TMA stores).
+    // The first update reads u as a bf16 hi | lo pair (32 columns per chunk);
+    // later updates read the fp16 iterate (64 columns).  Updates write fp16.
+    static constexpr bool HILO_IN = UPD && !F16;
+    static constexpr int CHUNK = HILO_IN ? 32 : 64;      // columns per chunk
     static constexpr int NCHUNK = BN / CHUNK;
     static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
-    static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // bf16 128 x 32
+    static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // 128 x 32, 16-bit
     static constexpr int ISLOTS = UPD ? 3 : (HAS_EIN ? 1 : 0);
-    static constexpr int IN_BYTES = UPD ? 2 * HALF_BYTES : kBM * 64 * 2;              // X hi|lo / A chunk
+    static constexpr int IN_BYTES = kBM * 64 * 2;        // u hi | lo (32 columns) / X or A (64 columns)
     static constexpr int OSLOTS = (MODE == MODE_GRAM) ? 1 : 2;
-    static constexpr int OUT_BYTES = UPD ? 2 * HALF_BYTES : 2 * kBM * 64 * 2;         // X' hi|lo / out|mirror
+    static constexpr int OUT_BYTES = UPD ? kBM * 64 * 2 : 2 * kBM * 64 * 2;           // X' / out | mirror
     static constexpr int SMEM_BYTES =
         STAGES * STAGE_BYTES + ISLOTS * IN_BYTES + OSLOTS * OUT_BYTES + 1024 /*align*/ + 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -83,9 +88,9 @@ constexpr int kEpiThreads = 256;  // warps 2-9
 constexpr int kLoaderWarp = 10;
 constexpr int kStoreThread = 64;  // warp 2, lane 0: issues and tracks the bulk stores
 
-template <int MODE>
+template <int MODE, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constant__ GemmParams p) {
-    using C = TcCfg<MODE>;
+    using C = TcCfg<MODE, F16>;
     constexpr int BN = C::BN;
     constexpr int STAGES = C::STAGES;
 
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         if (C::HAS_EIN && lane == 0) {
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_ein[g]);
-                if (C::UPD) tma_prefetch_desc(&p.map_ein2[g]);
+                if (C::HILO_IN) tma_prefetch_desc(&p.map_ein2[g]);
             }
             int slot = 0;
             uint32_t phase = 0;
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     mbar_arrive_expect_tx(&ein_full[slot], C::IN_BYTES);
                     uint8_t* dst = sI + slot * C::IN_BYTES;
                     tma_load_3d(dst, &p.map_ein[g], &ein_full[slot], tj * BN + c * C::CHUNK, ti * kBM, idx);
-                    if (C::UPD)
+                    if (C::HILO_IN)
                         tma_load_3d(dst + C::HALF_BYTES, &p.map_ein2[g], &ein_full[slot], tj * BN + c * C::CHUNK,
                                     ti * kBM, idx);
                     issued[slot] = true;
@@ -333,10 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     if (ochunk >= C::OSLOTS)
                         mbar_wait(&obuf_free[ob], (uint32_t)((ochunk / C::OSLOTS - 1) & 1), abort_flag, p.status);
                 };
-                if (MODE == MODE_UPDATE) {
+                if (C::HILO_IN) {
+                    // first update: X0 = s u with u as a bf16 hi | lo pair; X1 in fp16
                     float v[16];
                     tmem_load_32x16(t_acc + c * 32 + half * 16, v);
-                    // inputs: hi and lo halves of X, rows of 64 bytes, 64-byte swizzle
+                    // inputs: hi and lo halves of u, rows of 64 bytes, 64-byte swizzle
                     mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
                     uint4 hw[2], lw[2];
 #pragma unroll
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         lw[jj] = *reinterpret_cast<const uint4*>(ein + C::HALF_BYTES + sw64(r, j));
                     }
                     mbar_arrive(&ein_empty[islot]);  // this thread is done with the input slot
-                    uint32_t ho[2][4], lo[2][4];
+                    uint32_t ow[2][4];
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
                         const uint32_t hs[4] = {hw[jj].x, hw[jj].y, hw[jj].z, hw[jj].w};
@@ -355,13 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         for (int h = 0; h < 4; ++h) {
                             const float x0 = __uint_as_float(hs[h] << 16) + __uint_as_float(ls[h] << 16);
                             const float x1 = __uint_as_float(hs[h] & 0xFFFF0000u) + __uint_as_float(ls[h] & 0xFFFF0000u);
-                            const float y0 = scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]);
-                            const float y1 = scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]);
-                            const uint16_t b0 = f2bf(y0), b1 = f2bf(y1);
-                            ho[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-                            lo[jj][h] = pack_bf2(y0 - bf2f(b0), y1 - bf2f(b1));
+                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]));
+                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]));
+                            ow[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                             if (p.want_rowsq) {
-                                const float o0 = bf2f(b0), o1 = bf2f(b1);
+                                const float o0 = h2f(b0), o1 = h2f(b1);
                                 sumsq = fmaf(o0, o0, sumsq);
                                 sumsq = fmaf(o1, o1, sumsq);
                             }
@@ -369,13 +373,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     }
                     wait_obuf();
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const uint32_t j = (uint32_t)(half * 2 + jj);
-                        *reinterpret_cast<uint4*>(obuf + sw64(r, j)) = make_uint4(ho[jj][0], ho[jj][1], ho[jj][2], ho[jj][3]);
-                        if (!p.last)
-                            *reinterpret_cast<uint4*>(obuf + C::HALF_BYTES + sw64(r, j)) =
-                                make_uint4(lo[jj][0], lo[jj][1], lo[jj][2], lo[jj][3]);
+                    for (int jj = 0; jj < 2; ++jj)
+                        *reinterpret_cast<uint4*>(obuf + sw64(r, (uint32_t)(half * 2 + jj))) =
+                            make_uint4(ow[jj][0], ow[jj][1], ow[jj][2], ow[jj][3]);
+                } else if (MODE == MODE_UPDATE) {
+                    // later updates: fp16 iterate in and out, 64-column chunks, 128-byte swizzle
+                    float v[32];
+                    tmem_load_32x32(t_acc + c * 64 + half * 32, v);
+                    mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
+                    uint4 xw[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        xw[jj] = *reinterpret_cast<const uint4*>(ein + sw128(r, (uint32_t)(half * 4 + jj)));
+                    mbar_arrive(&ein_empty[islot]);  // this thread is done with the input slot
+                    uint32_t ow[4][4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t xs[4] = {xw[jj].x, xw[jj].y, xw[jj].z, xw[jj].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const float x0 = h2f((uint16_t)(xs[h] & 0xFFFFu)), x1 = h2f((uint16_t)(xs[h] >> 16));
+                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]));
+                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]));
+                            ow[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                            if (p.want_rowsq) {
+                                const float o0 = h2f(b0), o1 = h2f(b1);
+                                sumsq = fmaf(o0, o0, sumsq);
+                                sumsq = fmaf(o1, o1, sumsq);
+                            }
+                        }
                     }
+                    wait_obuf();
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        *reinterpret_cast<uint4*>(obuf + sw128(r, (uint32_t)(half * 4 + jj))) =
+                            make_uint4(ow[jj][0], ow[jj][1], ow[jj][2], ow[jj][3]);
                 } else {
                     float v[32];
                     tmem_load_32x32(t_acc + c * 64 + half * 32, v);
@@ -391,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                             const uint32_t ws[4] = {aw[jj].x, aw[jj].y, aw[jj].z, aw[jj].w};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
-                                const float lo = __uint_as_float(ws[h] << 16), hi = __uint_as_float(ws[h] & 0xFFFF0000u);
+                                const float lo = x2f<F16>((uint16_t)(ws[h] & 0xFFFFu)), hi = x2f<F16>((uint16_t)(ws[h] >> 16));
                                 v[8 * jj + 2 * h] = fmaf(p.cb, lo, p.cc * v[8 * jj + 2 * h]);
                                 v[8 * jj + 2 * h + 1] = fmaf(p.cb, hi, p.cc * v[8 * jj + 2 * h + 1]);
                             }
@@ -402,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     }
                     uint16_t b[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) b[e] = f2bf(v[e]);
+                    for (int e = 0; e < 32; ++e) b[e] = f2x<F16>(v[e]);
                     wait_obuf();
                     uint8_t* eout = obuf;                  // 128 x 64 bf16, 128-byte swizzle
                     uint8_t* emir = obuf + kBM * 64 * 2;  // transposed chunk: two 64 x 64 boxes
@@ -431,10 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                 named_barrier(1, kEpiThreads);
                 if (store_thread) {
                     if (MODE == MODE_UPDATE) {
-                        if (col0 < G.n) {
-                            tma_store_3d(&p.map_out[g], obuf, col0, ti * kBM, idx);
-                            if (!p.last) tma_store_3d(&p.map_out2[g], obuf + C::HALF_BYTES, col0, ti * kBM, idx);
-                        }
+                        if (col0 < G.n) tma_store_3d(&p.map_out[g], obuf, col0, ti * kBM, idx);
                     } else if (col0 < G.m) {
                         tma_store_3d(&p.map_out[g], obuf, col0, ti * kBM, idx);
                         if (mirror) {
@@ -479,29 +508,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
     }
 }
 
+template <int MODE, bool F16>
+static cudaError_t configure_one() {
+    return cudaFuncSetAttribute(k_ns_gemm_tc<MODE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TcCfg<MODE, F16>::SMEM_BYTES);
+}
+
 cudaError_t ns_gemm_tc_configure() {
-    cudaError_t e = cudaFuncSetAttribute(k_ns_gemm_tc<MODE_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<MODE_GRAM>::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_ns_gemm_tc<MODE_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcCfg<MODE_POLY>::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_ns_gemm_tc<MODE_UPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcCfg<MODE_UPDATE>::SMEM_BYTES);
+    cudaError_t e = configure_one<MODE_GRAM, false>();
+    if (e == cudaSuccess) e = configure_one<MODE_GRAM, true>();
+    if (e == cudaSuccess) e = configure_one<MODE_POLY, false>();
+    if (e == cudaSuccess) e = configure_one<MODE_POLY, true>();
+    if (e == cudaSuccess) e = configure_one<MODE_UPDATE, false>();
+    if (e == cudaSuccess) e = configure_one<MODE_UPDATE, true>();
     return e;
 }
 
-template <int MODE>
+template <int MODE, bool F16>
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, int num_sms, cudaStream_t stream) {
-    using C = TcCfg<MODE>;
+    using C = TcCfg<MODE, F16>;
     if (p.ntiles <= 0) return cudaSuccess;
     const int grid = p.ntiles < num_sms ? p.ntiles : num_sms;
-    k_ns_gemm_tc<MODE><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
+    k_ns_gemm_tc<MODE, F16><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_ns_gemm_tc<MODE_GRAM>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_POLY>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_UPDATE>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_GRAM, false>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_UPDATE, false>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_UPDATE, true>(const GemmParams&, int, cudaStream_t);
 
 }  // namespace muon

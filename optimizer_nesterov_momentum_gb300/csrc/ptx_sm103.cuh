@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace muon {
 
@@ -183,13 +184,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 
 // Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, both operands
 // K-major unless b_mn_major.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_major) {
+// kind::f16 instruction descriptor: fp32 accumulator, A and B both fp16 or both bf16.
+__host__ __device__ constexpr uint32_t make_idesc_16bit(int M, int N, bool b_mn_major, bool fp16) {
     return (1u << 4)                               // D format: f32
-           | (1u << 7)                             // A format: bf16
-           | (1u << 10)                            // B format: bf16
+           | ((fp16 ? 0u : 1u) << 7)               // A format: 0 = f16, 1 = bf16
+           | ((fp16 ? 0u : 1u) << 10)              // B format: the same type as A
            | ((b_mn_major ? 1u : 0u) << 16)        // B major-ness
            | ((uint32_t)(N >> 3) << 17)            // N / 8
            | ((uint32_t)(M >> 4) << 24);           // M / 16
+}
+
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_major) {
+    return make_idesc_16bit(M, N, b_mn_major, false);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -251,6 +257,21 @@ __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(((uin
 
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+}
+
+// ---------------------------------------------------------------- fp16 helpers
+__device__ __forceinline__ uint16_t f2h(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// 16-bit value <-> float in either format
+template <bool FP16>
+__device__ __forceinline__ uint16_t f2x(float x) {
+    return FP16 ? f2h(x) : f2bf(x);
+}
+template <bool FP16>
+__device__ __forceinline__ float x2f(uint16_t b) {
+    return FP16 ? h2f(b) : bf2f(b);
 }
 
 }  // namespace muon

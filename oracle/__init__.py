@@ -19,6 +19,7 @@ from .muon_oracle import (
     OracleConfig,
     MuonOracle,
     bf16_round,
+    fp16_round,
     momentum_update,
     nesterov_direction,
     split_matrix,
@@ -52,6 +53,7 @@ __all__ = [
     "OracleConfig",
     "MuonOracle",
     "bf16_round",
+    "fp16_round",
     "momentum_update",
     "nesterov_direction",
     "split_matrix",

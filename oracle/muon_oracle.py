@@ -69,6 +69,12 @@ V_FLOOR: float = 1e-10
 # bf16 emulation (diagnostic only)
 # ---------------------------------------------------------------------------
 
+def fp16_round(x: np.ndarray) -> np.ndarray:
+    """Round to IEEE binary16 (round-to-nearest-even, subnormals kept) via float32, return float64."""
+    f = np.asarray(np.asarray(x, dtype=np.float32), dtype=np.float16)
+    return f.astype(np.float64)
+
+
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round to bfloat16 (round-to-nearest-even) via float32, return float64.
 
@@ -198,23 +204,30 @@ def newton_schulz(x: np.ndarray, steps: int = 5, coeffs=None, form: str = "page"
 
 
 def newton_schulz_mixed(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarray:
-    """Diagnostic: the iteration with the rounding points of a mixed-precision
-    bf16 tensor-core implementation (not a definition of the method).
+    """Diagnostic: the iteration with the rounding points of the mixed-precision
+    tensor-core implementation (not a definition of the method).
 
-    The iterate is held in fp32; each product reads bf16-rounded operands and
-    accumulates exactly; A and P = b A + c A A are stored in bf16; the output
-    is rounded to bf16.  Used only to size the bf16 error of tiny matrices,
-    where a relative Frobenius error is dominated by a handful of singular
-    values and can exceed the 2e-2 bound that holds for the workloads.
+    The first iteration reads bf16-rounded operands of an fp32 iterate (the
+    normalised input, held as a bf16 hi + lo pair), stores A and P = b A + c A A
+    in bf16 and rounds its result to fp16.  Every later iteration holds X, A
+    and P in fp16.  Products accumulate exactly.  Used only to size the
+    rounding error of tiny matrices, where a relative Frobenius error is
+    dominated by a handful of singular values and can exceed the 2e-2 bound
+    that holds for the workloads.
     """
     f32 = lambda v: np.asarray(v, dtype=np.float32).astype(np.float64)
     x = f32(x)
-    for a, b, c in _coeff_list(coeffs, steps):
-        xb = bf16_round(x)
-        A = bf16_round(xb @ xb.T)
-        P = bf16_round(b * A + c * (A @ A))
-        x = f32(a * x + P @ xb)
-    return bf16_round(x)
+    for k, (a, b, c) in enumerate(_coeff_list(coeffs, steps)):
+        if k == 0:
+            xb = bf16_round(x)
+            A = bf16_round(xb @ xb.T)
+            P = bf16_round(b * A + c * (A @ A))
+            x = fp16_round(a * x + P @ xb)
+        else:
+            A = fp16_round(x @ x.T)
+            P = fp16_round(b * A + c * (A @ A))
+            x = fp16_round(a * x + P @ x)
+    return x
 
 
 def zeropower_via_newtonschulz5(g: np.ndarray, steps: int = 5, eps: float = NORM_EPS, coeffs=None,

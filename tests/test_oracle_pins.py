@@ -293,6 +293,14 @@ def test_split_contiguous_and_columns():
 # bf16 emulation vs a library cast
 # ---------------------------------------------------------------------------
 
+def test_fp16_round_exact_cases():
+    # binary16: 11 significant bits, ties to even, max 65504, subnormal step 2^-24
+    cases = [(1.0 + 2.0 ** -11, 1.0), (1.0 + 3 * 2.0 ** -12, 1.0 + 2.0 ** -10), (1.0 + 2.0 ** -10, 1.0 + 2.0 ** -10),
+             (65504.0, 65504.0), (3 * 2.0 ** -25, 2.0 ** -23), (2.0 ** -25, 0.0), (-0.1, -0.0999755859375)]
+    for x, want in cases:
+        assert oracle.fp16_round(np.array([x]))[0] == want, x
+
+
 def test_bf16_round_matches_torch_cast():
     rng = np.random.default_rng(1)
     x = np.concatenate([rng.standard_normal(10000) * 10.0 ** rng.integers(-8, 8, 10000),
