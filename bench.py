@@ -420,10 +420,12 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16+fp16", "data": "synthetic",
             "config": {"workload": wl.name, "description": wl.description, "matrices": len(wl.sub_shapes()),
                        "elements": model["elems"], "ns_steps": nsi, "grad_dtype": wl.grad_dtype,
-                       "launch": "cuda graph of muon_step", "l2": "inputs larger than L2 (grads+params+momentum "
+                       "launch": "cuda graph of muon_step",
+                       "tensor_core_operands": "bf16 (first Newton-Schulz iteration), fp16 (later ones); fp32 state",
+                       "l2": "inputs larger than L2 (grads+params+momentum "
                        f"{(model['elems'] * (grad_bytes + 8)) / 1e6:.0f} MB > 129 MB)",
                        "parallelism": "replicas" if world > 1 else "single"},
             "ns": {"tflops_algorithmic": ns_tflops, "frac_of_bf16_peak": ns_tflops / tc_peak,
