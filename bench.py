@@ -164,9 +164,10 @@ def oracle_sample_time(wl, layers=1, repeats=1, seed_step=0):
         t0 = time.perf_counter()
         orc.step(params, grads)
         times.append(time.perf_counter() - t0)
-    scale = nl / layers
-    return min(times) * 1e3 * scale, f"{layers} of {nl} layers ({len(idx)} of {len(wl.matrices)} parameters), " \
-                                     f"one step, fp64 numpy, scaled x{scale:g}"
+    # scaled by the share of parameters sampled (every layer holds the same shapes)
+    scale = len(wl.matrices) / len(idx)
+    return min(times) * 1e3 * scale, f"{min(layers, nl)} of {nl} layers ({len(idx)} of {len(wl.matrices)} " \
+                                     f"parameters), one step, fp64 numpy, scaled x{scale:g}"
 
 
 def cores():
