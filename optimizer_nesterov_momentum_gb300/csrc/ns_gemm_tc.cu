@@ -57,6 +57,7 @@ struct TcCfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr bool B_MN = UPD;
     static constexpr uint32_t IDESC = make_idesc_16bit(kBM, BN, B_MN, F16);
+    static constexpr uint32_t IDESC_N128 = make_idesc_16bit(kBM, 128, B_MN, F16);  // right half of a tile
     // epilogue: column chunks; an input ring (TMA-loaded operands of the
     // combine) and a double-buffered output staging area (read by TMA stores).
     // The first update reads u as a bf16 hi | lo pair (32 columns per chunk);
@@ -76,6 +77,20 @@ struct TcCfg {
     static_assert(!HAS_EIN || ISLOTS >= 1, "an epilogue with inputs needs an input slot");
     static_assert(OSLOTS >= 1 && OSLOTS <= 2, "two output-buffer mbarriers are reserved");
 };
+
+// Operand sharing in the symmetric products.  The rows of tile (ti, tj) are
+// rows of the operand too, so a tile whose rows lie inside its own 256-column
+// block needs fewer bytes:
+//   SYM_FULL   rows outside the block: 128 left rows + 256 right rows per k-block
+//   SYM_LEFT   ti == 2 tj: the left operand is the first half of the right one
+//   SYM_RIGHT  ti == 2 tj + 1: only the right half of the tile is live (the left
+//              half lies below the diagonal), and it is the 128 x 128 product of
+//              those same rows with themselves: one 128-row load, N = 128, into
+//              TMEM columns 128..255
+enum { SYM_FULL = 0, SYM_LEFT = 1, SYM_RIGHT = 2 };
+__device__ __forceinline__ int sym_tile_kind(int ti, int tj) {
+    return ti == 2 * tj ? SYM_LEFT : (ti == 2 * tj + 1 ? SYM_RIGHT : SYM_FULL);
+}
 
 // A 64-column chunk of a symmetric tile is live unless its 128-column block
 // lies left of (below) the diagonal block of the tile's rows.
@@ -160,21 +175,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 const int K = (MODE == MODE_GRAM) ? p.grp[g].n : p.grp[g].m;
                 const int nkb = (K + kBK - 1) / kBK;
+                const int kind = C::SYM ? sym_tile_kind(ti, tj) : SYM_FULL;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     uint8_t* a_dst = sA + stage * C::A_BYTES;
                     uint8_t* b_dst = sB + stage * C::B_BYTES;
-                    tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
                     if (C::B_MN) {
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
                             tma_load_3d(b_dst + c * (64 * kBK * 2), &p.map_b[g], &full[stage], tj * BN + c * 64,
                                         kb * kBK, idx);
+                    } else if (kind == SYM_RIGHT) {
+                        // the tile's own 128 rows only, in the left-operand slot
+                        mbar_arrive_expect_tx(&full[stage], C::A_BYTES);
+                        tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, tj * BN + kBM, idx);
                     } else {
+                        mbar_arrive_expect_tx(&full[stage], kind == SYM_LEFT ? C::B_BYTES : C::STAGE_BYTES);
+                        if (kind == SYM_FULL) tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
 #pragma unroll
                         for (int h = 0; h < BN / kBM; ++h)
                             tma_load_3d(b_dst + h * (kBM * kBK * 2), &p.map_a[g], &full[stage], kb * kBK,
@@ -212,26 +234,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                 const int g = tile.x;
                 const int K = (MODE == MODE_GRAM) ? p.grp[g].n : p.grp[g].m;
                 const int nkb = (K + kBK - 1) / kBK;
+                const int kind = C::SYM ? sym_tile_kind(tile.z, tile.w) : SYM_FULL;
+                const uint32_t idesc = kind == SYM_RIGHT ? C::IDESC_N128 : C::IDESC;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                // SYM_RIGHT accumulates only the tile's right half: TMEM columns 128..255
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN) + (kind == SYM_RIGHT ? 128u : 0u);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_st = a_base + stage * C::A_BYTES;
-                    const uint32_t b_st = b_base + stage * C::B_BYTES;
+                    // SYM_LEFT: the left operand is the first 128 rows of the right one;
+                    // SYM_RIGHT: both operands are the 128 rows in the left slot
+                    const uint32_t a_st = kind == SYM_LEFT ? b_base + stage * C::B_BYTES : a_base + stage * C::A_BYTES;
+                    const uint32_t b_st = kind == SYM_RIGHT ? a_base + stage * C::A_BYTES : b_base + stage * C::B_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t adesc = make_sdesc_sw128(a_st + kk * 32, 16, 1024);
                         const uint64_t bdesc = C::B_MN ? make_sdesc_sw128(b_st + kk * (16 * 128), 64 * kBK * 2, 1024)
                                                        : make_sdesc_sw128(b_st + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                         any = true;
                     }
                     umma_commit(&empty[stage]);
