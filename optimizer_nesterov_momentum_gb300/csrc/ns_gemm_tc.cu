@@ -50,7 +50,10 @@ struct TcCfg {
     static constexpr bool UPD = (MODE == MODE_UPDATE);
     static constexpr bool SYM = !UPD;
     static constexpr int BN = UPD ? kBNUpd : kBNSym;
-    static constexpr int STAGES = (MODE == MODE_GRAM) ? 4 : 3;
+    // the mainloop is bound by stages in flight against load latency: four where the
+    // epilogue's staging leaves room (the Gram has no input; the fp16 update takes one
+    // input and one output slot)
+    static constexpr int STAGES = (MODE == MODE_GRAM || (UPD && F16)) ? 4 : 3;
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -67,9 +70,9 @@ struct TcCfg {
     static constexpr int NCHUNK = BN / CHUNK;
     static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
     static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // 128 x 32, 16-bit
-    static constexpr int ISLOTS = UPD ? 3 : (HAS_EIN ? 1 : 0);
+    static constexpr int ISLOTS = UPD ? (F16 ? 1 : 3) : (HAS_EIN ? 1 : 0);
     static constexpr int IN_BYTES = kBM * 64 * 2;        // u hi | lo (32 columns) / X or A (64 columns)
-    static constexpr int OSLOTS = (MODE == MODE_GRAM) ? 1 : 2;
+    static constexpr int OSLOTS = (MODE == MODE_GRAM || (UPD && F16)) ? 1 : 2;
     static constexpr int OUT_BYTES = UPD ? kBM * 64 * 2 : 2 * kBM * 64 * 2;           // X' / out | mirror
     static constexpr int SMEM_BYTES =
         STAGES * STAGE_BYTES + ISLOTS * IN_BYTES + OSLOTS * OUT_BYTES + 1024 /*align*/ + 512;
