@@ -106,7 +106,7 @@ struct GemmGroup {
 
 struct GemmParams {
     CUtensorMap map_a[kMaxGroupsPerLaunch];     // left operand (K-major)
-    CUtensorMap map_b[kMaxGroupsPerLaunch];     // right operand of the update (MN-major X)
+    CUtensorMap map_b[kMaxGroupsPerLaunch];     // right operand: 256-row K-major box (gram / poly), MN-major X (update)
     CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, update hi half of X
     CUtensorMap map_ein2[kMaxGroupsPerLaunch];  // epilogue input: update lo half of X
     CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: bf16 tile; update: hi half of X'

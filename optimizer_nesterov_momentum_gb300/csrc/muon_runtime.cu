@@ -70,6 +70,7 @@ struct Group {
     // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), 32 x 128 boxes of
     // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
+    CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
 };
 
@@ -532,9 +533,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         bool ok = encode_bf16_3d(enc, &g.map_u_k, g.u16, g.n, g.m, g.count, g.ldx, kBM) &&
                   encode_bf16_3d(enc, &g.map_u_mn, g.u16, g.n, g.m, g.count, g.ldx, 64) &&
                   encode_bf16_3d(enc, &g.map_a_k, g.a16, g.m, g.m, g.count, g.lda, kBM) &&
-                  encode_bf16_3d(enc, &g.map_p_k, g.p16, g.m, g.m, g.count, g.lda, kBM);
+                  encode_bf16_3d(enc, &g.map_p_k, g.p16, g.m, g.m, g.count, g.lda, kBM) &&
+                  encode_bf16_3d(enc, &g.map_u_k256, g.u16, g.n, g.m, g.count, g.ldx, 2 * kBM) &&
+                  encode_bf16_3d(enc, &g.map_a_k256, g.a16, g.m, g.m, g.count, g.lda, 2 * kBM);
         for (int b = 0; b < 2 && ok; ++b)
             ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
+                 encode_bf16_3d(enc, &g.map_x_k256[b], g.x16[b], g.n, g.m, g.count, g.ldx, 2 * kBM) &&
                  encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64) &&
                  encode_3d(enc, &g.map_x_o32[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
                            g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -654,6 +658,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     G.rowsq = g.rowsq;
                     if (mode == MODE_GRAM) {
                         gp.map_a[sl] = first ? g.map_u_k : g.map_x_k[in_buf];
+                        gp.map_b[sl] = first ? g.map_u_k256 : g.map_x_k256[in_buf];
                         gp.map_out[sl] = g.map_a_k;
                         gp.map_out2[sl] = g.map_a_mir;
                         G.out16 = g.a16;
@@ -661,6 +666,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         G.opr16 = xin16;
                     } else if (mode == MODE_POLY) {
                         gp.map_a[sl] = g.map_a_k;
+                        gp.map_b[sl] = g.map_a_k256;
                         gp.map_ein[sl] = g.map_a_k;
                         gp.map_out[sl] = g.map_p_k;
                         gp.map_out2[sl] = g.map_p_mir;

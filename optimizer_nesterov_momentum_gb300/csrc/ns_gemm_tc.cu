@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         if (lane == 0) {
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_a[g]);
-                if (C::B_MN) tma_prefetch_desc(&p.map_b[g]);
+                tma_prefetch_desc(&p.map_b[g]);
             }
             int stage = 0;
             uint32_t phase = 0;
@@ -200,10 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     } else {
                         mbar_arrive_expect_tx(&full[stage], kind == SYM_LEFT ? C::B_BYTES : C::STAGE_BYTES);
                         if (kind == SYM_FULL) tma_load_3d(a_dst, &p.map_a[g], &full[stage], kb * kBK, ti * kBM, idx);
-#pragma unroll
-                        for (int h = 0; h < BN / kBM; ++h)
-                            tma_load_3d(b_dst + h * (kBM * kBK * 2), &p.map_a[g], &full[stage], kb * kBK,
-                                        tj * BN + h * kBM, idx);
+                        // the right operand's 256 rows in one box
+                        tma_load_3d(b_dst, &p.map_b[g], &full[stage], kb * kBK, tj * BN, idx);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
