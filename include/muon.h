@@ -224,7 +224,8 @@ int muon_get_stage_times(muon_handle h, float* out);
 #define MUON_STATE_MOMENTUM 0      /* per parameter i: fp32 rows x cols, row-major, dense */
 #define MUON_STATE_SECOND_MOMENT 1 /* per split matrix: fp32 [m] */
 #define MUON_STATE_ORTHO 2         /* per split matrix: last Newton-Schulz output O, wide
-                                      orientation m x n, dense, raw fp16 (2 bytes each) */
+                                      orientation m x n, fp32, DEVICE destination only
+                                      (rebuilt on the device from its scaled fp16 copy) */
 #define MUON_STATE_DIRECTION 3     /* per split matrix: last Nesterov direction u, wide
                                       orientation m x n, fp32, DEVICE destination only
                                       (rebuilt on the device from its bf16 hi + lo pair) */

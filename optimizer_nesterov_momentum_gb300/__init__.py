@@ -187,7 +187,7 @@ class Muon:
             if which == MUON_STATE_SECOND_MOMENT:
                 out = torch.empty((info["m"],), dtype=torch.float32, device=dev)
             elif which == MUON_STATE_ORTHO:
-                out = torch.empty((info["m"], info["n"]), dtype=torch.float16, device=dev)
+                out = torch.empty((info["m"], info["n"]), dtype=torch.float32, device=dev)
             elif which == MUON_STATE_DIRECTION:
                 out = torch.empty((info["m"], info["n"]), dtype=torch.float32, device=dev)
             else:

@@ -203,15 +203,22 @@ __global__ void __launch_bounds__(256) k_norm_scale(const __grid_constant__ Norm
     float s = 0.f;
     for (int t = threadIdx.x; t < d.k1_ntiles; t += 256) s += p.norm_part[d.k1_tile0 + t];
     const float total = block_sum_256(s, red);
-    if (threadIdx.x == 0) p.norm_scale[blockIdx.x] = 1.f / (sqrtf(total) + kNormEps);
+    if (threadIdx.x == 0) {
+        const float norm = sqrtf(total);
+        const float sc = 1.f / (norm + kNormEps);
+        p.norm_scale[blockIdx.x] = sc;
+        // ||X0|| = ||u|| s: the Newton-Schulz kernels keep their iterate divided by it
+        p.iter_scale[blockIdx.x] = norm > 0.f ? norm * sc : 1.f;
+    }
 }
 
 __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ LaneParams p) {
     __shared__ float red[8];
     const SubDesc& d = p.subs[blockIdx.x];
     const float eff = p.hp[HP_LR] * d.lr_mul;
+    const float cs = p.iter_scale[blockIdx.x];  // O = cs * (the stored output)
     if (!p.normuon) {
-        const float f = eff * d.shape_scale;
+        const float f = eff * d.shape_scale * cs;
         for (int i = threadIdx.x; i < d.m; i += 256) d.lane[i] = f;
         return;
     }
@@ -221,6 +228,7 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
     for (int i = threadIdx.x; i < d.m; i += 256) {
         float rs = 0.f;
         for (int t = 0; t < 2 * d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n * 2 + t];
+        rs *= cs * cs;
         const float r = rs * inv_n;
         const float v0 = d.v[i];
         const float v1 = fmaf(1.f - beta2, r - v0, v0);  // v.lerp_(r, 1 - beta2)
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
     const float sb = block_sum_256(before, red);
     const float sa = block_sum_256(after, red);
     const float gamma = p.norm_preserve ? sqrtf(sb) / fmaxf(sqrtf(sa), kVFloor) : 1.f;
-    const float f = eff * gamma;
+    const float f = eff * gamma * cs;
     for (int i = threadIdx.x; i < d.m; i += 256) d.lane[i] *= f;
 }
 
@@ -326,6 +334,23 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
 }
 
 // u = hi + lo of one matrix into a dense fp32 m x n array (state access)
+// O = c * (the stored fp16 output), dense fp32 m x n
+__global__ void k_scale_f16(float* dst, const uint16_t* src, const float* c, int m, int n, int ld) {
+    const int64_t total = (int64_t)m * n;
+    const float cs = *c;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / n, j = e % n;
+        dst[e] = cs * h2f(src[i * ld + j]);
+    }
+}
+
+cudaError_t launch_scale_f16(float* dst, const uint16_t* src, const float* c, int m, int n, int ld, cudaStream_t s) {
+    const int64_t total = (int64_t)m * n;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    k_scale_f16<<<blocks, 256, 0, s>>>(dst, src, c, m, n, ld);
+    return cudaGetLastError();
+}
+
 __global__ void k_combine_hilo(float* dst, const uint16_t* hi, const uint16_t* lo, int m, int n, int ld) {
     const int64_t total = (int64_t)m * n;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {

@@ -5,7 +5,9 @@
 //   * per split matrix ("sub"), in the wide orientation m x n (m <= n):
 //       u16 / ulo16 Nesterov direction as a pair of bf16 arrays, u = hi + lo (S2)
 //       x16         Newton-Schulz iterate after the first iteration, fp16 (the
-//                   tensor-core operand); two buffers used in turn (S5-S7)
+//                   tensor-core operand), stored as X / c with c = ||X0|| so that
+//                   small inputs stay inside fp16's range (A and P likewise as
+//                   A / c^2, P / c^2); two buffers used in turn (S5-S7)
 //       a16 / p16   A = X X^T and P = b A + c A A, m x m: bf16 in the first
 //                   iteration (on u), fp16 after (S5, S6)
 //       rowsq       per (row, 256-column tile, column half) sums of O^2 from the
@@ -116,6 +118,7 @@ struct GemmParams {
     int32_t ntiles;
     int32_t ngroups;
     const float* norm_scale; // s per sub (first iteration), else nullptr
+    const float* iter_scale; // c per sub: X, A, P are stored as X / c, A / c^2, P / c^2
     float ca, cb, cc;        // (a, b, c) of this iteration
     int32_t first, last, want_rowsq;
     int32_t f16;             // operands and results fp16 (iterations after the first); else bf16
@@ -127,6 +130,7 @@ struct LaneParams {
     int32_t nsubs;
     const float* hp;
     int32_t normuon, norm_preserve;
+    const float* iter_scale;  // c per sub: the stored iterate is X / c
 };
 
 struct NormParams {
@@ -134,6 +138,7 @@ struct NormParams {
     int32_t nsubs;
     const float* norm_part;
     float* norm_scale;
+    float* iter_scale;        // c = ||u|| s = ||X0|| per sub (1 when u = 0)
 };
 
 }  // namespace muon

@@ -36,6 +36,7 @@ cudaError_t launch_set_hparams(float*, float, float, float, float, cudaStream_t)
 cudaError_t launch_schedule_set(DevSchedule*, const DevSchedule&, cudaStream_t);
 cudaError_t launch_schedule_advance(float*, DevSchedule*, cudaStream_t);
 cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, int, int, cudaStream_t);
+cudaError_t launch_scale_f16(float*, const uint16_t*, const float*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
 template <int MODE, bool F16>
 cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
@@ -109,6 +110,7 @@ struct muon_s {
     DevSchedule* sched = nullptr;  // step schedule + counter (zero at create)
     bool schedule_on = false;      // muon_step starts with the schedule kernel
     float* norm_scale = nullptr;
+    float* iter_scale = nullptr;   // c = ||X0|| per sub
     float* norm_part = nullptr;
     float* momentum = nullptr;
     SubDesc* d_subs = nullptr;
@@ -413,6 +415,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     const size_t o_status = take(sizeof(int));
     const size_t o_sched = take(sizeof(DevSchedule));
     const size_t o_norm_scale = take(sizeof(float) * nsubs);
+    const size_t o_iter_scale = take(sizeof(float) * nsubs);
     // elementwise tiles
     std::vector<int4> elem_tiles;
     std::vector<int32_t> k1_tile0(nsubs), k1_ntiles(nsubs);
@@ -513,6 +516,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->status = reinterpret_cast<int*>(base + o_status);
     h->sched = reinterpret_cast<DevSchedule*>(base + o_sched);
     h->norm_scale = reinterpret_cast<float*>(base + o_norm_scale);
+    h->iter_scale = reinterpret_cast<float*>(base + o_iter_scale);
     h->norm_part = reinterpret_cast<float*>(base + o_norm_part);
     h->momentum = reinterpret_cast<float*>(base + o_mom);
     h->d_subs = reinterpret_cast<SubDesc*>(base + o_subs);
@@ -622,6 +626,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 memset(&gp, 0, sizeof(gp));
                 gp.ngroups = ch.ng;
                 gp.norm_scale = h->norm_scale;
+                gp.iter_scale = h->iter_scale;
                 gp.ca = h->coeffs[3 * it + 0];
                 gp.cb = h->coeffs[3 * it + 1];
                 gp.cc = h->coeffs[3 * it + 2];
@@ -714,7 +719,7 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
     MUON_CUDA(h, mark(h, MUON_STAGE_MOMENTUM, s));
     if (h->schedule_on) MUON_CUDA(h, launch_schedule_advance(h->hp, h->sched, s));
     MUON_CUDA(h, run_elem_any(h, params, grads, false, s));
-    NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale};
+    NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale, h->iter_scale};
     MUON_CUDA(h, mark(h, MUON_STAGE_NORM, s));
     MUON_CUDA(h, launch_norm_scale(np, s));
     const int nch = (int)h->chunks.size();
@@ -748,7 +753,7 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
             }
         }
     }
-    LaneParams lp{h->d_subs, (int32_t)h->subs.size(), h->hp, h->cfg.normuon, h->cfg.norm_preserve};
+    LaneParams lp{h->d_subs, (int32_t)h->subs.size(), h->hp, h->cfg.normuon, h->cfg.norm_preserve, h->iter_scale};
     MUON_CUDA(h, mark(h, MUON_STAGE_LANE, s));
     MUON_CUDA(h, launch_lane_stats(lp, s));
     MUON_CUDA(h, mark(h, MUON_STAGE_APPLY, s));
@@ -942,18 +947,18 @@ int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void*
     const SubDesc& d = h->subs[index];
     if (which == MUON_STATE_SECOND_MOMENT) {
         MUON_CUDA(h, cudaMemcpyAsync(dst, d.v, sizeof(float) * d.m, cudaMemcpyDefault, s));
-    } else if (which == MUON_STATE_ORTHO) {
-        MUON_CUDA(h, cudaMemcpy2DAsync(dst, sizeof(uint16_t) * d.n, d.o16, sizeof(uint16_t) * d.ldx,
-                                       sizeof(uint16_t) * d.n, d.m, cudaMemcpyDefault, s));
-    } else if (which == MUON_STATE_DIRECTION) {
-        // u is stored as a bf16 hi + lo pair: combine it on the device into the caller's array
+    } else if (which == MUON_STATE_ORTHO || which == MUON_STATE_DIRECTION) {
+        // both are rebuilt on the device: O = c * (stored fp16 output), u = hi + lo
         cudaPointerAttributes attr;
         if (cudaPointerGetAttributes(&attr, dst) != cudaSuccess ||
             (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)) {
             cudaGetLastError();
-            return fail(h, MUON_ERR_ARG, "MUON_STATE_DIRECTION needs a device destination");
+            return fail(h, MUON_ERR_ARG, "MUON_STATE_ORTHO / MUON_STATE_DIRECTION need a device destination");
         }
-        MUON_CUDA(h, launch_combine_hilo(static_cast<float*>(dst), d.u16, d.ulo16, d.m, d.n, d.ldx, s));
+        if (which == MUON_STATE_ORTHO)
+            MUON_CUDA(h, launch_scale_f16(static_cast<float*>(dst), d.o16, h->iter_scale + index, d.m, d.n, d.ldx, s));
+        else
+            MUON_CUDA(h, launch_combine_hilo(static_cast<float*>(dst), d.u16, d.ulo16, d.m, d.n, d.ldx, s));
     } else {
         return fail(h, MUON_ERR_ARG, "bad state selector %d", which);
     }

@@ -64,7 +64,10 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
         __syncthreads();
     }
 
-    const float s = p.first ? p.norm_scale[G.sub0 + idx] : 1.f;
+    // stored iterate X / c (c = ||X0||): see the tensor-core kernels
+    const float cs = p.iter_scale[G.sub0 + idx];
+    const float c2 = cs * cs;
+    const float s = p.first ? p.norm_scale[G.sub0 + idx] / cs : 1.f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = ti * 64 + ty * 4 + r;
@@ -77,13 +80,13 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
                 G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(acc[r][c] * (s * s));
             } else if (MODE == MODE_POLY) {
                 const float a = dec(G.a16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j]);
-                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(fmaf(p.cb, a, p.cc * acc[r][c]));
+                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(fmaf(p.cb, a, (p.cc * c2) * acc[r][c]));
             } else {
                 const int64_t off = (int64_t)idx * G.x_stride + (int64_t)i * G.ldx + j;
                 // the first update reads u as hi + lo (bf16); later ones the fp16 iterate
                 const float x = p.f16 ? h2f(R[(int64_t)i * ldr + j])
                                       : bf2f(R[(int64_t)i * ldr + j]) + bf2f(G.xlo_in[off]);
-                G.x16_out[off] = f2h(s * fmaf(p.ca, x, acc[r][c]));  // the next iterate is fp16
+                G.x16_out[off] = f2h(s * fmaf(p.ca, x, c2 * acc[r][c]));  // the next iterate is fp16
             }
         }
     }

@@ -348,9 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
             tc_fence_after();
             const uint32_t t_acc = tmem_base + lane_off + (uint32_t)(acc * BN);
+            // the iterate is stored as X / c (c = ||X0||): the first Gram scales u u^T by
+            // (s / c)^2, the first update u by s / c; A A and P X carry a factor c^2
+            const float cs = p.iter_scale[G.sub0 + idx];
+            const float c2 = cs * cs;
             float scale = 1.f;
             if (p.first && MODE != MODE_POLY) {
-                const float s = p.norm_scale[G.sub0 + idx];
+                const float s = p.norm_scale[G.sub0 + idx] / cs;
                 scale = (MODE == MODE_GRAM) ? s * s : s;
             }
             float sumsq = 0.f;
@@ -389,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         for (int h = 0; h < 4; ++h) {
                             const float x0 = __uint_as_float(hs[h] << 16) + __uint_as_float(ls[h] << 16);
                             const float x1 = __uint_as_float(hs[h] & 0xFFFF0000u) + __uint_as_float(ls[h] & 0xFFFF0000u);
-                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]));
-                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]));
+                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, c2 * v[8 * jj + 2 * h]));
+                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, c2 * v[8 * jj + 2 * h + 1]));
                             ow[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                             if (p.want_rowsq) {
                                 const float o0 = h2f(b0), o1 = h2f(b1);
@@ -421,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
                             const float x0 = h2f((uint16_t)(xs[h] & 0xFFFFu)), x1 = h2f((uint16_t)(xs[h] >> 16));
-                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, v[8 * jj + 2 * h]));
-                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, v[8 * jj + 2 * h + 1]));
+                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, c2 * v[8 * jj + 2 * h]));
+                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, c2 * v[8 * jj + 2 * h + 1]));
                             ow[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                             if (p.want_rowsq) {
                                 const float o0 = h2f(b0), o1 = h2f(b1);
@@ -452,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 const float lo = x2f<F16>((uint16_t)(ws[h] & 0xFFFFu)), hi = x2f<F16>((uint16_t)(ws[h] >> 16));
-                                v[8 * jj + 2 * h] = fmaf(p.cb, lo, p.cc * v[8 * jj + 2 * h]);
-                                v[8 * jj + 2 * h + 1] = fmaf(p.cb, hi, p.cc * v[8 * jj + 2 * h + 1]);
+                                v[8 * jj + 2 * h] = fmaf(p.cb, lo, (p.cc * c2) * v[8 * jj + 2 * h]);
+                                v[8 * jj + 2 * h + 1] = fmaf(p.cb, hi, (p.cc * c2) * v[8 * jj + 2 * h + 1]);
                             }
                         }
                     } else {

@@ -210,24 +210,29 @@ def newton_schulz_mixed(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarra
     The first iteration reads bf16-rounded operands of an fp32 iterate (the
     normalised input, held as a bf16 hi + lo pair), stores A and P = b A + c A A
     in bf16 and rounds its result to fp16.  Every later iteration holds X, A
-    and P in fp16.  Products accumulate exactly.  Used only to size the
-    rounding error of tiny matrices, where a relative Frobenius error is
-    dominated by a handful of singular values and can exceed the 2e-2 bound
-    that holds for the workloads.
+    and P in fp16.  All stored arrays are divided by a fixed per-matrix scale
+    -- X by c = ||X0||, A and P by c^2 -- so that an input far below unit norm
+    keeps its precision in fp16; in exact arithmetic the scale cancels.
+    Products accumulate exactly.  Used only to size the rounding error of tiny
+    matrices, where a relative Frobenius error is dominated by a handful of
+    singular values and can exceed the 2e-2 bound that holds for the workloads.
     """
     f32 = lambda v: np.asarray(v, dtype=np.float32).astype(np.float64)
     x = f32(x)
+    cs = float(np.linalg.norm(x)) or 1.0
+    c2 = cs * cs
+    xs = None  # the stored fp16 iterate X / c of the later iterations
     for k, (a, b, c) in enumerate(_coeff_list(coeffs, steps)):
         if k == 0:
             xb = bf16_round(x)
-            A = bf16_round(xb @ xb.T)
-            P = bf16_round(b * A + c * (A @ A))
-            x = fp16_round(a * x + P @ xb)
+            A = bf16_round((xb @ xb.T) / c2)
+            P = bf16_round(b * A + (c * c2) * (A @ A))
+            xs = fp16_round((a * x + c2 * (P @ xb)) / cs)
         else:
-            A = fp16_round(x @ x.T)
-            P = fp16_round(b * A + c * (A @ A))
-            x = fp16_round(a * x + P @ x)
-    return x
+            A = fp16_round(xs @ xs.T)
+            P = fp16_round(b * A + (c * c2) * (A @ A))
+            xs = fp16_round(a * xs + c2 * (P @ xs))
+    return cs * xs
 
 
 def zeropower_via_newtonschulz5(g: np.ndarray, steps: int = 5, eps: float = NORM_EPS, coeffs=None,

@@ -199,6 +199,20 @@ def test_device_schedule_followed_by_graph_replays():
     errs.assert_within()
 
 
+@pytest.mark.parametrize("gscale", [1e-12, 1e-9, 1e4])
+def test_extreme_gradient_scales(gscale):
+    """X0 = u / (||u|| + 1e-7) is far from unit norm when ||u|| is tiny; the fp16
+    iterate is stored divided by ||X0|| so such inputs keep their precision."""
+    shapes = [Shape(256, 512), Shape(512, 256), Shape(192, 192)]
+    params, grads = _inputs(shapes, 2, seed=25, grad_dtype="f32")
+    grads = [[(g * gscale).contiguous() for g in gs] for gs in grads]
+    # zero parameters: an update of ~1e-7 would otherwise be measured against the
+    # fp32 rounding of parameters of size ~0.02, not against the kernels
+    params = [torch.zeros_like(p) for p in params]
+    errs, _, _ = run_parity(shapes, params, grads, grad_dtype="f32")
+    errs.assert_within()
+
+
 def test_zero_gradient_keeps_params_and_is_finite():
     shapes = [Shape(64, 192), Shape(192, 64)]
     opt = make_optimizer(shapes, lr=0.03)
