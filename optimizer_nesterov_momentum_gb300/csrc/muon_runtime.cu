@@ -682,8 +682,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         gp.map_a[sl] = g.map_p_k;
                         gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
                         // first update: u hi | lo in 32-column boxes, X1 out in 32-column boxes;
-                        // later updates: the fp16 iterate in and out in 64-column boxes
-                        gp.map_ein[sl] = first ? g.map_u_hi : g.map_x_k[in_buf];
+                        // later updates (a on the diagonal of P): no input, X' out in 64-column boxes
+                        gp.map_ein[sl] = g.map_u_hi;
                         gp.map_ein2[sl] = g.map_u_lo;
                         gp.map_out[sl] = first ? g.map_x_o32[out_buf] : g.map_x_k[out_buf];
                         G.opl16 = g.p16;

@@ -80,13 +80,19 @@ __global__ void __launch_bounds__(256) k_ns_gemm_simt(const __grid_constant__ Ge
                 G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(acc[r][c] * (s * s));
             } else if (MODE == MODE_POLY) {
                 const float a = dec(G.a16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j]);
-                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(fmaf(p.cb, a, (p.cc * c2) * acc[r][c]));
+                float v = fmaf(p.cb, a, (p.cc * c2) * acc[r][c]);
+                if (p.f16) v = c2 * v + (i == j ? p.ca : 0.f);  // later iterations: P' = a I + P, unscaled
+                G.out16[(int64_t)idx * G.a_stride + (int64_t)i * G.lda + j] = enc(v);
             } else {
                 const int64_t off = (int64_t)idx * G.x_stride + (int64_t)i * G.ldx + j;
-                // the first update reads u as hi + lo (bf16); later ones the fp16 iterate
-                const float x = p.f16 ? h2f(R[(int64_t)i * ldr + j])
-                                      : bf2f(R[(int64_t)i * ldr + j]) + bf2f(G.xlo_in[off]);
-                G.x16_out[off] = f2h(s * fmaf(p.ca, x, c2 * acc[r][c]));  // the next iterate is fp16
+                // the first update reads u as hi + lo (bf16) for its a X term; later ones
+                // find a on the diagonal of P.  The next iterate is fp16.
+                if (p.f16) {
+                    G.x16_out[off] = f2h(acc[r][c]);
+                } else {
+                    const float x = bf2f(R[(int64_t)i * ldr + j]) + bf2f(G.xlo_in[off]);
+                    G.x16_out[off] = f2h(s * fmaf(p.ca, x, c2 * acc[r][c]));
+                }
             }
         }
     }

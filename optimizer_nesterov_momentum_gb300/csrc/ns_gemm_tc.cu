@@ -6,7 +6,9 @@
 //
 //   MODE_GRAM    A = sc * X X^T           (sc = s^2 on the first iteration, s = 1/(||u||+eps))
 //   MODE_POLY    P = b A + c A A          (A symmetric, so A A = sum_k A[i,k] A[j,k])
-//   MODE_UPDATE  X' = s1 (a X + P X)      (s1 = s on the first iteration)
+//   MODE_UPDATE  X' = s (a X + P X)       on the first iteration
+//                X' = P X                 on later ones, whose POLY adds a to the
+//                                         diagonal of P: a X + P X = (a I + P) X
 //
 // A and P are symmetric: GRAM and POLY compute 128 x 256 tiles that reach the
 // diagonal or lie above it, and store every 128 x 128 block above the
@@ -27,15 +29,19 @@
 //              chunk, warps 6-9 the second), combine in fp32, round, write
 //              swizzled shared-memory staging tiles; one thread issues TMA
 //              bulk stores
-//   warp 10    epilogue loader (one thread, POLY and UPDATE): TMA-loads the
-//              tiles the epilogue combines with (A for POLY; the hi and lo
-//              halves of the iterate for UPDATE) into an input ring whose
-//              slots come back as soon as every epilogue thread has read its
-//              part into registers; results go to a separate, double-buffered
-//              output staging area that the bulk stores read from
-// The iterate X is held as two bf16 arrays, X = hi + lo (about 16 mantissa
-// bits): hi is the tensor-core operand, and the UPDATE epilogue rebuilds X
-// from both halves for the a*X term and splits the result the same way.
+//   warp 10    epilogue loader (one thread, POLY and the first UPDATE):
+//              TMA-loads the tiles the epilogue combines with (A for POLY; the
+//              hi and lo halves of u for the first UPDATE) into an input ring
+//              whose slots come back as soon as every epilogue thread has read
+//              its part into registers; results go to a separate output
+//              staging area that the bulk stores read from
+// Precision: the first iteration runs on the Nesterov direction u, held as a
+// bf16 pair u = hi + lo (about 16 mantissa bits): hi is the tensor-core
+// operand of the Gram and the update, and the first update rebuilds u from
+// both halves for its a*X term.  Its result and every later X, A and P are
+// fp16, stored divided by a per-matrix scale (X / c, A / c^2, P / c^2 with
+// c = ||X0|| <= 1) that keeps them near unit size whatever the gradient's norm;
+// the folded P' = a I + P of the later iterations is stored unscaled.
 // Every wait is bounded (2 s); on a timeout the kernel sets the status word,
 // lets copies and MMAs in flight finish, frees TMEM and returns.
 #include "muon_internal.h"
@@ -49,11 +55,13 @@ template <int MODE, bool F16>
 struct TcCfg {
     static constexpr bool UPD = (MODE == MODE_UPDATE);
     static constexpr bool SYM = !UPD;
+    // from the second iteration on, the a X term rides on the tensor cores: POLY adds a
+    // to the diagonal of P and UPDATE is the plain product, with no epilogue input
+    static constexpr bool FOLD = F16;
     static constexpr int BN = UPD ? kBNUpd : kBNSym;
     // the mainloop is bound by stages in flight against load latency: four where the
-    // epilogue's staging leaves room (the Gram has no input; the fp16 update takes one
-    // input and one output slot)
-    static constexpr int STAGES = (MODE == MODE_GRAM || (UPD && F16)) ? 4 : 3;
+    // epilogue's staging leaves room (the Gram and the folded update have no input)
+    static constexpr int STAGES = (MODE == MODE_GRAM || (UPD && FOLD)) ? 4 : 3;
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -64,15 +72,15 @@ struct TcCfg {
     // epilogue: column chunks; an input ring (TMA-loaded operands of the
     // combine) and a double-buffered output staging area (read by TMA stores).
     // The first update reads u as a bf16 hi | lo pair (32 columns per chunk);
-    // later updates read the fp16 iterate (64 columns).  Updates write fp16.
-    static constexpr bool HILO_IN = UPD && !F16;
+    // later updates read nothing (64 columns).  Updates write fp16.
+    static constexpr bool HILO_IN = UPD && !FOLD;
     static constexpr int CHUNK = HILO_IN ? 32 : 64;      // columns per chunk
     static constexpr int NCHUNK = BN / CHUNK;
-    static constexpr bool HAS_EIN = (MODE != MODE_GRAM);
+    static constexpr bool HAS_EIN = (MODE == MODE_POLY) || HILO_IN;
     static constexpr int HALF_BYTES = kBM * 32 * 2;                                     // 128 x 32, 16-bit
-    static constexpr int ISLOTS = UPD ? (F16 ? 1 : 3) : (HAS_EIN ? 1 : 0);
-    static constexpr int IN_BYTES = kBM * 64 * 2;        // u hi | lo (32 columns) / X or A (64 columns)
-    static constexpr int OSLOTS = (MODE == MODE_GRAM || (UPD && F16)) ? 1 : 2;
+    static constexpr int ISLOTS = HILO_IN ? 3 : (HAS_EIN ? 1 : 0);
+    static constexpr int IN_BYTES = kBM * 64 * 2;        // u hi | lo (32 columns) / A (64 columns)
+    static constexpr int OSLOTS = (MODE == MODE_GRAM) ? 1 : 2;
     static constexpr int OUT_BYTES = UPD ? kBM * 64 * 2 : 2 * kBM * 64 * 2;           // X' / out | mirror
     static constexpr int SMEM_BYTES =
         STAGES * STAGE_BYTES + ISLOTS * IN_BYTES + OSLOTS * OUT_BYTES + 1024 /*align*/ + 512;
@@ -409,24 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         *reinterpret_cast<uint4*>(obuf + sw64(r, (uint32_t)(half * 2 + jj))) =
                             make_uint4(ow[jj][0], ow[jj][1], ow[jj][2], ow[jj][3]);
                 } else if (MODE == MODE_UPDATE) {
-                    // later updates: fp16 iterate in and out, 64-column chunks, 128-byte swizzle
+                    // later updates: X' / c = P' (X / c) with P' = a I + P, no input;
+                    // fp16 out, 64-column chunks, 128-byte swizzle
                     float v[32];
                     tmem_load_32x32(t_acc + c * 64 + half * 32, v);
-                    mbar_wait(&ein_full[islot], iphase, abort_flag, p.status);
-                    uint4 xw[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        xw[jj] = *reinterpret_cast<const uint4*>(ein + sw128(r, (uint32_t)(half * 4 + jj)));
-                    mbar_arrive(&ein_empty[islot]);  // this thread is done with the input slot
                     uint32_t ow[4][4];
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const uint32_t xs[4] = {xw[jj].x, xw[jj].y, xw[jj].z, xw[jj].w};
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
-                            const float x0 = h2f((uint16_t)(xs[h] & 0xFFFFu)), x1 = h2f((uint16_t)(xs[h] >> 16));
-                            const uint16_t b0 = f2h(scale * fmaf(p.ca, x0, c2 * v[8 * jj + 2 * h]));
-                            const uint16_t b1 = f2h(scale * fmaf(p.ca, x1, c2 * v[8 * jj + 2 * h + 1]));
+                            const uint16_t b0 = f2h(v[8 * jj + 2 * h]);
+                            const uint16_t b1 = f2h(v[8 * jj + 2 * h + 1]);
                             ow[jj][h] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                             if (p.want_rowsq) {
                                 const float o0 = h2f(b0), o1 = h2f(b1);
@@ -459,6 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                                 v[8 * jj + 2 * h] = fmaf(p.cb, lo, (p.cc * c2) * v[8 * jj + 2 * h]);
                                 v[8 * jj + 2 * h + 1] = fmaf(p.cb, hi, (p.cc * c2) * v[8 * jj + 2 * h + 1]);
                             }
+                        }
+                        if (C::FOLD) {
+                            // P' = a I + P, stored unscaled (P' multiplies X / c into X' / c);
+                            // c <= 1, so it stays near a in size
+                            const int dcol = ti * kBM + (int)r - (col0 + half * 32);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = c2 * v[e] + (e == dcol ? p.ca : 0.f);
                         }
                     } else {
 #pragma unroll

@@ -210,8 +210,10 @@ def newton_schulz_mixed(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarra
     The first iteration reads bf16-rounded operands of an fp32 iterate (the
     normalised input, held as a bf16 hi + lo pair), stores A and P = b A + c A A
     in bf16 and rounds its result to fp16.  Every later iteration holds X, A
-    and P in fp16.  All stored arrays are divided by a fixed per-matrix scale
-    -- X by c = ||X0||, A and P by c^2 -- so that an input far below unit norm
+    and P in fp16 and folds its a X term into the polynomial: P' = a I + b A +
+    c A A is rounded once and X' = P' X.  The stored arrays are divided by a
+    fixed per-matrix scale -- X by c = ||X0|| <= 1, A and the first P by c^2,
+    P' not at all (X' / c = P' X / c) -- so that an input far below unit norm
     keeps its precision in fp16; in exact arithmetic the scale cancels.
     Products accumulate exactly.  Used only to size the rounding error of tiny
     matrices, where a relative Frobenius error is dominated by a handful of
@@ -230,8 +232,8 @@ def newton_schulz_mixed(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarra
             xs = fp16_round((a * x + c2 * (P @ xb)) / cs)
         else:
             A = fp16_round(xs @ xs.T)
-            P = fp16_round(b * A + (c * c2) * (A @ A))
-            xs = fp16_round(a * xs + c2 * (P @ xs))
+            P = fp16_round(c2 * (b * A + (c * c2) * (A @ A)) + a * np.eye(A.shape[0]))
+            xs = fp16_round(P @ xs)
     return cs * xs
 
 
