@@ -9,7 +9,8 @@
 //                   small inputs stay inside fp16's range (A and P likewise as
 //                   A / c^2, P / c^2); two buffers used in turn (S5-S7)
 //       a16 / p16   A = X X^T and P = b A + c A A, m x m: bf16 in the first
-//                   iteration (on u), fp16 after (S5, S6)
+//                   iteration (on u), fp16 after (S5, S6); from the second
+//                   iteration on p16 holds P' = a I + P, unscaled
 //       rowsq       per (row, 256-column tile, column half) sums of O^2 from the
 //                   last iteration (S8)
 //       v           second moment, fp32 [m] (S8)
@@ -43,7 +44,7 @@ struct DevSchedule {
 };
 
 // bits of the device status word
-enum { STATUS_TIMEOUT = 1 };
+enum { STATUS_TIMEOUT = 1, STATUS_PAIR = 2 };  // PAIR: an SM pair did not get one shared TMEM allocation
 
 enum GemmMode { MODE_GRAM = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
 
@@ -109,10 +110,10 @@ struct GemmGroup {
 struct GemmParams {
     CUtensorMap map_a[kMaxGroupsPerLaunch];     // left operand (K-major)
     CUtensorMap map_b[kMaxGroupsPerLaunch];     // right operand: 256-row K-major box (gram / poly), MN-major X (update)
-    CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, update hi half of X
-    CUtensorMap map_ein2[kMaxGroupsPerLaunch];  // epilogue input: update lo half of X
-    CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: bf16 tile; update: hi half of X'
-    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored bf16 tile; update: lo half of X'
+    CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, first update hi half of u
+    CUtensorMap map_ein2[kMaxGroupsPerLaunch];  // epilogue input: first update lo half of u
+    CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: A / P tile; update: X' tile
+    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored tile
     GemmGroup grp[kMaxGroupsPerLaunch];
     const int4* tiles;       // {group slot, index in group, tile row, tile col}
     int32_t ntiles;
@@ -122,6 +123,7 @@ struct GemmParams {
     float ca, cb, cc;        // (a, b, c) of this iteration
     int32_t first, last, want_rowsq;
     int32_t f16;             // operands and results fp16 (iterations after the first); else bf16
+    int32_t pair;            // update on SM pairs: tiles are 256 x 256 (tile row and column in units of 256)
     int* status;
 };
 

@@ -38,6 +38,8 @@ cudaError_t launch_schedule_advance(float*, DevSchedule*, cudaStream_t);
 cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, int, int, cudaStream_t);
 cudaError_t launch_scale_f16(float*, const uint16_t*, const float*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
+cudaError_t ns_update_pair_configure();
+cudaError_t launch_ns_update_pair(const GemmParams&, int, cudaStream_t);
 template <int MODE, bool F16>
 cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
 template <int MODE>
@@ -73,6 +75,7 @@ struct Group {
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
+    CUtensorMap map_x_w32[2];  // 32 x 32 boxes, 64-byte swizzle: stores of the SM-pair update's warps
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
@@ -80,6 +83,7 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     int32_t gram_off = 0, gram_n = 0;
     int32_t poly_off = 0, poly_n = 0;
     int32_t upd_off = 0, upd_n = 0;
+    int32_t pair_off = 0, pair_n = 0;  // 256 x 256 update tiles for SM pairs (0: chunk not eligible)
 };
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -118,6 +122,7 @@ struct muon_s {
     int4* d_gemm_tiles = nullptr;
     // pre-built GEMM parameter blocks: [iteration][chunk][mode]
     std::vector<GemmParams> gparams;
+    bool pair_update = true;        // folded updates on SM pairs where the shapes allow
     std::string last_error;
     // profiling: one event before every launch plus one at the end
     bool profiling = false;
@@ -496,6 +501,23 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         emit(gram, ch.gram_off, ch.gram_n);
         emit(poly, ch.poly_off, ch.poly_n);
         emit(upd, ch.upd_off, ch.upd_n);
+        // the folded updates (second iteration on) run on SM pairs when every group of the
+        // chunk tiles exactly into 256 x 256 pair tiles
+        bool pair_fit = true;
+        for (int sl = 0; sl < ch.ng; ++sl) {
+            const Group& g = h->groups[g0 + sl];
+            pair_fit = pair_fit && g.m % 256 == 0 && g.n % 256 == 0;
+        }
+        if (pair_fit && h->pair_update) {
+            std::vector<T> pr;
+            for (int sl = 0; sl < ch.ng; ++sl) {
+                const Group& g = h->groups[g0 + sl];
+                for (int idx = 0; idx < g.count; ++idx)
+                    for (int ti = 0; ti < g.m / 256; ++ti)
+                        for (int tj = 0; tj < g.n / 256; ++tj) pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+            }
+            emit(pr, ch.pair_off, ch.pair_n);
+        }
         h->chunks.push_back(ch);
     }
     const size_t o_gtiles = take(sizeof(int4) * std::max<size_t>(gemm_tiles.size(), 1));
@@ -545,7 +567,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                  encode_bf16_3d(enc, &g.map_x_k256[b], g.x16[b], g.n, g.m, g.count, g.ldx, 2 * kBM) &&
                  encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64) &&
                  encode_3d(enc, &g.map_x_o32[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
-                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B);
+                           g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                 encode_3d(enc, &g.map_x_w32[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
+                           g.ldx, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_u_hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32, kBM,
                        CU_TENSOR_MAP_SWIZZLE_64B) &&
@@ -609,7 +633,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                                 cudaMemcpyHostToDevice) == cudaSuccess);
     float hpv[HP_COUNT] = {cfg.lr, cfg.momentum, cfg.beta2, cfg.weight_decay};
     ok = ok && cudaMemcpy(h->hp, hpv, sizeof(hpv), cudaMemcpyHostToDevice) == cudaSuccess;
-    ok = ok && ns_gemm_tc_configure() == cudaSuccess;
+    ok = ok && ns_gemm_tc_configure() == cudaSuccess && ns_update_pair_configure() == cudaSuccess;
     if (!ok) {
         cudaFree(h->arena);
         delete h;
@@ -641,6 +665,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 } else if (mode == MODE_POLY) {
                     gp.tiles = h->d_gemm_tiles + ch.poly_off;
                     gp.ntiles = ch.poly_n;
+                } else if (it > 0 && ch.pair_n > 0) {
+                    gp.tiles = h->d_gemm_tiles + ch.pair_off;
+                    gp.ntiles = ch.pair_n;
+                    gp.pair = 1;
                 } else {
                     gp.tiles = h->d_gemm_tiles + ch.upd_off;
                     gp.ntiles = ch.upd_n;
@@ -685,7 +713,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         // later updates (a on the diagonal of P): no input, X' out in 64-column boxes
                         gp.map_ein[sl] = g.map_u_hi;
                         gp.map_ein2[sl] = g.map_u_lo;
-                        gp.map_out[sl] = first ? g.map_x_o32[out_buf] : g.map_x_k[out_buf];
+                        gp.map_out[sl] = first ? g.map_x_o32[out_buf] : (gp.pair ? g.map_x_w32[out_buf] : g.map_x_k[out_buf]);
                         G.opl16 = g.p16;
                         G.opr16 = xin16;
                     }
@@ -739,8 +767,9 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                         e = f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
                                 : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s);
                     if (mode == MODE_UPDATE)
-                        e = f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
-                                : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s);
+                        e = gp.pair ? launch_ns_update_pair(gp, h->num_sms, s)
+                                    : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
+                                           : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s));
                     MUON_CUDA(h, e);
                 } else {
                     for (int sl = 0; sl < gp.ngroups; ++sl) {
@@ -839,6 +868,7 @@ int muon_sync_status(muon_handle h, void* stream) {
     if (st != 0) {
         MUON_CUDA(h, cudaMemset(h->status, 0, sizeof(int)));
         if (st & STATUS_TIMEOUT) return fail(h, MUON_ERR_TIMEOUT, "a kernel's bounded wait gave up");
+        if (st & STATUS_PAIR) return fail(h, MUON_ERR_CUDA, "an SM pair did not get one shared TMEM allocation");
     }
     return MUON_OK;
 }

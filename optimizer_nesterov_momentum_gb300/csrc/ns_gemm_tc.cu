@@ -9,6 +9,8 @@
 //   MODE_UPDATE  X' = s (a X + P X)       on the first iteration
 //                X' = P X                 on later ones, whose POLY adds a to the
 //                                         diagonal of P: a X + P X = (a I + P) X
+//                                         (these run on SM pairs, ns_update_pair.cu,
+//                                         where the shapes tile by 256)
 //
 // A and P are symmetric: GRAM and POLY compute 128 x 256 tiles that reach the
 // diagonal or lie above it, and store every 128 x 128 block above the

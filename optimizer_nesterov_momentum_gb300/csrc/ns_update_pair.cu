@@ -1,0 +1,395 @@
+// Newton-Schulz update on SM pairs: X' = P' X for the iterations after the
+// first ("modded-nanogpt 50B-token" write-up, section "Muon from the source":
+// X <- a X + (b A + c A^2) X, with a I folded into P' = a I + b A + c A^2 by
+// the polynomial kernel), on tcgen05.mma.cta_group::2.
+//
+// The two CTAs of a cluster share one 256 x 256 output tile: CTA r holds rows
+// 128 r .. 128 r + 127 of the tile's left operand (P' rows, K-major) and
+// columns 128 r .. 128 r + 127 of its right operand (X rows, MN-major), and its
+// own TMEM receives its 128 rows of the product.  The MMA, issued by CTA 0
+// (M = 256, N = 256, K = 16), reads both CTAs' shared memory.  Each SM thus
+// stages 32 KB per 64-deep k-block for the same 4.2 MFLOP that a one-SM
+// 128 x 256 tile stages 48 KB for: the update's mainloop is bound by how fast
+// shared memory fills, so this is 1.5x the math per staged byte.
+//
+// Warp roles (320 threads per CTA, one CTA per SM):
+//   warp 0     TMA producer (both CTAs): loads its own halves into its own
+//              stage ring; every copy signals CTA 0's "full" mbarrier, which
+//              CTA 0's producer armed with the bytes of both halves
+//   warp 1     TMEM: one pair-wide 512-column allocation, made together by
+//              warp 1 of both CTAs (the accumulator is double-buffered); CTA
+//              0's lane 0 issues the MMAs and commits stage releases and
+//              "accumulator full" to both CTAs' mbarriers at once (multicast
+//              commit)
+//   warps 2-9  epilogue (both CTAs): drain this CTA's 128 accumulator rows,
+//              round to fp16, stage and TMA-store them warp by warp (each warp
+//              its own 32 x 32 blocks, no barrier across warps); NorMuon row
+//              sums on the last iteration; then release the accumulator on CTA
+//              0's mbarrier
+// Every mbarrier wait is bounded (2 s) and raises the status word on expiry.
+// The allocation is checked before use: both CTAs must see the same TMEM
+// address, else the kernel reports the mismatch in the status word and does
+// no work.
+#include "muon_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace muon {
+namespace {
+
+constexpr int kPairThreads = 320;
+constexpr int kPairStages = 6;
+constexpr int kPairA = kBM * kBK * 2;    // 16 KB: this CTA's 128 rows of P'
+constexpr int kPairB = 128 * kBK * 2;    // 16 KB: this CTA's 128 columns of X (two 64-column blocks)
+constexpr int kPairStage = kPairA + kPairB;
+constexpr int kWarpSlot = 32 * 32 * 2;   // one warp's 32 x 32 fp16 output block (64-byte rows, 64-byte swizzle)
+constexpr int kWarpSlots = 2;            // staging slots per epilogue warp
+constexpr int kPairEpiWarps = 8;
+constexpr int kPairOutBytes = kPairEpiWarps * kWarpSlots * kWarpSlot;
+constexpr int kPairSmem = kPairStages * kPairStage + kPairOutBytes + 1024 + 512;
+static_assert(kPairSmem <= 232448, "shared memory budget");
+constexpr uint32_t kPairIdesc = make_idesc_16bit(256, 256, /*b_mn_major=*/true, /*fp16=*/true);
+constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------ cluster / pair PTX
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(p)), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// All threads of both CTAs.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// Tensor copy into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (`bar` is a cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` in both CTAs of the pair when this thread's MMAs so far complete.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 columns into r[], without waiting: the registers are valid only
+// after tmem_wait_loads().
+__device__ __forceinline__ void tmem_load_32x32_async(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_loads() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    k_ns_update_pair(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kPairStages * kPairA;
+    uint8_t* sO = sB + kPairStages * kPairB;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sO + kPairOutBytes);  // CTA 0's are used
+    uint64_t* empty = full + kPairStages;
+    uint64_t* tfull = empty + kPairStages;  // [2]
+    uint64_t* tempty = tfull + 2;           // [2] CTA 0's are used: 8 warps of each CTA arrive
+    uint64_t* mma_done = tempty + 2;        // abort path only
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* pair_ok = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 2 * kPairEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *tmem_slot = kNoTmem;
+        *abort_flag = 0;
+        *pair_ok = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();  // barriers initialised and the allocation written in both CTAs
+    tc_fence_after();
+    if (threadIdx.x == 32) {
+        const uint32_t mine = *tmem_slot;
+        const uint32_t peer = ld_cluster_u32(cluster_addr(tmem_slot, rank ^ 1u));
+        const int ok = (mine != kNoTmem && mine == peer) ? 1 : 0;
+        *pair_ok = ok;
+        if (!ok) {
+            *abort_flag = 1;
+            atomicOr(p.status, STATUS_PAIR);
+        }
+    }
+    __syncthreads();
+    const bool run = *pair_ok != 0;
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t tacc[2] = {tbase, tbase + 256u};
+    bool mma_any = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ operand producer
+        if (lane == 0 && run) {
+            for (int g = 0; g < p.ngroups; ++g) {
+                tma_prefetch_desc(&p.map_a[g]);
+                tma_prefetch_desc(&p.map_b[g]);
+            }
+            const uint32_t full0 = cluster_addr(&full[0], 0);  // CTA 0's full barriers
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = pair; t < p.ntiles && ok; t += npairs) {
+                const int4 tile = p.tiles[t];
+                const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
+                const int nkb = (p.grp[g].m + kBK - 1) / kBK;
+                const int row0 = ti * 2 * kBM + (int)rank * kBM;
+                const int col0 = tj * 256 + (int)rank * 128;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPairStage);
+                    const uint32_t bar = full0 + (uint32_t)(stage * 8);
+                    tma_load_3d_pair(sA + stage * kPairA, &p.map_a[g], bar, kb * kBK, row0, idx);
+                    tma_load_3d_pair(sB + stage * kPairB, &p.map_b[g], bar, col0, kb * kBK, idx);
+                    tma_load_3d_pair(sB + stage * kPairB + 64 * kBK * 2, &p.map_b[g], bar, col0 + 64, kb * kBK, idx);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (CTA 0)
+        if (lane == 0 && run && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_base = smem_u32(sA);
+            const uint32_t b_base = smem_u32(sB);
+            for (int t = pair; t < p.ntiles && ok; t += npairs) {
+                const int4 tile = p.tiles[t];
+                const int nkb = (p.grp[tile.x].m + kBK - 1) / kBK;
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t adesc = make_sdesc_sw128(a_base + stage * kPairA + kk * 32, 16, 1024);
+                        const uint64_t bdesc =
+                            make_sdesc_sw128(b_base + stage * kPairB + kk * (16 * 128), 64 * kBK * 2, 1024);
+                        umma_f16_pair(tacc[acc], adesc, bdesc, kPairIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        mma_any = true;
+                    }
+                    umma_commit_pair(&empty[stage]);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && mma_any) {
+                // the MMAs in flight read both CTAs' stages and write both TMEMs
+                umma_commit_pair(mma_done);
+                mbar_wait_drain(mma_done, 0, 100000000ull);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        // Each warp drains its 32 TMEM lanes x 32 columns of every 64-column chunk and
+        // stores that 32 x 32 block itself from a ring of private staging slots: no
+        // barrier across warps.
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        uint8_t* wst = sO + (warp - 2) * (kWarpSlots * kWarpSlot);
+        const uint32_t tempty0 = cluster_addr(&tempty[0], 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int wchunk = 0;  // chunks this warp has staged
+        for (int t = pair; run && t < p.ntiles; t += npairs) {
+            const int4 tile = p.tiles[t];
+            const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
+            const GemmGroup& G = p.grp[g];
+            const int row0 = ti * 2 * kBM + (int)rank * kBM + quad * 32;  // this warp's first row
+            mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
+            tc_fence_after();
+            const uint32_t t_acc = tacc[acc] + lane_off + (uint32_t)(half * 32);
+            float sumsq = 0.f;
+            // all four chunks in flight at once, one wait
+            uint32_t raw[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_load_32x32_async(t_acc + c * 64, raw[c]);
+            tmem_wait_loads();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t ow[4][4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const __half2 hv = __floats2half2_rn(__uint_as_float(raw[c][8 * jj + 2 * h]),
+                                                             __uint_as_float(raw[c][8 * jj + 2 * h + 1]));
+                        ow[jj][h] = *reinterpret_cast<const uint32_t*>(&hv);
+                        if (p.want_rowsq) {
+                            const float2 o = __half22float2(hv);
+                            sumsq = fmaf(o.x, o.x, sumsq);
+                            sumsq = fmaf(o.y, o.y, sumsq);
+                        }
+                    }
+                }
+                uint8_t* slot = wst + (wchunk % kWarpSlots) * kWarpSlot;
+                // the store issued kWarpSlots chunks ago read this slot: it must be done with it
+                if (wchunk >= kWarpSlots && lane == 0) bulk_wait_read<kWarpSlots - 1>();
+                __syncwarp();
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    *reinterpret_cast<uint4*>(slot + sw64((uint32_t)lane, (uint32_t)jj)) =
+                        make_uint4(ow[jj][0], ow[jj][1], ow[jj][2], ow[jj][3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&p.map_out[g], slot, tj * 256 + c * 64 + half * 32, row0, idx);
+                    bulk_commit();
+                }
+                ++wchunk;
+            }
+            if (p.want_rowsq) {
+                const int row = row0 + lane;
+                if (row < G.m) G.rowsq[(((int64_t)idx * G.m + row) * G.ntile_n + tj) * 2 + half] = sumsq;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait<0>();
+    }
+
+    if (*abort_flag && run) {
+        // copies of the peer may still be landing in this CTA's stages (they are
+        // counted on CTA 0's barriers): give them time before the CTA can exit
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 2000000ull) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no MMA, copy or remote arrival of the pair is still in flight
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        if (tbase != kNoTmem) tmem_dealloc_pair(tbase, 512);
+    }
+}
+
+cudaError_t ns_update_pair_configure() {
+    return cudaFuncSetAttribute(k_ns_update_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+}
+
+// p.tiles: 256 x 256 tiles {group slot, index, tile row (of 256), tile column (of 256)}.
+cudaError_t launch_ns_update_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
+    if (p.ntiles <= 0) return cudaSuccess;
+    const int pairs = p.ntiles < num_sms / 2 ? p.ntiles : num_sms / 2;
+    k_ns_update_pair<<<2 * pairs, kPairThreads, kPairSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace muon

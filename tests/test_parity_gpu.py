@@ -213,6 +213,25 @@ def test_extreme_gradient_scales(gscale):
     errs.assert_within()
 
 
+def test_sm_pair_update_shapes_two_steps():
+    """Every group tiles into 256 x 256 blocks, so the updates after the first run on
+    SM pairs (tcgen05.mma.cta_group::2); tall and wide matrices, NorMuon row sums."""
+    shapes = [Shape(256, 512), Shape(512, 256), Shape(256, 256), Shape(512, 1024, lr_mul=2.0)]
+    params, grads = _inputs(shapes, 2, seed=31)
+    errs, _, _ = run_parity(shapes, params, grads)
+    errs.assert_within()
+
+
+@pytest.mark.parametrize("gscale", [1e-12, 1e4])
+def test_sm_pair_update_extreme_scales(gscale):
+    shapes = [Shape(256, 512), Shape(512, 256)]
+    params, grads = _inputs(shapes, 2, seed=37, grad_dtype="f32")
+    grads = [[(g * gscale).contiguous() for g in gs] for gs in grads]
+    params = [torch.zeros_like(p) for p in params]
+    errs, _, _ = run_parity(shapes, params, grads, grad_dtype="f32")
+    errs.assert_within()
+
+
 def test_zero_gradient_keeps_params_and_is_finite():
     shapes = [Shape(64, 192), Shape(192, 64)]
     opt = make_optimizer(shapes, lr=0.03)
