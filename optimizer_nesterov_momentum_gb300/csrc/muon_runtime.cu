@@ -40,9 +40,9 @@ cudaError_t launch_scale_f16(float*, const uint16_t*, const float*, int, int, in
 cudaError_t ns_gemm_tc_configure();
 cudaError_t ns_update_pair_configure();
 cudaError_t launch_ns_update_pair(const GemmParams&, int, cudaStream_t);
-cudaError_t ns_sym_pair_configure();
-template <int MODE, bool F16>
-cudaError_t launch_ns_sym_pair(const GemmParams&, int, cudaStream_t);
+cudaError_t ns_gram_pair_configure();
+template <bool F16>
+cudaError_t launch_ns_gram_pair(const GemmParams&, int, cudaStream_t);
 template <int MODE, bool F16>
 cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
 template <int MODE>
@@ -79,7 +79,7 @@ struct Group {
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
     CUtensorMap map_x_w32[2];  // 32 x 32 boxes, 64-byte swizzle: stores of the SM-pair update's warps
-    CUtensorMap map_a_w32, map_p_w32;  // the same for A and P (SM-pair Gram / polynomial)
+    CUtensorMap map_a_w32;     // the same for A (SM-pair Gram)
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
@@ -89,7 +89,6 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     int32_t upd_off = 0, upd_n = 0;
     int32_t pair_off = 0, pair_n = 0;  // 256 x 256 update tiles for SM pairs (0: chunk not eligible)
     int32_t spg_off = 0, spg_n = 0;    // 256 x 256 Gram tiles (J >= I) for SM pairs
-    int32_t spp_off = 0, spp_n = 0;    // the same, ordered for the polynomial
 };
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -523,18 +522,14 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         for (int tj = 0; tj < g.n / 256; ++tj) pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
             }
             emit(pr, ch.pair_off, ch.pair_n);
-            std::vector<T> sg, sp;
+            std::vector<T> sg;
             for (int sl = 0; sl < ch.ng; ++sl) {
                 const Group& g = h->groups[g0 + sl];
                 for (int idx = 0; idx < g.count; ++idx)
                     for (int ti = 0; ti < g.m / 256; ++ti)
-                        for (int tj = ti; tj < g.m / 256; ++tj) {
-                            sg.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
-                            sp.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
-                        }
+                        for (int tj = ti; tj < g.m / 256; ++tj) sg.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
             }
             emit(sg, ch.spg_off, ch.spg_n);
-            emit(sp, ch.spp_off, ch.spp_n);
         }
         h->chunks.push_back(ch);
     }
@@ -590,8 +585,6 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                            g.ldx, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_a_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.a16, g.m, g.m, g.count, g.lda, 32, 32,
-                       CU_TENSOR_MAP_SWIZZLE_64B) &&
-             encode_3d(enc, &g.map_p_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.p16, g.m, g.m, g.count, g.lda, 32, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_u_hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32, kBM,
@@ -657,7 +650,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     float hpv[HP_COUNT] = {cfg.lr, cfg.momentum, cfg.beta2, cfg.weight_decay};
     ok = ok && cudaMemcpy(h->hp, hpv, sizeof(hpv), cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && ns_gemm_tc_configure() == cudaSuccess && ns_update_pair_configure() == cudaSuccess &&
-         ns_sym_pair_configure() == cudaSuccess;
+         ns_gram_pair_configure() == cudaSuccess;
     if (!ok) {
         cudaFree(h->arena);
         delete h;
@@ -690,10 +683,6 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 } else if (mode == MODE_GRAM) {
                     gp.tiles = h->d_gemm_tiles + ch.gram_off;
                     gp.ntiles = ch.gram_n;
-                } else if (mode == MODE_POLY && ch.spp_n > 0) {
-                    gp.tiles = h->d_gemm_tiles + ch.spp_off;
-                    gp.ntiles = ch.spp_n;
-                    gp.pair = 1;
                 } else if (mode == MODE_POLY) {
                     gp.tiles = h->d_gemm_tiles + ch.poly_off;
                     gp.ntiles = ch.poly_n;
@@ -732,8 +721,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     } else if (mode == MODE_POLY) {
                         gp.map_a[sl] = g.map_a_k;
                         gp.map_b[sl] = g.map_a_k256;
-                        gp.map_ein[sl] = gp.pair ? g.map_a_w32 : g.map_a_k;
-                        gp.map_out[sl] = gp.pair ? g.map_p_w32 : g.map_p_k;
+                        gp.map_ein[sl] = g.map_a_k;
+                        gp.map_out[sl] = g.map_p_k;
                         gp.map_out2[sl] = g.map_p_mir;
                         G.out16 = g.p16;
                         G.opl16 = g.a16;
@@ -793,15 +782,11 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                     const bool f16 = it > 0;
                     cudaError_t e = cudaSuccess;
                     if (mode == MODE_GRAM && gp.pair)
-                        e = f16 ? launch_ns_sym_pair<MODE_GRAM, true>(gp, h->num_sms, s)
-                                : launch_ns_sym_pair<MODE_GRAM, false>(gp, h->num_sms, s);
+                        e = f16 ? launch_ns_gram_pair<true>(gp, h->num_sms, s) : launch_ns_gram_pair<false>(gp, h->num_sms, s);
                     else if (mode == MODE_GRAM)
                         e = f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, s)
                                 : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, s);
-                    if (mode == MODE_POLY && gp.pair)
-                        e = f16 ? launch_ns_sym_pair<MODE_POLY, true>(gp, h->num_sms, s)
-                                : launch_ns_sym_pair<MODE_POLY, false>(gp, h->num_sms, s);
-                    else if (mode == MODE_POLY)
+                    if (mode == MODE_POLY)
                         e = f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
                                 : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s);
                     if (mode == MODE_UPDATE)

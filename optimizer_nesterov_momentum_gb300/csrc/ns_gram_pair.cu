@@ -1,27 +1,22 @@
-// The symmetric Newton-Schulz products on SM pairs ("modded-nanogpt 50B-token"
-// write-up, section "Muon from the source"):
+// The Gram product of the Newton-Schulz iteration on SM pairs ("modded-nanogpt
+// 50B-token" write-up, section "Muon from the source"):
 //
-//   MODE_GRAM    A = sc * X X^T        (sc = (s / c)^2 on the first iteration, else 1)
-//   MODE_POLY    P = b A + c A A       (first iteration, bf16)
-//                P' = c^2 (b A + c c^2 A A) + a I   (later iterations, fp16; the
-//                update then needs no a X term, and P' multiplies X / c)
+//   A = sc * X X^T      (sc = (s / c)^2 on the first iteration, else 1)
 //
 // with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) issued by CTA 0 of a
 // two-CTA cluster.  A pair tile is the 256 x 256 block (I, J), J >= I, of the
-// symmetric result.  CTA r stages rows 256 I + 128 r .. + 127 of the operand
-// (the left operand's half) and rows 256 J + 128 r .. + 127 (the right
-// operand's half, both K-major), so an off-diagonal tile stages 32 KB per SM
-// per 64-deep k-block and a diagonal tile, whose two halves are the same rows,
-// 16 KB.  CTA r's TMEM receives rows 128 r .. + 127 of the tile.
+// symmetric result.  CTA r stages rows 256 I + 128 r .. + 127 of X (the left
+// operand's half) and rows 256 J + 128 r .. + 127 (the right operand's half,
+// both K-major), so an off-diagonal tile stages 32 KB per SM per 64-deep
+// k-block and a diagonal tile, whose two halves are the same rows, 16 KB.
+// CTA r's TMEM receives rows 128 r .. + 127 of the tile.
 //
 // The epilogue works warp by warp: warp (quad, half) owns TMEM lanes
 // 32 quad .. + 31 and columns 32 half .. + 31 of each 64-column chunk, i.e.
 // four 32 x 32 blocks per tile.  It stores each block, and for an
 // off-diagonal tile (I < J) also its transpose at (J, I), from its own ring of
 // shared-memory slots; a diagonal tile is computed whole (both triangles) and
-// stored once.  POLY reads the matching 32 x 32 block of A for its b A term
-// by TMA into the warp's own input slots, issued before the accumulator is
-// ready.  No barrier spans warps.
+// stored once.  No barrier spans warps.
 //
 // Warp 0: TMA producer (both CTAs), warp 1: pair-wide TMEM allocation (both)
 // and the MMA issuer (CTA 0), warps 2-9: epilogue (both).  All mbarrier waits
@@ -40,39 +35,31 @@ constexpr int kBlk = 32 * 32 * 2;        // one 32 x 32 16-bit block (64-byte ro
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
 
-template <int MODE>
-struct SymPairCfg {
-    static constexpr bool POLY = MODE == MODE_POLY;
-    static constexpr int STAGES = POLY ? 4 : 5;
-    static constexpr int OUT_SLOTS = 4;                // per warp: blocks and mirrors in flight
-    static constexpr int IN_SLOTS = POLY ? 2 : 0;      // per warp: A blocks (POLY)
-    static constexpr int SMEM = STAGES * kSymStage + kEpiWarps * (OUT_SLOTS + IN_SLOTS) * kBlk + 1024 + 512;
-    static_assert(SMEM <= 232448, "shared memory budget");
-};
+constexpr int kGramStages = 5;
+constexpr int kOutSlots = 4;  // per warp: blocks and mirrors in flight
+constexpr int kGramSmem = kGramStages * kSymStage + kEpiWarps * kOutSlots * kBlk + 1024 + 512;
+static_assert(kGramSmem <= 232448, "shared memory budget");
 
 }  // namespace
 
 using namespace pair;
 
-template <int MODE, bool F16>
+template <bool F16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
-    k_ns_sym_pair(const __grid_constant__ GemmParams p) {
-    using C = SymPairCfg<MODE>;
-    constexpr int STAGES = C::STAGES;
+    k_ns_gram_pair(const __grid_constant__ GemmParams p) {
+    constexpr int STAGES = kGramStages;
     constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/false, F16);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sS = smem;                                   // STAGES x (left | right)
-    uint8_t* sO = sS + STAGES * kSymStage;                // per warp OUT_SLOTS blocks
-    uint8_t* sI = sO + kEpiWarps * C::OUT_SLOTS * kBlk;   // per warp IN_SLOTS blocks
-    uint64_t* full = reinterpret_cast<uint64_t*>(sI + kEpiWarps * C::IN_SLOTS * kBlk);  // CTA 0's are used
+    uint8_t* sO = sS + STAGES * kSymStage;                // per warp kOutSlots blocks
+    uint64_t* full = reinterpret_cast<uint64_t*>(sO + kEpiWarps * kOutSlots * kBlk);  // CTA 0's are used
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;   // [2]
     uint64_t* tempty = tfull + 2;       // [2] CTA 0's: 8 warps of each CTA arrive
     uint64_t* mma_done = tempty + 2;    // abort path only
-    uint64_t* in_full = mma_done + 1;   // [kEpiWarps][2] (POLY)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_full + 2 * kEpiWarps);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* pair_ok = abort_flag + 1;
 
@@ -92,7 +79,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             mbar_init(&tempty[a], 2 * kEpiWarps);
         }
         mbar_init(mma_done, 1);
-        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&in_full[i], 1);
         *tmem_slot = kNoTmem;
         *abort_flag = 0;
         *pair_ok = 0;
@@ -131,7 +117,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = p.tiles[t];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
-                const int K = (MODE == MODE_GRAM) ? p.grp[g].n : p.grp[g].m;
+                const int K = p.grp[g].n;
                 const int nkb = (K + kBK - 1) / kBK;
                 const bool diag = ti == tj;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -163,7 +149,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             const uint32_t s_base = smem_u32(sS);
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = p.tiles[t];
-                const int K = (MODE == MODE_GRAM) ? p.grp[tile.x].n : p.grp[tile.x].m;
+                const int K = p.grp[tile.x].n;
                 const int nkb = (K + kBK - 1) / kBK;
                 const bool diag = tile.z == tile.w;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
@@ -210,43 +196,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
         const int quad = warp & 3;
         const int half = ew >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        uint8_t* wout = sO + ew * (C::OUT_SLOTS * kBlk);
-        uint8_t* win = sI + ew * (C::IN_SLOTS > 0 ? C::IN_SLOTS : 1) * kBlk;
-        uint64_t* wbar = &in_full[2 * ew];
+        uint8_t* wout = sO + ew * (kOutSlots * kBlk);
         const uint32_t tempty0 = cluster_addr(&tempty[0], 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        int nout = 0;                       // output slots used so far (one bulk group each)
-        uint32_t in_phase[2] = {0u, 0u};    // POLY: parity of the next wait on each input slot
-        bool in_pending[2] = {false, false};
-        if (C::POLY && lane == 0)
-            for (int g = 0; g < p.ngroups; ++g) tma_prefetch_desc(&p.map_ein[g]);
+        int nout = 0;  // output slots used so far (one bulk group each)
         for (int t = pr; run && t < p.ntiles; t += npairs) {
             const int4 tile = p.tiles[t];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             const bool diag = ti == tj;
-            const int rl = (int)rank * kBM + quad * 32;  // this warp's first row within the tile
-            const int row0 = ti * 256 + rl;
-            // POLY: this warp's A blocks for chunks 0 and 1, before the accumulator is ready
-            if (C::POLY && lane == 0) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    mbar_arrive_expect_tx(&wbar[c], kBlk);
-                    tma_load_3d(win + c * kBlk, &p.map_ein[g], &wbar[c], tj * 256 + c * 64 + half * 32, row0, idx);
-                    in_pending[c] = true;
-                }
-            }
+            const int row0 = ti * 256 + (int)rank * kBM + quad * 32;  // this warp's first row
             mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
             tc_fence_after();
             uint32_t raw[2][32];
             const uint32_t t_acc = tbase + (uint32_t)(acc * 256) + lane_off + (uint32_t)(half * 32);
-
-            const float cs = p.iter_scale[G.sub0 + idx];
-            const float c2 = cs * cs;
             float scale = 1.f;
-            if (MODE == MODE_GRAM && p.first) {
-                const float s = p.norm_scale[G.sub0 + idx] / cs;
+            if (p.first) {
+                const float s = p.norm_scale[G.sub0 + idx] / p.iter_scale[G.sub0 + idx];
                 scale = s * s;
             }
 #pragma unroll
@@ -263,55 +230,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                         if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
                     }
                 }
-                const int cl = c * 64 + half * 32;  // this block's first column within the tile
-                float v[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw[c & 1][e]);
-                if (C::POLY) {
-                    const int sl = c & 1;
-                    mbar_wait(&wbar[sl], in_phase[sl], abort_flag, p.status);
-                    in_phase[sl] ^= 1u;
-                    in_pending[sl] = false;
-                    uint4 aw[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        aw[jj] = *reinterpret_cast<const uint4*>(win + sl * kBlk + sw64((uint32_t)lane, (uint32_t)jj));
-                    __syncwarp();  // every lane has read the slot
-                    if (lane == 0 && c + 2 < 4) {
-                        mbar_arrive_expect_tx(&wbar[sl], kBlk);
-                        tma_load_3d(win + sl * kBlk, &p.map_ein[g], &wbar[sl], tj * 256 + (c + 2) * 64 + half * 32,
-                                    row0, idx);
-                        in_pending[sl] = true;
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const uint32_t ws[4] = {aw[jj].x, aw[jj].y, aw[jj].z, aw[jj].w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const float a0 = x2f<F16>((uint16_t)(ws[h] & 0xFFFFu));
-                            const float a1 = x2f<F16>((uint16_t)(ws[h] >> 16));
-                            v[8 * jj + 2 * h] = fmaf(p.cb, a0, (p.cc * c2) * v[8 * jj + 2 * h]);
-                            v[8 * jj + 2 * h + 1] = fmaf(p.cb, a1, (p.cc * c2) * v[8 * jj + 2 * h + 1]);
-                        }
-                    }
-                    if (F16) {
-                        // P' = c^2 P / c^2 + a I, unscaled (see the header)
-                        const int dcol = (diag && rl == cl) ? lane : -1;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = c2 * v[e] + (e == dcol ? p.ca : 0.f);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] *= scale;
-                }
+                const int col0 = tj * 256 + c * 64 + half * 32;  // this block's first column
                 uint16_t b[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) b[e] = f2x<F16>(v[e]);
+                for (int e = 0; e < 32; ++e) b[e] = f2x<F16>(scale * __uint_as_float(raw[c & 1][e]));
 
-                // this block at (row0, tile column cl)
+                // this block at (row0, col0)
                 {
-                    uint8_t* slot = wout + (nout % C::OUT_SLOTS) * kBlk;
-                    if (nout >= C::OUT_SLOTS && lane == 0) bulk_wait_read<C::OUT_SLOTS - 1>();
+                    uint8_t* slot = wout + (nout % kOutSlots) * kBlk;
+                    if (nout >= kOutSlots && lane == 0) bulk_wait_read<kOutSlots - 1>();
                     __syncwarp();
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -325,15 +252,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&p.map_out[g], slot, tj * 256 + cl, row0, idx);
+                        tma_store_3d(&p.map_out[g], slot, col0, row0, idx);
                         bulk_commit();
                     }
                     ++nout;
                 }
                 if (!diag) {
-                    // its transpose at (tile column cl, row0): element (lane, e) goes to row e, column lane
-                    uint8_t* slot = wout + (nout % C::OUT_SLOTS) * kBlk;
-                    if (nout >= C::OUT_SLOTS && lane == 0) bulk_wait_read<C::OUT_SLOTS - 1>();
+                    // its transpose at (col0, row0): element (lane, e) goes to row e, column lane
+                    uint8_t* slot = wout + (nout % kOutSlots) * kBlk;
+                    if (nout >= kOutSlots && lane == 0) bulk_wait_read<kOutSlots - 1>();
                     __syncwarp();
                     const uint32_t cj = (uint32_t)lane >> 3, cb2 = ((uint32_t)lane & 7u) * 2u;
 #pragma unroll
@@ -342,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&p.map_out[g], slot, row0, tj * 256 + cl, idx);
+                        tma_store_3d(&p.map_out[g], slot, row0, col0, idx);
                         bulk_commit();
                     }
                     ++nout;
@@ -350,12 +277,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
-        }
-        if (C::POLY && lane == 0) {
-            // input copies of an aborted run still in flight must land before the CTA exits
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl)
-                if (in_pending[sl]) mbar_wait_drain(&wbar[sl], in_phase[sl], 100000000ull);
         }
         if (lane == 0) bulk_wait<0>();
     }
@@ -377,32 +298,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     }
 }
 
-template <int MODE, bool F16>
-static cudaError_t configure_sym_pair() {
-    return cudaFuncSetAttribute(k_ns_sym_pair<MODE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SymPairCfg<MODE>::SMEM);
-}
-
-cudaError_t ns_sym_pair_configure() {
-    cudaError_t e = configure_sym_pair<MODE_GRAM, false>();
-    if (e == cudaSuccess) e = configure_sym_pair<MODE_GRAM, true>();
-    if (e == cudaSuccess) e = configure_sym_pair<MODE_POLY, false>();
-    if (e == cudaSuccess) e = configure_sym_pair<MODE_POLY, true>();
+cudaError_t ns_gram_pair_configure() {
+    cudaError_t e = cudaFuncSetAttribute(k_ns_gram_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_ns_gram_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramSmem);
     return e;
 }
 
 // p.tiles: 256 x 256 tiles {group slot, index, tile row I, tile column J >= I} (units of 256).
-template <int MODE, bool F16>
-cudaError_t launch_ns_sym_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
+template <bool F16>
+cudaError_t launch_ns_gram_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
     const int pairs = p.ntiles < num_sms / 2 ? p.ntiles : num_sms / 2;
-    k_ns_sym_pair<MODE, F16><<<2 * pairs, kSymThreads, SymPairCfg<MODE>::SMEM, stream>>>(p);
+    k_ns_gram_pair<F16><<<2 * pairs, kSymThreads, kGramSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_ns_sym_pair<MODE_GRAM, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gram_pair<false>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gram_pair<true>(const GemmParams&, int, cudaStream_t);
 
 }  // namespace muon

@@ -228,6 +228,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_load_32x32_async(t_acc + c * 64, raw[c]);
             tmem_wait_loads();
+            // the accumulator is in registers: hand it back to the MMA before the stores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t ow[4][4];
@@ -265,9 +269,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const int row = row0 + lane;
                 if (row < G.m) G.rowsq[(((int64_t)idx * G.m + row) * G.ntile_n + tj) * 2 + half] = sumsq;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
