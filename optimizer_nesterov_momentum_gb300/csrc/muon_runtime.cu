@@ -39,7 +39,7 @@ cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, i
 cudaError_t launch_scale_f16(float*, const uint16_t*, const float*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
 cudaError_t ns_update_pair_configure();
-cudaError_t launch_ns_update_pair(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_ns_update_pair(const GemmParams&, bool, int, cudaStream_t);
 cudaError_t ns_gram_pair_configure();
 template <bool F16>
 cudaError_t launch_ns_gram_pair(const GemmParams&, int, cudaStream_t);
@@ -80,6 +80,7 @@ struct Group {
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
     CUtensorMap map_x_w32[2];  // 32 x 32 boxes, 64-byte swizzle: stores of the SM-pair update's warps
     CUtensorMap map_a_w32;     // the same for A (SM-pair Gram)
+    CUtensorMap map_u_hi_w32, map_u_lo_w32;  // and for u's halves (first SM-pair update)
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
@@ -585,7 +586,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                            g.ldx, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_a_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.a16, g.m, g.m, g.count, g.lda, 32, 32,
-                       CU_TENSOR_MAP_SWIZZLE_64B);
+                       CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_3d(enc, &g.map_u_hi_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32,
+                       32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_3d(enc, &g.map_u_lo_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.ulo16, g.n, g.m, g.count, g.ldx, 32,
+                       32, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_u_hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32, kBM,
                        CU_TENSOR_MAP_SWIZZLE_64B) &&
@@ -686,7 +691,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 } else if (mode == MODE_POLY) {
                     gp.tiles = h->d_gemm_tiles + ch.poly_off;
                     gp.ntiles = ch.poly_n;
-                } else if (it > 0 && ch.pair_n > 0) {
+                } else if (ch.pair_n > 0) {
                     gp.tiles = h->d_gemm_tiles + ch.pair_off;
                     gp.ntiles = ch.pair_n;
                     gp.pair = 1;
@@ -732,9 +737,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
                         // first update: u hi | lo in 32-column boxes, X1 out in 32-column boxes;
                         // later updates (a on the diagonal of P): no input, X' out in 64-column boxes
-                        gp.map_ein[sl] = g.map_u_hi;
-                        gp.map_ein2[sl] = g.map_u_lo;
-                        gp.map_out[sl] = first ? g.map_x_o32[out_buf] : (gp.pair ? g.map_x_w32[out_buf] : g.map_x_k[out_buf]);
+                        gp.map_ein[sl] = gp.pair ? g.map_u_hi_w32 : g.map_u_hi;
+                        gp.map_ein2[sl] = gp.pair ? g.map_u_lo_w32 : g.map_u_lo;
+                        gp.map_out[sl] = gp.pair ? g.map_x_w32[out_buf] : (first ? g.map_x_o32[out_buf] : g.map_x_k[out_buf]);
                         G.opl16 = g.p16;
                         G.opr16 = xin16;
                     }
@@ -790,7 +795,7 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                         e = f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
                                 : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s);
                     if (mode == MODE_UPDATE)
-                        e = gp.pair ? launch_ns_update_pair(gp, h->num_sms, s)
+                        e = gp.pair ? launch_ns_update_pair(gp, !f16, h->num_sms, s)
                                     : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
                                            : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s));
                     MUON_CUDA(h, e);

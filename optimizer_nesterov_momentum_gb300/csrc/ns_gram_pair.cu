@@ -35,8 +35,8 @@ constexpr int kBlk = 32 * 32 * 2;        // one 32 x 32 16-bit block (64-byte ro
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
 
-constexpr int kGramStages = 5;
-constexpr int kOutSlots = 4;  // per warp: blocks and mirrors in flight
+constexpr int kGramStages = 6;
+constexpr int kOutSlots = 2;  // per warp: blocks and mirrors in flight
 constexpr int kGramSmem = kGramStages * kSymStage + kEpiWarps * kOutSlots * kBlk + 1024 + 512;
 static_assert(kGramSmem <= 232448, "shared memory budget");
 

@@ -1,7 +1,8 @@
-// Newton-Schulz update on SM pairs: X' = P' X for the iterations after the
-// first ("modded-nanogpt 50B-token" write-up, section "Muon from the source":
-// X <- a X + (b A + c A^2) X, with a I folded into P' = a I + b A + c A^2 by
-// the polynomial kernel), on tcgen05.mma.cta_group::2.
+// Newton-Schulz update on SM pairs ("modded-nanogpt 50B-token" write-up, section
+// "Muon from the source": X <- a X + (b A + c A^2) X), on tcgen05.mma.cta_group::2:
+//   first iteration   X1 = s (a u + P0 u_hi), u read as its bf16 hi + lo pair
+//   later iterations  X' = P' X, with a I folded into P' = a I + b A + c A^2 by
+//                     the polynomial kernel
 //
 // The two CTAs of a cluster share one 256 x 256 output tile: CTA r holds rows
 // 128 r .. 128 r + 127 of the tile's left operand (P' rows, K-major) and
@@ -38,36 +39,50 @@ namespace muon {
 namespace {
 
 constexpr int kPairThreads = 320;
-constexpr int kPairStages = 6;
 constexpr int kPairA = kBM * kBK * 2;    // 16 KB: this CTA's 128 rows of P'
 constexpr int kPairB = 128 * kBK * 2;    // 16 KB: this CTA's 128 columns of X (two 64-column blocks)
 constexpr int kPairStage = kPairA + kPairB;
-constexpr int kWarpSlot = 32 * 32 * 2;   // one warp's 32 x 32 fp16 output block (64-byte rows, 64-byte swizzle)
-constexpr int kWarpSlots = 2;            // staging slots per epilogue warp
+constexpr int kWarpSlot = 32 * 32 * 2;   // one warp's 32 x 32 16-bit block (64-byte rows, 64-byte swizzle)
+constexpr int kWarpSlots = 2;            // output staging slots per epilogue warp
 constexpr int kPairEpiWarps = 8;
 constexpr int kPairOutBytes = kPairEpiWarps * kWarpSlots * kWarpSlot;
-constexpr int kPairSmem = kPairStages * kPairStage + kPairOutBytes + 1024 + 512;
-static_assert(kPairSmem <= 232448, "shared memory budget");
-constexpr uint32_t kPairIdesc = make_idesc_16bit(256, 256, /*b_mn_major=*/true, /*fp16=*/true);
 constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
+
+// HILO: the first iteration, X1 = (s / c)(a u + c^2 (P / c^2) u_hi) with u a bf16
+// hi + lo pair: bf16 operands, and each warp reads its 32 x 32 blocks of u's hi and
+// lo halves for the a u term (two chunks ahead, by TMA).  Otherwise the folded
+// fp16 update, which reads nothing.
+template <bool HILO>
+struct UpdPairCfg {
+    static constexpr int STAGES = HILO ? 4 : 6;
+    static constexpr int IN_WARP = HILO ? 2 * 2 * kWarpSlot : 0;  // two chunks in flight, hi and lo
+    static constexpr int SMEM = STAGES * kPairStage + kPairOutBytes + kPairEpiWarps * IN_WARP + 1024 + 512;
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/true, /*fp16=*/!HILO);
+};
 
 }  // namespace
 
 using namespace pair;
 
+template <bool HILO>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     k_ns_update_pair(const __grid_constant__ GemmParams p) {
+    using C = UpdPairCfg<HILO>;
+    constexpr int kPairStages = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + kPairStages * kPairA;
     uint8_t* sO = sB + kPairStages * kPairB;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sO + kPairOutBytes);  // CTA 0's are used
+    uint8_t* sI = sO + kPairOutBytes;  // HILO: per warp two chunks of (hi | lo) blocks
+    uint64_t* full = reinterpret_cast<uint64_t*>(sI + kPairEpiWarps * C::IN_WARP);  // CTA 0's are used
     uint64_t* empty = full + kPairStages;
     uint64_t* tfull = empty + kPairStages;  // [2]
     uint64_t* tempty = tfull + 2;           // [2] CTA 0's are used: 8 warps of each CTA arrive
     uint64_t* mma_done = tempty + 2;        // abort path only
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* in_full = mma_done + 1;       // HILO: [kPairEpiWarps][2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_full + 2 * kPairEpiWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* pair_ok = abort_flag + 1;
 
@@ -87,6 +102,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_init(&tempty[a], 2 * kPairEpiWarps);
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < 2 * kPairEpiWarps; ++i) mbar_init(&in_full[i], 1);
         *tmem_slot = kNoTmem;
         *abort_flag = 0;
         *pair_ok = 0;
@@ -180,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         const uint64_t adesc = make_sdesc_sw128(a_base + stage * kPairA + kk * 32, 16, 1024);
                         const uint64_t bdesc =
                             make_sdesc_sw128(b_base + stage * kPairB + kk * (16 * 128), 64 * kBK * 2, 1024);
-                        umma_f16_pair(tacc[acc], adesc, bdesc, kPairIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16_pair(tacc[acc], adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
                         mma_any = true;
                     }
                     umma_commit_pair(&empty[stage]);
@@ -210,42 +226,110 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int half = (warp - 2) >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint8_t* wst = sO + (warp - 2) * (kWarpSlots * kWarpSlot);
+        uint8_t* win = sI + (warp - 2) * C::IN_WARP;  // HILO: slot c holds hi | lo of a chunk
+        uint64_t* ibar = &in_full[2 * (warp - 2)];
         const uint32_t tempty0 = cluster_addr(&tempty[0], 0);
         int acc = 0;
         uint32_t acc_phase = 0;
         int wchunk = 0;  // chunks this warp has staged
+        uint32_t in_phase[2] = {0u, 0u};
+        bool in_pending[2] = {false, false};
+        if (HILO && lane == 0)
+            for (int g = 0; g < p.ngroups; ++g) {
+                tma_prefetch_desc(&p.map_ein[g]);
+                tma_prefetch_desc(&p.map_ein2[g]);
+            }
         for (int t = pair; run && t < p.ntiles; t += npairs) {
             const int4 tile = p.tiles[t];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             const int row0 = ti * 2 * kBM + (int)rank * kBM + quad * 32;  // this warp's first row
+            auto load_in = [&](int c, int sl) {  // u's hi and lo blocks of chunk c (HILO, lane 0)
+                mbar_arrive_expect_tx(&ibar[sl], 2 * kWarpSlot);
+                const int col = tj * 256 + c * 64 + half * 32;
+                tma_load_3d(win + sl * 2 * kWarpSlot, &p.map_ein[g], &ibar[sl], col, row0, idx);
+                tma_load_3d(win + sl * 2 * kWarpSlot + kWarpSlot, &p.map_ein2[g], &ibar[sl], col, row0, idx);
+                in_pending[sl] = true;
+            };
+            if (HILO && lane == 0) {
+                load_in(0, 0);  // before the accumulator is ready
+                load_in(1, 1);
+            }
             mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
             tc_fence_after();
             const uint32_t t_acc = tacc[acc] + lane_off + (uint32_t)(half * 32);
             float sumsq = 0.f;
-            // all four chunks in flight at once, one wait
-            uint32_t raw[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_load_32x32_async(t_acc + c * 64, raw[c]);
-            tmem_wait_loads();
-            // the accumulator is in registers: hand it back to the MMA before the stores
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
+            float scale = 1.f, c2 = 1.f;
+            if (HILO) {
+                // the first iteration: X1 / c = (s / c)(a u + c^2 (P0 / c^2) u_hi)
+                const float cs = p.iter_scale[G.sub0 + idx];
+                scale = p.norm_scale[G.sub0 + idx] / cs;
+                c2 = cs * cs;
+            }
+            // LB chunks in flight per TMEM wait (all four for the folded update); after the
+            // last wait the accumulator is in registers and goes back to the MMA
+            constexpr int LB = HILO ? 2 : 4;
+            uint32_t raw[LB][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                if (c % LB == 0) {
+#pragma unroll
+                    for (int i = 0; i < LB; ++i) tmem_load_32x32_async(t_acc + (c + i) * 64, raw[i]);
+                    tmem_wait_loads();
+                    if (c + LB == 4) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
+                    }
+                }
+                const uint32_t* r32 = raw[c % LB];
                 uint32_t ow[4][4];
+                if (HILO) {
+                    const int sl = c & 1;
+                    mbar_wait(&ibar[sl], in_phase[sl], abort_flag, p.status);
+                    in_phase[sl] ^= 1u;
+                    in_pending[sl] = false;
+                    uint4 hw[4], lw[4];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
+                    for (int jj = 0; jj < 4; ++jj) {
+                        hw[jj] = *reinterpret_cast<const uint4*>(win + sl * 2 * kWarpSlot + sw64((uint32_t)lane, (uint32_t)jj));
+                        lw[jj] = *reinterpret_cast<const uint4*>(win + sl * 2 * kWarpSlot + kWarpSlot +
+                                                                 sw64((uint32_t)lane, (uint32_t)jj));
+                    }
+                    __syncwarp();  // every lane has read the slot
+                    if (lane == 0 && c + 2 < 4) load_in(c + 2, sl);
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const __half2 hv = __floats2half2_rn(__uint_as_float(raw[c][8 * jj + 2 * h]),
-                                                             __uint_as_float(raw[c][8 * jj + 2 * h + 1]));
-                        ow[jj][h] = *reinterpret_cast<const uint32_t*>(&hv);
-                        if (p.want_rowsq) {
-                            const float2 o = __half22float2(hv);
-                            sumsq = fmaf(o.x, o.x, sumsq);
-                            sumsq = fmaf(o.y, o.y, sumsq);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t hs[4] = {hw[jj].x, hw[jj].y, hw[jj].z, hw[jj].w};
+                        const uint32_t ls[4] = {lw[jj].x, lw[jj].y, lw[jj].z, lw[jj].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const float x0 = __uint_as_float(hs[h] << 16) + __uint_as_float(ls[h] << 16);
+                            const float x1 = __uint_as_float(hs[h] & 0xFFFF0000u) + __uint_as_float(ls[h] & 0xFFFF0000u);
+                            const float y0 = scale * fmaf(p.ca, x0, c2 * __uint_as_float(r32[8 * jj + 2 * h]));
+                            const float y1 = scale * fmaf(p.ca, x1, c2 * __uint_as_float(r32[8 * jj + 2 * h + 1]));
+                            const __half2 hv = __floats2half2_rn(y0, y1);
+                            ow[jj][h] = *reinterpret_cast<const uint32_t*>(&hv);
+                            if (p.want_rowsq) {
+                                const float2 o = __half22float2(hv);
+                                sumsq = fmaf(o.x, o.x, sumsq);
+                                sumsq = fmaf(o.y, o.y, sumsq);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __half2 hv = __floats2half2_rn(__uint_as_float(r32[8 * jj + 2 * h]),
+                                                                 __uint_as_float(r32[8 * jj + 2 * h + 1]));
+                            ow[jj][h] = *reinterpret_cast<const uint32_t*>(&hv);
+                            if (p.want_rowsq) {
+                                const float2 o = __half22float2(hv);
+                                sumsq = fmaf(o.x, o.x, sumsq);
+                                sumsq = fmaf(o.y, o.y, sumsq);
+                            }
                         }
                     }
                 }
@@ -272,6 +356,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (HILO && lane == 0) {
+            // input copies of an aborted run still in flight must land before the CTA exits
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl)
+                if (in_pending[sl]) mbar_wait_drain(&ibar[sl], in_phase[sl], 100000000ull);
+        }
         if (lane == 0) bulk_wait<0>();
     }
 
@@ -293,14 +383,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 }
 
 cudaError_t ns_update_pair_configure() {
-    return cudaFuncSetAttribute(k_ns_update_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_ns_update_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         UpdPairCfg<false>::SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_ns_update_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 UpdPairCfg<true>::SMEM);
+    return e;
 }
 
 // p.tiles: 256 x 256 tiles {group slot, index, tile row (of 256), tile column (of 256)}.
-cudaError_t launch_ns_update_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
+// hilo: the first iteration (bf16 operands, u read as hi + lo for the a u term).
+cudaError_t launch_ns_update_pair(const GemmParams& p, bool hilo, int num_sms, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
     const int pairs = p.ntiles < num_sms / 2 ? p.ntiles : num_sms / 2;
-    k_ns_update_pair<<<2 * pairs, kPairThreads, kPairSmem, stream>>>(p);
+    if (hilo)
+        k_ns_update_pair<true><<<2 * pairs, kPairThreads, UpdPairCfg<true>::SMEM, stream>>>(p);
+    else
+        k_ns_update_pair<false><<<2 * pairs, kPairThreads, UpdPairCfg<false>::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
