@@ -84,7 +84,8 @@ struct Group {
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
-    int32_t g0 = 0, ng = 0;
+    int32_t ng = 0;
+    int32_t gi[kMaxGroupsPerLaunch] = {};  // the chunk's groups (indices into muon_s::groups)
     int32_t gram_off = 0, gram_n = 0;
     int32_t poly_off = 0, poly_n = 0;
     int32_t upd_off = 0, upd_n = 0;
@@ -470,12 +471,24 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     const size_t o_subs = take(sizeof(SubDesc) * nsubs);
     const size_t o_etiles = take(sizeof(int4) * elem_tiles.size());
 
-    // GEMM tile lists, per chunk of groups
+    // GEMM tile lists, per chunk of groups.  Groups whose m and n are multiples of 256 run
+    // the Gram and the update on SM pairs; they are chunked apart from the others so that
+    // one group of another shape does not take its chunk-mates off the pair kernels.
     std::vector<int4> gemm_tiles;
-    for (int g0 = 0; g0 < (int)h->groups.size(); g0 += kMaxGroupsPerLaunch) {
+    std::vector<std::vector<int>> chunk_groups;
+    for (int fit = 1; fit >= 0; --fit) {
+        std::vector<int> gs;
+        for (int gi = 0; gi < (int)h->groups.size(); ++gi) {
+            const Group& g = h->groups[gi];
+            if ((g.m % 256 == 0 && g.n % 256 == 0) == (fit == 1)) gs.push_back(gi);
+        }
+        for (size_t i = 0; i < gs.size(); i += kMaxGroupsPerLaunch)
+            chunk_groups.emplace_back(gs.begin() + i, gs.begin() + std::min(gs.size(), i + kMaxGroupsPerLaunch));
+    }
+    for (const std::vector<int>& cg : chunk_groups) {
         Chunk ch;
-        ch.g0 = g0;
-        ch.ng = std::min<int>(kMaxGroupsPerLaunch, (int)h->groups.size() - g0);
+        ch.ng = (int32_t)cg.size();
+        for (int sl = 0; sl < ch.ng; ++sl) ch.gi[sl] = cg[(size_t)sl];
         struct T {
             int4 t;
             int64_t cost;
@@ -488,7 +501,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         };
         std::vector<T> gram, poly, upd;
         for (int sl = 0; sl < ch.ng; ++sl) {
-            const Group& g = h->groups[g0 + sl];
+            const Group& g = h->groups[ch.gi[sl]];
             const int tm = (g.m + kBM - 1) / kBM;
             const int tn = (g.n + kBNUpd - 1) / kBNUpd;
             const int ts = (g.m + kBNSym - 1) / kBNSym;  // 256-column blocks of A / P
@@ -507,17 +520,17 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         emit(gram, ch.gram_off, ch.gram_n);
         emit(poly, ch.poly_off, ch.poly_n);
         emit(upd, ch.upd_off, ch.upd_n);
-        // the folded updates (second iteration on) run on SM pairs when every group of the
-        // chunk tiles exactly into 256 x 256 pair tiles
+        // the Gram and the updates run on SM pairs when every group of the chunk tiles
+        // exactly into 256 x 256 pair tiles
         bool pair_fit = true;
         for (int sl = 0; sl < ch.ng; ++sl) {
-            const Group& g = h->groups[g0 + sl];
+            const Group& g = h->groups[ch.gi[sl]];
             pair_fit = pair_fit && g.m % 256 == 0 && g.n % 256 == 0;
         }
         if (pair_fit && h->pair_update) {
             std::vector<T> pr;
             for (int sl = 0; sl < ch.ng; ++sl) {
-                const Group& g = h->groups[g0 + sl];
+                const Group& g = h->groups[ch.gi[sl]];
                 for (int idx = 0; idx < g.count; ++idx)
                     for (int ti = 0; ti < g.m / 256; ++ti)
                         for (int tj = 0; tj < g.n / 256; ++tj) pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
@@ -525,7 +538,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             emit(pr, ch.pair_off, ch.pair_n);
             std::vector<T> sg;
             for (int sl = 0; sl < ch.ng; ++sl) {
-                const Group& g = h->groups[g0 + sl];
+                const Group& g = h->groups[ch.gi[sl]];
                 for (int idx = 0; idx < g.count; ++idx)
                     for (int ti = 0; ti < g.m / 256; ++ti)
                         for (int tj = ti; tj < g.m / 256; ++tj) sg.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
@@ -700,7 +713,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     gp.ntiles = ch.upd_n;
                 }
                 for (int sl = 0; sl < ch.ng; ++sl) {
-                    const Group& g = h->groups[ch.g0 + sl];
+                    const Group& g = h->groups[ch.gi[sl]];
                     GemmGroup& G = gp.grp[sl];
                     G.m = g.m;
                     G.n = g.n;
@@ -801,7 +814,7 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                     MUON_CUDA(h, e);
                 } else {
                     for (int sl = 0; sl < gp.ngroups; ++sl) {
-                        const int cnt = h->groups[h->chunks[c].g0 + sl].count;
+                        const int cnt = h->groups[h->chunks[c].gi[sl]].count;
                         if (mode == MODE_GRAM) MUON_CUDA(h, launch_ns_gemm_simt<MODE_GRAM>(gp, sl, cnt, s));
                         if (mode == MODE_POLY) MUON_CUDA(h, launch_ns_gemm_simt<MODE_POLY>(gp, sl, cnt, s));
                         if (mode == MODE_UPDATE) MUON_CUDA(h, launch_ns_gemm_simt<MODE_UPDATE>(gp, sl, cnt, s));

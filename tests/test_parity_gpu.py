@@ -222,6 +222,19 @@ def test_sm_pair_update_shapes_two_steps():
     errs.assert_within()
 
 
+def test_sm_pair_step_counts_and_coefficient_tables():
+    """The pair kernels with one Newton-Schulz step (the first update is also the last,
+    so it writes the NorMuon row sums) and with per-iteration coefficients, including
+    an iteration without a linear term (a = 0 on the folded diagonal).  The 192 x 320
+    matrix runs on the one-SM kernels in a chunk of its own."""
+    shapes = [Shape(256, 512), Shape(256, 256), Shape(192, 320)]
+    params, grads = _inputs(shapes, 1, seed=41)
+    for steps, table in [(1, None), (3, [(3.4445, -4.7750, 2.0315), (3.0, -3.2, 1.2), (2.0, -1.5, 0.5)]),
+                         (3, [(3.4445, -4.7750, 2.0315), (0.0, 1.2, -0.4), (2.0, -1.5, 0.5)])]:
+        errs, _, _ = run_parity(shapes, params, grads, ns_steps=steps, ns_coeffs=table)
+        errs.assert_within()
+
+
 @pytest.mark.parametrize("gscale", [1e-12, 1e4])
 def test_sm_pair_update_extreme_scales(gscale):
     shapes = [Shape(256, 512), Shape(512, 256)]
