@@ -129,7 +129,6 @@ struct muon_s {
     int4* d_gemm_tiles = nullptr;
     // pre-built GEMM parameter blocks: [iteration][chunk][mode]
     std::vector<GemmParams> gparams;
-    bool pair_update = true;        // folded updates on SM pairs where the shapes allow
     std::string last_error;
     // profiling: one event before every launch plus one at the end
     bool profiling = false;
@@ -527,7 +526,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             const Group& g = h->groups[ch.gi[sl]];
             pair_fit = pair_fit && g.m % 256 == 0 && g.n % 256 == 0;
         }
-        if (pair_fit && h->pair_update) {
+        if (pair_fit) {
             std::vector<T> pr;
             for (int sl = 0; sl < ch.ng; ++sl) {
                 const Group& g = h->groups[ch.gi[sl]];
