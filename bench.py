@@ -323,6 +323,20 @@ def run_ours(args):
     barrier()
     ms = max_over_ranks(start.elapsed_time(end) / args.steps)
     clocks = clk.summary()
+
+    # ---- spread of single steps: a second pass with an event after every replay
+    # (the events add about 1 % to a step, so ``value`` comes from the pass above)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    torch.cuda.synchronize()
+    marks[0].record()
+    for k in range(args.steps):
+        graphs[k % nbank].replay()
+        marks[k + 1].record()
+    torch.cuda.synchronize()
+    per_step = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps)]
+    step_stats = {"mean": statistics.fmean(per_step), "median": statistics.median(per_step),
+                  "std": statistics.pstdev(per_step), "min": min(per_step), "max": max(per_step),
+                  "pass": "second pass, one event per replay"}
     opt.sync_status()
 
     # ---- eager step timing (same work, launched through the API each step)
@@ -488,6 +502,7 @@ def run_ours(args):
             "kernels": kern,
             "roofline": roofline,
             "cpu_baseline": cpu,
+            "step_ms_stats": step_stats,
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": True, "serial_ms": e2e_serial_ms,
                     "note": "gradients copied in from pinned host memory and parameters read back every step; "
