@@ -179,6 +179,27 @@ def cores():
         return os.cpu_count()
 
 
+# ---------------------------------------------------------------------------- ranks
+def rank_barrier(world):
+    """Barrier over the ranks of a multi-GPU run (replicas: each rank steps its own copy)."""
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def rank_max(x, world, device):
+    """Max of a per-rank time over all ranks (the slowest replica sets the step time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -300,15 +321,10 @@ def run_ours(args):
     opt.sync_status()
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return rank_max(x, world, dev)
 
     # ---- timed region: graph replays
     barrier()
