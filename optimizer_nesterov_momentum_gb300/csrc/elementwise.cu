@@ -122,7 +122,7 @@ __device__ __forceinline__ float momentum_elem(float g, float& b, float mu, int 
 }
 
 template <int CAP, bool GRAD_F32>
-__global__ void __launch_bounds__(256) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
+__global__ void __launch_bounds__(256, 6) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float su[kTile][kTile + 1];
     __shared__ float red[8];
     const int4 tile = p.tiles[blockIdx.x];
