@@ -22,11 +22,13 @@
 //              0's lane 0 issues the MMAs and commits stage releases and
 //              "accumulator full" to both CTAs' mbarriers at once (multicast
 //              commit)
-//   warps 2-9  epilogue (both CTAs): drain this CTA's 128 accumulator rows,
-//              round to fp16, stage and TMA-store them warp by warp (each warp
-//              its own 32 x 32 blocks, no barrier across warps); NorMuon row
-//              sums on the last iteration; then release the accumulator on CTA
-//              0's mbarrier
+//   warps 2-9  epilogue (both CTAs): drain this CTA's 128 accumulator rows
+//              into registers and release the accumulator on CTA 0's mbarrier,
+//              then round to fp16 (the first iteration first adds a u, from
+//              32 x 32 blocks of u's hi and lo halves each warp TMA-loads two
+//              chunks ahead), stage and TMA-store warp by warp (each warp its
+//              own 32 x 32 blocks, no barrier across warps); NorMuon row sums
+//              on the last iteration
 // Every mbarrier wait is bounded (2 s) and raises the status word on expiry.
 // The allocation is checked before use: both CTAs must see the same TMEM
 // address, else the kernel reports the mismatch in the status word and does
