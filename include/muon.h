@@ -35,8 +35,20 @@
  * Errors.  Functions return MUON_OK (0) or a negative muon_status.  The text
  * of the last error of a handle is available from muon_last_error(); errors
  * raised before a handle exists go to muon_last_error(NULL).  Errors detected
- * on the device (a bounded wait that gave up) are recorded in a device status
- * word and reported by muon_sync_status().
+ * on the device are recorded in a device status word and reported by
+ * muon_sync_status():
+ *   - a bounded wait that gave up (MUON_ERR_TIMEOUT), or an SM pair that did not
+ *     get one shared TMEM allocation (MUON_ERR_CUDA), is fatal: from the step in
+ *     which it happened until muon_sync_status clears the word, every step leaves
+ *     the parameters, the momentum and the second moment as they were (the
+ *     failed step itself has already folded its gradient into the momentum);
+ *   - a matrix whose update direction is not finite (a NaN or infinite gradient
+ *     element, or an overflow) is reported as MUON_ERR_NONFINITE: only that
+ *     matrix's step is skipped (its parameters and second moment stay as they
+ *     were), and a momentum element whose new value would not be finite keeps
+ *     its previous value.  Later steps run normally.
+ * None of the pages specifies failure handling; the pages' only stability
+ * advice concerns spikes in the gradient norm.
  */
 #ifndef MUON_GB300_H
 #define MUON_GB300_H
@@ -58,7 +70,8 @@ typedef enum {
     MUON_ERR_TIMEOUT = -5,     /* a kernel's bounded wait gave up (device status word) */
     MUON_ERR_DESTROYED = -6,   /* the handle was destroyed */
     MUON_ERR_NOMEM = -7,       /* device allocation failed in muon_create */
-    MUON_ERR_UNSUPPORTED = -8  /* the current device is not an sm_103 GPU */
+    MUON_ERR_UNSUPPORTED = -8, /* the current device is not an sm_103 GPU */
+    MUON_ERR_NONFINITE = -9    /* a matrix's update direction was not finite; its step was skipped */
 } muon_status;
 
 typedef enum { MUON_GRAD_BF16 = 0, MUON_GRAD_F32 = 1 } muon_grad_dtype;
@@ -70,6 +83,16 @@ typedef enum { MUON_GRAD_BF16 = 0, MUON_GRAD_F32 = 1 } muon_grad_dtype;
 /* Newton-Schulz gemm engine (muon_config.gemm_engine) */
 #define MUON_GEMM_TCGEN05 0      /* tcgen05 / TMEM / TMA grouped kernels (the product path) */
 #define MUON_GEMM_SIMT 1         /* plain CUDA-core kernels; a slow debugging cross-check */
+
+/* NorMuon lanes (muon_config.normuon_lanes): which rows or columns of a matrix
+ * each get one second-moment entry.  The FixMuonLR record write-up (background
+ * and change 2) has NorMuon average the squared update along the longer
+ * dimension and scale each remaining lane by an rsqrt; it also says the early
+ * attention reshape makes NorMuon act per column (per output dimension).
+ * SHORT_SIDE is the first statement taken literally and is the default. */
+#define MUON_LANES_SHORT_SIDE 0  /* one lane per row of the short side (mean over the long side) */
+#define MUON_LANES_ROWS 1        /* one lane per row of the matrix as stored (mean over its columns) */
+#define MUON_LANES_COLS 2        /* one lane per column of the matrix as stored (mean over its rows) */
 
 #define MUON_MAX_MATRICES 1024   /* parameter matrices per handle */
 #define MUON_MAX_NS_STEPS 16
@@ -103,11 +126,12 @@ typedef struct {
     const float* wd_mul;   /* host array [n_mats] or NULL (all 1.0); copied at create */
     const float* ns_coeffs;/* host array [ns_steps * 3] of (a, b, c) per iteration, or NULL
                               for (3.4445, -4.7750, 2.0315) every iteration; copied */
+    int32_t normuon_lanes; /* MUON_LANES_*: the second moment's lanes (NorMuon only) */
 } muon_config;
 
 /* Fills *cfg with: lr 0.02, momentum 0.95, beta2 0.95, weight_decay 0, ns_steps 5,
  * nesterov 1, lerp_form 1, normuon 1, norm_preserve 1, grad_dtype BF16,
- * gemm_engine TCGEN05, NULL arrays. */
+ * gemm_engine TCGEN05, NULL arrays, normuon_lanes MUON_LANES_SHORT_SIDE. */
 void muon_config_default(muon_config* cfg);
 
 /* Builds the execution plan for `n_mats` matrices on CUDA device `device`:
@@ -175,8 +199,9 @@ int muon_set_schedule(muon_handle h, const muon_schedule* sched, int64_t start_s
  * the next muon_step will use (0 when no schedule was ever installed). */
 int muon_get_step(muon_handle h, int64_t* step, void* stream);
 
-/* Synchronises `stream`, reads and clears the device status word.
- * Returns MUON_OK, MUON_ERR_TIMEOUT, or MUON_ERR_CUDA. */
+/* Synchronises `stream`, reads and clears the device status word (see
+ * "Errors" above).  Returns MUON_OK, MUON_ERR_TIMEOUT, MUON_ERR_CUDA or
+ * MUON_ERR_NONFINITE (in that order of precedence when several were raised). */
 int muon_sync_status(muon_handle h, void* stream);
 
 /* Releases all device memory of the handle.  Synchronises the device. */
@@ -192,8 +217,9 @@ int muon_num_matrices(muon_handle h, int32_t* out);
 
 /* Describes split matrix `index`: out[0] = parent parameter index, out[1] =
  * split index, out[2] = rows, out[3] = cols (as stored), out[4] = 1 if it is
- * worked on transposed, out[5] = m = min(rows, cols), out[6] = n = max(rows, cols). */
-int muon_matrix_info(muon_handle h, int32_t index, int64_t out[7]);
+ * worked on transposed, out[5] = m = min(rows, cols), out[6] = n = max(rows, cols),
+ * out[7] = number of NorMuon lanes (the length of its second moment). */
+int muon_matrix_info(muon_handle h, int32_t index, int64_t out[8]);
 
 /* Bytes of device memory owned by the handle. */
 int muon_workspace_bytes(muon_handle h, int64_t* out);
@@ -222,7 +248,8 @@ int muon_set_profiling(muon_handle h, int32_t enable);
 int muon_get_stage_times(muon_handle h, float* out);
 
 #define MUON_STATE_MOMENTUM 0      /* per parameter i: fp32 rows x cols, row-major, dense */
-#define MUON_STATE_SECOND_MOMENT 1 /* per split matrix: fp32 [m] */
+#define MUON_STATE_SECOND_MOMENT 1 /* per split matrix: fp32, one per NorMuon lane (muon_matrix_info out[7]);
+                                      lanes in the order of the rows or columns they stand for */
 #define MUON_STATE_ORTHO 2         /* per split matrix: last Newton-Schulz output O, wide
                                       orientation m x n, fp32, DEVICE destination only
                                       (rebuilt on the device from its scaled fp16 copy) */
@@ -236,6 +263,17 @@ int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void*
 
 /* Overwrites one state array (MOMENTUM or SECOND_MOMENT) from `src`. */
 int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src, void* stream);
+
+/* ---- test support ----------------------------------------------------------
+ *
+ * For failure-handling tests only; no part of the optimizer step uses it.
+ * Makes the next muon_step's first polynomial launch (a one-SM tcgen05 kernel)
+ * wait on an mbarrier that nothing arrives on, so that its bounded wait gives
+ * up after about 2 s: the kernel then sets the status word, lets the copies it
+ * issued land, frees its TMEM and returns, and the step leaves the parameters
+ * and second moment unchanged (see "Errors").  One-shot.  MUON_ERR_ARG when
+ * gemm_engine is not MUON_GEMM_TCGEN05. */
+int muon_debug_inject_stall(muon_handle h);
 
 /* ---- allocation-free entry point ------------------------------------------
  *
@@ -259,7 +297,12 @@ int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src,
  * MUON_ERR_SHAPE.  All calls share the array; calls whose work overlaps on
  * the GPU race, so order them on one stream.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress) with that device
- * current; make it before any stream capture.  Returns MUON_OK, MUON_ERR_ARG,
+ * current, and looks it up again when the device's current context has
+ * changed (after cudaDeviceReset the array may sit elsewhere); make the first
+ * call, and the first call after a reset, before any stream capture.
+ * momentum, x0 and grad must not overlap (identical pointers: MUON_ERR_ARG).
+ * A CUDA error pending from earlier work of the caller is returned as
+ * MUON_ERR_CUDA before anything is enqueued.  Returns MUON_OK, MUON_ERR_ARG,
  * MUON_ERR_SHAPE or MUON_ERR_CUDA. */
 #define MUON_NOALLOC_MAX_TILES 65536
 int muon_nesterov_normalize_noalloc(const void* grad, int32_t grad_dtype, float* momentum, float* x0,

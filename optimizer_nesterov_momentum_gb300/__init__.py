@@ -15,8 +15,13 @@ from typing import Optional, Sequence
 
 from . import _abi
 from ._abi import (  # noqa: F401  (re-exported names of the C ABI)
+    MUON_ERR_NONFINITE,
+    MUON_ERR_TIMEOUT,
     MUON_GEMM_SIMT,
     MUON_GEMM_TCGEN05,
+    MUON_LANES_COLS,
+    MUON_LANES_ROWS,
+    MUON_LANES_SHORT_SIDE,
     MUON_SPLIT_COLUMNS,
     MUON_SPLIT_CONTIGUOUS,
     MUON_STATE_DIRECTION,
@@ -59,14 +64,16 @@ class Muon:
 
     Hyper-parameters follow the C ABI's ``muon_config``.  ``grad_dtype`` is
     "bf16" or "f32"; ``gemm_engine`` is "tcgen05" (the product path) or
-    "simt" (a slow cross-check engine for debugging).
+    "simt" (a slow cross-check engine for debugging); ``normuon_lanes`` is
+    "short_side" (default: one second-moment entry per row of the short side),
+    "rows" or "cols" (per row / per column of each matrix as stored).
     """
 
     def __init__(self, specs: Sequence, *, lr: float = 0.02, momentum: float = 0.95, beta2: float = 0.95,
                  weight_decay: float = 0.0, ns_steps: int = 5, nesterov: bool = True, lerp_form: bool = True,
                  normuon: bool = True, norm_preserve: bool = True, grad_dtype: str = "bf16",
                  gemm_engine: str = "tcgen05", ns_coeffs: Optional[Sequence[Sequence[float]]] = None,
-                 device: Optional[int] = None):
+                 normuon_lanes: str = "short_side", device: Optional[int] = None):
         import torch
 
         self.specs = [s if isinstance(s, MatrixSpec) else MatrixSpec(*s) for s in specs]
@@ -81,6 +88,8 @@ class Muon:
         cfg.norm_preserve = int(norm_preserve)
         cfg.grad_dtype = _abi.MUON_GRAD_BF16 if grad_dtype == "bf16" else _abi.MUON_GRAD_F32
         cfg.gemm_engine = {"tcgen05": MUON_GEMM_TCGEN05, "simt": MUON_GEMM_SIMT}[gemm_engine]
+        cfg.normuon_lanes = {"short_side": MUON_LANES_SHORT_SIDE, "rows": MUON_LANES_ROWS,
+                             "cols": MUON_LANES_COLS}[normuon_lanes]
         n = len(self.specs)
         self._lr_mul = (ctypes.c_float * n)(*[s.lr_mul for s in self.specs])
         self._wd_mul = (ctypes.c_float * n)(*[s.wd_mul for s in self.specs])
@@ -150,15 +159,23 @@ class Muon:
         return _abi.muon_get_step(self.handle, _stream_ptr(stream))
 
     def sync_status(self, stream=None) -> None:
+        """Synchronises ``stream`` and raises MuonError if a kernel reported a failure
+        (MUON_ERR_TIMEOUT, MUON_ERR_NONFINITE, ...); clears the device status word."""
         _abi.muon_sync_status(self.handle, _stream_ptr(stream))
+
+    def debug_inject_stall(self) -> None:
+        """Test support: the next step's first polynomial launch waits on an mbarrier
+        that nothing arrives on until its bounded wait gives up (see muon.h)."""
+        _abi.muon_debug_inject_stall(self.handle)
 
     # -------------------------------------------------------------- introspection
     def num_matrices(self) -> int:
         return _abi.muon_num_matrices(self.handle)
 
     def matrix_info(self, index: int) -> dict:
-        parent, q, rows, cols, transposed, m, n = _abi.muon_matrix_info(self.handle, index)
-        return dict(parent=parent, split_index=q, rows=rows, cols=cols, transposed=bool(transposed), m=m, n=n)
+        parent, q, rows, cols, transposed, m, n, lanes = _abi.muon_matrix_info(self.handle, index)
+        return dict(parent=parent, split_index=q, rows=rows, cols=cols, transposed=bool(transposed), m=m, n=n,
+                    lanes=lanes)
 
     def workspace_bytes(self) -> int:
         return _abi.muon_workspace_bytes(self.handle)
@@ -185,7 +202,7 @@ class Muon:
         else:
             info = self.matrix_info(index)
             if which == MUON_STATE_SECOND_MOMENT:
-                out = torch.empty((info["m"],), dtype=torch.float32, device=dev)
+                out = torch.empty((info["lanes"],), dtype=torch.float32, device=dev)
             elif which == MUON_STATE_ORTHO:
                 out = torch.empty((info["m"], info["n"]), dtype=torch.float32, device=dev)
             elif which == MUON_STATE_DIRECTION:

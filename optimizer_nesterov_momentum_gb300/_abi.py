@@ -23,6 +23,7 @@ MUON_ERR_TIMEOUT = -5
 MUON_ERR_DESTROYED = -6
 MUON_ERR_NOMEM = -7
 MUON_ERR_UNSUPPORTED = -8
+MUON_ERR_NONFINITE = -9
 
 MUON_GRAD_BF16 = 0
 MUON_GRAD_F32 = 1
@@ -30,6 +31,9 @@ MUON_SPLIT_CONTIGUOUS = 0
 MUON_SPLIT_COLUMNS = 1
 MUON_GEMM_TCGEN05 = 0
 MUON_GEMM_SIMT = 1
+MUON_LANES_SHORT_SIDE = 0
+MUON_LANES_ROWS = 1
+MUON_LANES_COLS = 2
 MUON_MAX_MATRICES = 1024
 MUON_MAX_NS_STEPS = 16
 
@@ -62,6 +66,7 @@ EXPORTED = (
     "muon_get_stage_times",
     "muon_get_state",
     "muon_set_state",
+    "muon_debug_inject_stall",
     "muon_nesterov_normalize_noalloc",
     # include/muon_adam.h
     "muon_adam_config_default",
@@ -124,6 +129,7 @@ class muon_config(ctypes.Structure):
         ("lr_mul", POINTER(c_float)),
         ("wd_mul", POINTER(c_float)),
         ("ns_coeffs", POINTER(c_float)),
+        ("normuon_lanes", c_int32),
     ]
 
 
@@ -184,6 +190,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_get_stage_times.argtypes = [c_void_p, POINTER(c_float)]
     lib.muon_get_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
     lib.muon_set_state.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.muon_debug_inject_stall.argtypes = [c_void_p]
     lib.muon_nesterov_normalize_noalloc.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_int64,
                                                     c_float, c_int32, c_int32, c_void_p]
     for name in EXPORTED:
@@ -261,9 +268,13 @@ def muon_num_matrices(h) -> int:
 
 
 def muon_matrix_info(h, index: int):
-    out = (c_int64 * 7)()
+    out = (c_int64 * 8)()
     _check(load_library().muon_matrix_info(h, index, out), h)
     return tuple(out)
+
+
+def muon_debug_inject_stall(h) -> None:
+    _check(load_library().muon_debug_inject_stall(h), h)
 
 
 def muon_workspace_bytes(h) -> int:

@@ -4,16 +4,28 @@
 //                 of the FixMuonLR record, or the mul/add form of the
 //                 "modded-nanogpt 50B-token" write-up), Nesterov direction u,
 //                 u written in the wide orientation (through shared memory for
-//                 tall matrices) as fp32 and bf16, per-tile partial sums of u^2
-//   k_norm_scale  S4: s = 1 / (||u||_F + 1e-7) per matrix (fixed-order reduction)
-//   k_lane_stats  S8 + S9 factors: r_i from the update epilogue's row sums,
-//                 v <- lerp(v, r, 1 - beta2), q_i = 1/sqrt(max(v_i, 1e-10)),
-//                 norm-preserving gamma, lane factor lr * lr_mul * gamma * q_i
-//                 (plain Muon: lr * lr_mul * max(1, R/C)^0.5)
+//                 tall matrices) as a bf16 hi + lo pair, per-tile partial sums
+//                 of u^2
+//   k_norm_scale  S4: s = 1 / (||u||_F + 1e-7) per matrix (fixed-order reduction);
+//                 flags a matrix whose ||u|| is not finite
+//   k_col_sumsq   S8 for column lanes: per (64-row slab, column) sums of O^2
+//   k_lane_stats  S8 + S9 factors: r from the update epilogue's row sums (or the
+//                 column sums), v <- lerp(v, r, 1 - beta2),
+//                 q = 1/sqrt(max(v, 1e-10)), norm-preserving gamma, lane factor
+//                 lr * lr_mul * gamma * q (plain Muon: lr * lr_mul * max(1, R/C)^0.5)
 //   k_apply       S10: p <- p * (1 - lr*lr_mul*wd*wd_mul) - lane_factor * O,
 //                 O read in the wide orientation and written back in the
 //                 caller's orientation
 // Reductions are two-stage with a fixed order, so results are reproducible.
+//
+// Failure handling.  A fatal bit in the status word (a bounded wait that gave
+// up, or an SM pair without a shared TMEM allocation) makes k_momentum,
+// k_lane_stats and k_apply return without writing, so neither the caller's
+// parameters nor the optimizer state take in what a failed Newton-Schulz
+// launch left behind; this holds for every step until muon_sync_status clears
+// the word.  A momentum element whose new value is not finite keeps its old
+// value and makes u non-finite; k_norm_scale then flags the matrix, and its
+// second moment and parameters are left as they were for that step.
 #include <algorithm>
 
 #include "muon_internal.h"
@@ -110,21 +122,29 @@ __device__ __forceinline__ void load8_f16(const uint16_t* src, float (&v)[8]) {
     }
 }
 
-// momentum and Nesterov direction of one element
+// momentum and Nesterov direction of one element.  A new buffer value that is
+// not finite (a non-finite gradient, or an overflow) is not stored: the element
+// keeps its old value and the direction is NaN, which flags the matrix.
 __device__ __forceinline__ float momentum_elem(float g, float& b, float mu, int lerp_form, int nesterov) {
+    float bn, u;
     if (lerp_form) {
-        b = fmaf(1.f - mu, g - b, b);          // buf.lerp_(g, 1 - mu)
-        return nesterov ? fmaf(mu, b - g, g)   // lerp(g, buf, mu)
-                        : b;
+        bn = fmaf(1.f - mu, g - b, b);          // buf.lerp_(g, 1 - mu)
+        u = nesterov ? fmaf(mu, bn - g, g)      // lerp(g, buf, mu)
+                     : bn;
+    } else {
+        bn = fmaf(mu, b, g);                    // buf.mul_(mu).add_(g)
+        u = nesterov ? fmaf(mu, bn, g) : bn;    // g + mu * buf
     }
-    b = fmaf(mu, b, g);                        // buf.mul_(mu).add_(g)
-    return nesterov ? fmaf(mu, b, g) : b;      // g + mu * buf
+    const bool ok = isfinite(bn);
+    b = ok ? bn : b;
+    return ok ? u : __int_as_float(0x7fc00000);
 }
 
 template <int CAP, bool GRAD_F32>
 __global__ void __launch_bounds__(256, 6) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float su[kTile][kTile + 1];
     __shared__ float red[8];
+    if (*p.status & kStatusFatal) return;  // an earlier step failed: leave the momentum as it is
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
     const int r0 = tile.y, c0 = tile.z;
@@ -209,27 +229,70 @@ __global__ void __launch_bounds__(256) k_norm_scale(const __grid_constant__ Norm
         p.norm_scale[blockIdx.x] = sc;
         // ||X0|| = ||u|| s: the Newton-Schulz kernels keep their iterate divided by it
         p.iter_scale[blockIdx.x] = norm > 0.f ? norm * sc : 1.f;
+        // a non-finite direction: this matrix's second moment and parameters are left alone
+        const int bad = isfinite(total) ? 0 : 1;
+        *d.skip = bad;
+        if (bad) atomicOr(p.status, STATUS_NONFINITE);
+    }
+}
+
+// Per (sub, 64-row slab): sums over the slab's rows of O^2 for every column of
+// the wide orientation (subs whose NorMuon lanes are its columns).
+__global__ void __launch_bounds__(256) k_col_sumsq(const __grid_constant__ ColSumParams p) {
+    const int2 w = p.work[blockIdx.x];
+    const SubDesc& d = p.subs[w.x];
+    const int r0 = w.y * kTile, r1 = min(r0 + kTile, d.m);
+    float* out = d.colsq + (int64_t)w.y * d.n;
+    for (int j0 = threadIdx.x * 8; j0 < d.n; j0 += 256 * 8) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        if (j0 + 8 <= d.n) {
+            for (int r = r0; r < r1; ++r) {
+                float o[8];
+                load8_f16(d.o16 + (int64_t)r * d.ldx + j0, o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(o[e], o[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) out[j0 + e] = acc[e];
+        } else {
+            for (int r = r0; r < r1; ++r)
+                for (int e = 0; e < 8 && j0 + e < d.n; ++e) {
+                    const float o = h2f(d.o16[(int64_t)r * d.ldx + j0 + e]);
+                    acc[e] = fmaf(o, o, acc[e]);
+                }
+            for (int e = 0; e < 8 && j0 + e < d.n; ++e) out[j0 + e] = acc[e];
+        }
     }
 }
 
 __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ LaneParams p) {
     __shared__ float red[8];
     const SubDesc& d = p.subs[blockIdx.x];
+    // a failed step (fatal status) or a non-finite direction: the second moment stays as it is
+    if ((*p.status & kStatusFatal) || *d.skip) return;
     const float eff = p.hp[HP_LR] * d.lr_mul;
     const float cs = p.iter_scale[blockIdx.x];  // O = cs * (the stored output)
+    const int nl = d.lane_cols ? d.n : d.m;     // lanes
     if (!p.normuon) {
         const float f = eff * d.shape_scale * cs;
-        for (int i = threadIdx.x; i < d.m; i += 256) d.lane[i] = f;
+        for (int i = threadIdx.x; i < nl; i += 256) d.lane[i] = f;
         return;
     }
     const float beta2 = p.hp[HP_BETA2];
-    const float inv_n = 1.f / (float)d.n;
+    const float inv_len = 1.f / (float)(d.lane_cols ? d.m : d.n);  // the mean runs across the lanes' length
+    const int nslab = (d.m + kTile - 1) / kTile;
     float before = 0.f, after = 0.f;
-    for (int i = threadIdx.x; i < d.m; i += 256) {
+    for (int i = threadIdx.x; i < nl; i += 256) {
         float rs = 0.f;
-        for (int t = 0; t < 2 * d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n * 2 + t];
+        if (d.lane_cols) {
+            for (int t = 0; t < nslab; ++t) rs += d.colsq[(int64_t)t * d.n + i];
+        } else {
+            for (int t = 0; t < 2 * d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n * 2 + t];
+        }
         rs *= cs * cs;
-        const float r = rs * inv_n;
+        const float r = rs * inv_len;
         const float v0 = d.v[i];
         const float v1 = fmaf(1.f - beta2, r - v0, v0);  // v.lerp_(r, 1 - beta2)
         d.v[i] = v1;
@@ -242,14 +305,16 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
     const float sa = block_sum_256(after, red);
     const float gamma = p.norm_preserve ? sqrtf(sb) / fmaxf(sqrtf(sa), kVFloor) : 1.f;
     const float f = eff * gamma * cs;
-    for (int i = threadIdx.x; i < d.m; i += 256) d.lane[i] *= f;
+    for (int i = threadIdx.x; i < nl; i += 256) d.lane[i] *= f;
 }
 
 template <int CAP>
 __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float so[kTile][kTile + 1];
+    if (*p.status & kStatusFatal) return;  // a Newton-Schulz launch failed: keep the caller's parameters
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
+    if (*d.skip) return;                   // this matrix's direction was not finite
     const int r0 = tile.y, c0 = tile.z;
     const int tr = threadIdx.x >> 3, tc = threadIdx.x & 7;
     const float decay = 1.f - p.hp[HP_LR] * d.lr_mul * p.hp[HP_WD] * d.wd_mul;
@@ -314,8 +379,10 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
         if (!act[pass]) continue;
         const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
         float* pp = P + (int64_t)r * d.ld + c;
+        // lanes along the caller's columns (rows of a transposed matrix's wide
+        // orientation, or the wide columns of an untransposed one), else along its rows
         float f[8];
-        if (d.transposed) {
+        if (d.transposed != d.lane_cols) {
             for (int e = 0; e < 8; ++e) f[e] = (c + e < d.cols) ? d.lane[c + e] : 0.f;
         } else {
             const float fr = d.lane[r];
@@ -416,6 +483,12 @@ cudaError_t launch_apply(const ElemParams<CAP>& p, cudaStream_t s) {
 cudaError_t launch_norm_scale(const NormParams& p, cudaStream_t s) {
     if (p.nsubs <= 0) return cudaSuccess;
     k_norm_scale<<<p.nsubs, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_col_sumsq(const ColSumParams& p, cudaStream_t s) {
+    if (p.nwork <= 0) return cudaSuccess;
+    k_col_sumsq<<<p.nwork, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

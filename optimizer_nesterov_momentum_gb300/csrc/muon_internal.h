@@ -13,7 +13,10 @@
 //                   iteration on p16 holds P' = a I + P, unscaled
 //       rowsq       per (row, 256-column tile, column half) sums of O^2 from the
 //                   last iteration (S8)
-//       v           second moment, fp32 [m] (S8)
+//       colsq       column lanes only: per (64-row slab, column) sums of O^2
+//       v           second moment, fp32, one per lane (S8): [m] when the lanes are
+//                   the rows of the wide orientation (the default), [n] when they
+//                   are its columns
 //       lane        per-lane update factor lr*lr_mul*gamma/sqrt(v) (S9)
 //   Matrices with the same (m, n) form a group and sit back to back in each
 //   arena, so one 3-D TMA descriptor (n, m, count) covers a whole group.
@@ -43,8 +46,16 @@ struct DevSchedule {
     float lr_base, lr_floor, momentum_start, momentum_end;
 };
 
-// bits of the device status word
-enum { STATUS_TIMEOUT = 1, STATUS_PAIR = 2 };  // PAIR: an SM pair did not get one shared TMEM allocation
+// bits of the device status word.  TIMEOUT and PAIR are fatal: once either is
+// raised the write-back, the second-moment update and the momentum update of
+// every later step are skipped until muon_sync_status clears the word.
+// NONFINITE records that some matrix had a non-finite update direction; only
+// that matrix's step was skipped (per-matrix flag, rewritten every step).
+enum { STATUS_TIMEOUT = 1, STATUS_PAIR = 2, STATUS_NONFINITE = 4 };  // PAIR: an SM pair did not get one shared TMEM allocation
+constexpr int kStatusFatal = STATUS_TIMEOUT | STATUS_PAIR;
+
+// NorMuon lanes (muon_config.normuon_lanes)
+enum { LANES_SHORT_SIDE = 0, LANES_ROWS = 1, LANES_COLS = 2 };
 
 enum GemmMode { MODE_GRAM = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
 
@@ -63,13 +74,17 @@ struct SubDesc {
     int32_t ntile_n;     // 256-column tiles per row (2 rowsq entries each)
     int32_t k1_tile0, k1_ntiles;  // range of this sub's elementwise tiles
     float lr_mul, wd_mul, shape_scale;
+    int32_t lane_cols;   // NorMuon lanes are the columns of the wide orientation (n lanes), else its rows (m)
+    int32_t colsq_tile0; // lane_cols: first (sub, slab) entry of this sub in the column-sum work list
     // wide-orientation arenas of this sub
     uint16_t* u16;        // hi half of u (bf16(u))
     uint16_t* ulo16;      // lo half of u (bf16(u - hi))
     const uint16_t* o16;  // final Newton-Schulz output (fp16), m x n, row stride ldx
     float* rowsq;         // m x ntile_n x 2
-    float* v;             // m
-    float* lane;          // m
+    float* colsq;         // lane_cols: ceil(m / 64) x n
+    float* v;             // one per lane
+    float* lane;          // one per lane
+    int* skip;            // per-sub flag: this step's direction was not finite (written by k_norm_scale)
 };
 
 // Per-launch pointer table of the caller's buffers (kernel parameter; CAP
@@ -89,6 +104,7 @@ struct ElemParams {
     const float* hp;         // HP_* slots
     float* norm_part;        // one partial sum of u^2 per tile
     int32_t nesterov, lerp_form;
+    const int* status;       // device status word: a fatal bit skips the kernel's writes
 };
 
 struct GemmGroup {
@@ -124,6 +140,8 @@ struct GemmParams {
     int32_t first, last, want_rowsq;
     int32_t f16;             // operands and results fp16 (iterations after the first); else bf16
     int32_t pair;            // update on SM pairs: tiles are 256 x 256 (tile row and column in units of 256)
+    int32_t debug_stall;     // test only (muon_debug_inject_stall): the MMA issuer first waits on an
+                             // mbarrier that nothing arrives on, until its bounded wait gives up
     int* status;
 };
 
@@ -133,6 +151,7 @@ struct LaneParams {
     const float* hp;
     int32_t normuon, norm_preserve;
     const float* iter_scale;  // c per sub: the stored iterate is X / c
+    const int* status;
 };
 
 struct NormParams {
@@ -141,6 +160,15 @@ struct NormParams {
     const float* norm_part;
     float* norm_scale;
     float* iter_scale;        // c = ||u|| s = ||X0|| per sub (1 when u = 0)
+    int* status;
+};
+
+// Column sums of O^2 for subs whose NorMuon lanes are the wide columns: one
+// block per (sub, 64-row slab).
+struct ColSumParams {
+    const SubDesc* subs;
+    const int2* work;         // {sub, slab}
+    int32_t nwork;
 };
 
 }  // namespace muon

@@ -32,6 +32,7 @@ template <int CAP>
 cudaError_t launch_apply(const ElemParams<CAP>&, cudaStream_t);
 cudaError_t launch_norm_scale(const NormParams&, cudaStream_t);
 cudaError_t launch_lane_stats(const LaneParams&, cudaStream_t);
+cudaError_t launch_col_sumsq(const ColSumParams&, cudaStream_t);
 cudaError_t launch_set_hparams(float*, float, float, float, float, cudaStream_t);
 cudaError_t launch_schedule_set(DevSchedule*, const DevSchedule&, cudaStream_t);
 cudaError_t launch_schedule_advance(float*, DevSchedule*, cudaStream_t);
@@ -73,6 +74,8 @@ struct Group {
     float* rowsq = nullptr;
     float* v = nullptr;
     float* lane = nullptr;
+    float* colsq = nullptr;   // column lanes: per matrix ceil(m / 64) x n
+    int32_t lane_stride = 0;  // floats per matrix in v / lane: m, or n when some matrix has column lanes
     // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), 32 x 128 boxes of
     // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
@@ -113,6 +116,8 @@ struct muon_s {
     std::vector<Chunk> chunks;
     std::vector<int64_t> mom_off;       // per parent, offset into momentum arena (floats)
     int32_t n_elem_tiles = 0;
+    int32_t n_colwork = 0;              // (sub, slab) blocks of k_col_sumsq (column lanes only)
+    bool stall_next = false;            // muon_debug_inject_stall: the next step's first polynomial stalls
     // device memory
     void* arena = nullptr;
     size_t arena_bytes = 0;
@@ -125,6 +130,8 @@ struct muon_s {
     float* norm_part = nullptr;
     float* momentum = nullptr;
     SubDesc* d_subs = nullptr;
+    int* skip = nullptr;               // per sub: this step's direction was not finite
+    int2* d_colwork = nullptr;
     int4* d_elem_tiles = nullptr;
     int4* d_gemm_tiles = nullptr;
     // pre-built GEMM parameter blocks: [iteration][chunk][mode]
@@ -222,6 +229,7 @@ cudaError_t run_elem(muon_s* h, float* const* params, const void* const* grads, 
     ep.norm_part = h->norm_part;
     ep.nesterov = h->cfg.nesterov;
     ep.lerp_form = h->cfg.lerp_form;
+    ep.status = h->status;
     if (apply) return launch_apply<CAP>(ep, s);
     return launch_momentum<CAP>(ep, h->cfg.grad_dtype == MUON_GRAD_F32, s);
 }
@@ -237,10 +245,12 @@ int launches_per_step(const muon_s* h) {
     // k_momentum, k_norm_scale, k_lane_stats, k_apply + the Newton-Schulz products
     // (+ k_schedule_advance while a schedule is installed)
     const int sched = h->schedule_on ? 1 : 0;
-    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) return sched + 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps;
+    const int colsum = h->n_colwork > 0 ? 1 : 0;  // k_col_sumsq for column lanes
+    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05)
+        return sched + colsum + 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps;
     const int per_iter = 3 * (int)h->groups.size();
     const int rowsq = h->cfg.normuon ? (int)h->groups.size() : 0;  // extra pass after the last update
-    return sched + 4 + per_iter * h->cfg.ns_steps + rowsq;
+    return sched + colsum + 4 + per_iter * h->cfg.ns_steps + rowsq;
 }
 
 cudaError_t mark(muon_s* h, int stage, cudaStream_t s) {
@@ -269,6 +279,7 @@ void muon_config_default(muon_config* cfg) {
     cfg->norm_preserve = 1;
     cfg->grad_dtype = MUON_GRAD_BF16;
     cfg->gemm_engine = MUON_GEMM_TCGEN05;
+    cfg->normuon_lanes = MUON_LANES_SHORT_SIDE;
 }
 
 const char* muon_error_string(int code) {
@@ -282,6 +293,7 @@ const char* muon_error_string(int code) {
         case MUON_ERR_DESTROYED: return "handle destroyed";
         case MUON_ERR_NOMEM: return "out of device memory";
         case MUON_ERR_UNSUPPORTED: return "device is not sm_103";
+        case MUON_ERR_NONFINITE: return "a matrix's update direction was not finite; its step was skipped";
         default: return "unknown error";
     }
 }
@@ -311,6 +323,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         return fail(nullptr, MUON_ERR_ARG, "bad grad_dtype");
     if (cfg.gemm_engine != MUON_GEMM_TCGEN05 && cfg.gemm_engine != MUON_GEMM_SIMT)
         return fail(nullptr, MUON_ERR_ARG, "bad gemm_engine");
+    if (cfg.normuon_lanes != MUON_LANES_SHORT_SIDE && cfg.normuon_lanes != MUON_LANES_ROWS &&
+        cfg.normuon_lanes != MUON_LANES_COLS)
+        return fail(nullptr, MUON_ERR_ARG, "bad normuon_lanes");
 
     // ---- shapes -> split matrices (host-only validation first)
     struct Pending {
@@ -427,6 +442,17 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     const size_t o_sched = take(sizeof(DevSchedule));
     const size_t o_norm_scale = take(sizeof(float) * nsubs);
     const size_t o_iter_scale = take(sizeof(float) * nsubs);
+    const size_t o_skip = take(sizeof(int) * nsubs);
+    // NorMuon lanes of each sub: the rows of its wide orientation, or its columns
+    // (the caller's rows of a tall matrix under MUON_LANES_ROWS, the caller's
+    // columns of a wide or square one under MUON_LANES_COLS)
+    std::vector<int> sub_lane_cols(nsubs, 0);
+    for (int sidx = 0; sidx < nsubs; ++sidx) {
+        const Pending& pd = pend[order[sidx]];
+        const bool tr = pd.rows > pd.cols;
+        sub_lane_cols[sidx] = cfg.normuon && ((cfg.normuon_lanes == MUON_LANES_ROWS && tr) ||
+                                              (cfg.normuon_lanes == MUON_LANES_COLS && !tr));
+    }
     // elementwise tiles
     std::vector<int4> elem_tiles;
     std::vector<int32_t> k1_tile0(nsubs), k1_ntiles(nsubs);
@@ -444,9 +470,20 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->n_elem_tiles = (int32_t)elem_tiles.size();
     const size_t o_norm_part = take(sizeof(float) * elem_tiles.size());
     const size_t o_mom = take(sizeof(float) * (size_t)mom_total);
-    std::vector<size_t> go_ulo, go_u16, go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane;
-    for (auto& g : h->groups) g.count = 0;
-    for (int sidx = 0; sidx < nsubs; ++sidx) h->groups[sub_group[order[sidx]]].count++;
+    std::vector<size_t> go_ulo, go_u16, go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane, go_colsq;
+    for (auto& g : h->groups) {
+        g.count = 0;
+        g.lane_stride = g.m;
+    }
+    std::vector<int> group_cols(h->groups.size(), 0);  // some matrix of the group has column lanes
+    for (int sidx = 0; sidx < nsubs; ++sidx) {
+        Group& g = h->groups[sub_group[order[sidx]]];
+        g.count++;
+        if (sub_lane_cols[sidx]) {
+            g.lane_stride = g.n;
+            group_cols[sub_group[order[sidx]]] = 1;
+        }
+    }
     {
         int s0 = 0;
         for (auto& g : h->groups) {
@@ -464,9 +501,24 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         go_a16.push_back(take(ae * 2));
         go_p16.push_back(take(ae * 2));
         go_rowsq.push_back(take((size_t)g.count * g.m * g.ntile_n * 2 * 4));
-        go_v.push_back(take((size_t)g.count * g.m * 4));
-        go_lane.push_back(take((size_t)g.count * g.m * 4));
+        go_v.push_back(take((size_t)g.count * g.lane_stride * 4));
+        go_lane.push_back(take((size_t)g.count * g.lane_stride * 4));
     }
+    for (size_t gi = 0; gi < h->groups.size(); ++gi) {
+        const Group& g = h->groups[gi];
+        go_colsq.push_back(group_cols[gi] ? take((size_t)g.count * ((g.m + kTile - 1) / kTile) * g.n * 4) : 0);
+    }
+    // k_col_sumsq work list: one block per (sub, 64-row slab) of the subs with column lanes
+    std::vector<int2> colwork;
+    std::vector<int32_t> colwork0(nsubs, 0);
+    for (int sidx = 0; sidx < nsubs; ++sidx) {
+        colwork0[sidx] = (int32_t)colwork.size();
+        if (!sub_lane_cols[sidx]) continue;
+        const Group& g = h->groups[sub_group[order[sidx]]];
+        for (int slab = 0; slab < (g.m + kTile - 1) / kTile; ++slab) colwork.push_back(make_int2(sidx, slab));
+    }
+    h->n_colwork = (int32_t)colwork.size();
+    const size_t o_colwork = take(sizeof(int2) * std::max<size_t>(colwork.size(), 1));
     const size_t o_subs = take(sizeof(SubDesc) * nsubs);
     const size_t o_etiles = take(sizeof(int4) * elem_tiles.size());
 
@@ -565,6 +617,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->sched = reinterpret_cast<DevSchedule*>(base + o_sched);
     h->norm_scale = reinterpret_cast<float*>(base + o_norm_scale);
     h->iter_scale = reinterpret_cast<float*>(base + o_iter_scale);
+    h->skip = reinterpret_cast<int*>(base + o_skip);
+    h->d_colwork = reinterpret_cast<int2*>(base + o_colwork);
     h->norm_part = reinterpret_cast<float*>(base + o_norm_part);
     h->momentum = reinterpret_cast<float*>(base + o_mom);
     h->d_subs = reinterpret_cast<SubDesc*>(base + o_subs);
@@ -582,6 +636,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         g.rowsq = reinterpret_cast<float*>(base + go_rowsq[gi]);
         g.v = reinterpret_cast<float*>(base + go_v[gi]);
         g.lane = reinterpret_cast<float*>(base + go_lane[gi]);
+        g.colsq = group_cols[gi] ? reinterpret_cast<float*>(base + go_colsq[gi]) : nullptr;
         bool ok = encode_bf16_3d(enc, &g.map_u_k, g.u16, g.n, g.m, g.count, g.ldx, kBM) &&
                   encode_bf16_3d(enc, &g.map_u_mn, g.u16, g.n, g.m, g.count, g.ldx, 64) &&
                   encode_bf16_3d(enc, &g.map_a_k, g.a16, g.m, g.m, g.count, g.lda, kBM) &&
@@ -652,8 +707,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         d.ulo16 = g.ulo16 + xo;
         d.o16 = g.x16[last_buf] + xo;
         d.rowsq = g.rowsq + (int64_t)gi * g.m * g.ntile_n * 2;
-        d.v = g.v + (int64_t)gi * g.m;
-        d.lane = g.lane + (int64_t)gi * g.m;
+        d.v = g.v + (int64_t)gi * g.lane_stride;
+        d.lane = g.lane + (int64_t)gi * g.lane_stride;
+        d.lane_cols = sub_lane_cols[sidx];
+        d.colsq_tile0 = colwork0[sidx];
+        d.colsq = g.colsq ? g.colsq + (int64_t)gi * ((g.m + kTile - 1) / kTile) * g.n : nullptr;
+        d.skip = h->skip + sidx;
         h->subs.push_back(d);
         h->sub_parent_q.push_back(pd.q);
     }
@@ -662,6 +721,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     bool ok = cudaMemcpy(h->d_subs, h->subs.data(), sizeof(SubDesc) * nsubs, cudaMemcpyHostToDevice) == cudaSuccess &&
               cudaMemcpy(h->d_elem_tiles, elem_tiles.data(), sizeof(int4) * elem_tiles.size(),
                          cudaMemcpyHostToDevice) == cudaSuccess &&
+              (colwork.empty() || cudaMemcpy(h->d_colwork, colwork.data(), sizeof(int2) * colwork.size(),
+                                             cudaMemcpyHostToDevice) == cudaSuccess) &&
               (gemm_tiles.empty() || cudaMemcpy(h->d_gemm_tiles, gemm_tiles.data(), sizeof(int4) * gemm_tiles.size(),
                                                 cudaMemcpyHostToDevice) == cudaSuccess);
     float hpv[HP_COUNT] = {cfg.lr, cfg.momentum, cfg.beta2, cfg.weight_decay};
@@ -785,14 +846,25 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
     MUON_CUDA(h, mark(h, MUON_STAGE_MOMENTUM, s));
     if (h->schedule_on) MUON_CUDA(h, launch_schedule_advance(h->hp, h->sched, s));
     MUON_CUDA(h, run_elem_any(h, params, grads, false, s));
-    NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale, h->iter_scale};
+    NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale, h->iter_scale, h->status};
     MUON_CUDA(h, mark(h, MUON_STAGE_NORM, s));
     MUON_CUDA(h, launch_norm_scale(np, s));
     const int nch = (int)h->chunks.size();
     for (int it = 0; it < h->cfg.ns_steps; ++it) {
         for (int mode = 0; mode < 3; ++mode) {
             for (int c = 0; c < nch; ++c) {
-                const GemmParams& gp = h->gparams[((size_t)it * nch + c) * 3 + mode];
+                const GemmParams* gpp = &h->gparams[((size_t)it * nch + c) * 3 + mode];
+                GemmParams stalled;
+                if (h->stall_next && it == 0 && c == 0 && mode == MODE_POLY &&
+                    h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
+                    // test only (muon_debug_inject_stall): this launch's MMA issuers wait on an
+                    // mbarrier that nothing arrives on until their bounded wait gives up
+                    stalled = *gpp;
+                    stalled.debug_stall = 1;
+                    gpp = &stalled;
+                    h->stall_next = false;
+                }
+                const GemmParams& gp = *gpp;
                 MUON_CUDA(h, mark(h, MUON_STAGE_GRAM + mode, s));
                 if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
                     // the first iteration works on bf16 u; later ones on the fp16 iterate
@@ -822,8 +894,13 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
             }
         }
     }
-    LaneParams lp{h->d_subs, (int32_t)h->subs.size(), h->hp, h->cfg.normuon, h->cfg.norm_preserve, h->iter_scale};
+    LaneParams lp{h->d_subs, (int32_t)h->subs.size(), h->hp, h->cfg.normuon, h->cfg.norm_preserve, h->iter_scale,
+                  h->status};
     MUON_CUDA(h, mark(h, MUON_STAGE_LANE, s));
+    if (h->n_colwork > 0) {
+        ColSumParams cp{h->d_subs, h->d_colwork, h->n_colwork};
+        MUON_CUDA(h, launch_col_sumsq(cp, s));
+    }
     MUON_CUDA(h, launch_lane_stats(lp, s));
     MUON_CUDA(h, mark(h, MUON_STAGE_APPLY, s));
     MUON_CUDA(h, run_elem_any(h, params, grads, true, s));
@@ -839,7 +916,8 @@ int muon_reset(muon_handle h, void* stream) {
     int64_t mom_floats = 0;
     for (size_t i = 0; i < h->shapes.size(); ++i) mom_floats += round_up(h->shapes[i].rows * h->shapes[i].cols, 64);
     MUON_CUDA(h, cudaMemsetAsync(h->momentum, 0, sizeof(float) * (size_t)mom_floats, s));
-    for (const Group& g : h->groups) MUON_CUDA(h, cudaMemsetAsync(g.v, 0, sizeof(float) * (size_t)g.count * g.m, s));
+    for (const Group& g : h->groups)
+        MUON_CUDA(h, cudaMemsetAsync(g.v, 0, sizeof(float) * (size_t)g.count * g.lane_stride, s));
     MUON_CUDA(h, cudaMemsetAsync(&h->sched->step, 0, sizeof(int64_t), s));
     return MUON_OK;
 }
@@ -907,8 +985,14 @@ int muon_sync_status(muon_handle h, void* stream) {
     MUON_CUDA(h, cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost));
     if (st != 0) {
         MUON_CUDA(h, cudaMemset(h->status, 0, sizeof(int)));
-        if (st & STATUS_TIMEOUT) return fail(h, MUON_ERR_TIMEOUT, "a kernel's bounded wait gave up");
+        if (st & STATUS_TIMEOUT)
+            return fail(h, MUON_ERR_TIMEOUT,
+                        "a kernel's bounded wait gave up; the parameters and the second moment were left unchanged "
+                        "from that step on");
         if (st & STATUS_PAIR) return fail(h, MUON_ERR_CUDA, "an SM pair did not get one shared TMEM allocation");
+        if (st & STATUS_NONFINITE)
+            return fail(h, MUON_ERR_NONFINITE,
+                        "a matrix's update direction was not finite; that matrix's step was skipped");
     }
     return MUON_OK;
 }
@@ -937,7 +1021,7 @@ int muon_num_matrices(muon_handle h, int32_t* out) {
     return MUON_OK;
 }
 
-int muon_matrix_info(muon_handle h, int32_t index, int64_t out[7]) {
+int muon_matrix_info(muon_handle h, int32_t index, int64_t out[8]) {
     int rc = check_handle(h);
     if (rc) return rc;
     if (!out || index < 0 || index >= (int32_t)h->subs.size()) return fail(h, MUON_ERR_ARG, "bad index");
@@ -949,6 +1033,7 @@ int muon_matrix_info(muon_handle h, int32_t index, int64_t out[7]) {
     out[4] = d.transposed;
     out[5] = d.m;
     out[6] = d.n;
+    out[7] = d.lane_cols ? d.n : d.m;
     return MUON_OK;
 }
 
@@ -1016,7 +1101,7 @@ int muon_get_state(muon_handle h, int32_t which, int32_t index, void* dst, void*
     if (index < 0 || index >= (int32_t)h->subs.size()) return fail(h, MUON_ERR_ARG, "bad matrix index");
     const SubDesc& d = h->subs[index];
     if (which == MUON_STATE_SECOND_MOMENT) {
-        MUON_CUDA(h, cudaMemcpyAsync(dst, d.v, sizeof(float) * d.m, cudaMemcpyDefault, s));
+        MUON_CUDA(h, cudaMemcpyAsync(dst, d.v, sizeof(float) * (d.lane_cols ? d.n : d.m), cudaMemcpyDefault, s));
     } else if (which == MUON_STATE_ORTHO || which == MUON_STATE_DIRECTION) {
         // both are rebuilt on the device: O = c * (stored fp16 output), u = hi + lo
         cudaPointerAttributes attr;
@@ -1051,10 +1136,19 @@ int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src,
     if (which == MUON_STATE_SECOND_MOMENT) {
         if (index < 0 || index >= (int32_t)h->subs.size()) return fail(h, MUON_ERR_ARG, "bad matrix index");
         const SubDesc& d = h->subs[index];
-        MUON_CUDA(h, cudaMemcpyAsync(d.v, src, sizeof(float) * d.m, cudaMemcpyDefault, s));
+        MUON_CUDA(h, cudaMemcpyAsync(d.v, src, sizeof(float) * (d.lane_cols ? d.n : d.m), cudaMemcpyDefault, s));
         return MUON_OK;
     }
     return fail(h, MUON_ERR_ARG, "state %d cannot be written", which);
+}
+
+int muon_debug_inject_stall(muon_handle h) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    if (h->cfg.gemm_engine != MUON_GEMM_TCGEN05)
+        return fail(h, MUON_ERR_ARG, "the stall is injected into a tensor-core kernel (gemm_engine TCGEN05 only)");
+    h->stall_next = true;
+    return MUON_OK;
 }
 
 }  // extern "C"

@@ -21,9 +21,15 @@
 //     GPU (different streams, or different host threads) race on the array and
 //     produce wrong results.  Order such calls on one stream.
 //   * in host code `g_noalloc_scratch` names a host-side stand-in, not a device
-//     address: the device address is fetched with cudaGetSymbolAddress once per
-//     device, on the first call made while that device is current.  Make that
-//     first call outside any stream capture.
+//     address: the device address is fetched with cudaGetSymbolAddress on the
+//     first call made while a device is current, and again whenever that
+//     device's current context has changed since (for instance after
+//     cudaDeviceReset, which unloads the module that holds the array).  Make
+//     the first call on a device, and the first call after a reset, outside
+//     any stream capture.
+//   * momentum, x0 and (for fp32 gradients) grad must not overlap; identical
+//     pointers are rejected with MUON_ERR_ARG.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -44,6 +50,24 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoallocMaxTiles + 64];
 
 std::mutex g_setup_mu;
 float* g_scratch_dev[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};  // context the address was looked up in
+
+typedef CUresult (*PFN_ctxGetCurrent)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link against libcuda)
+CUcontext current_context() {
+    static PFN_ctxGetCurrent fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_ctxGetCurrent>(p);
+    }
+    CUcontext c = nullptr;
+    return fn(&c) == CUDA_SUCCESS ? c : nullptr;
+}
 
 // momentum buffer and Nesterov direction of one element (lerp or mul/add form)
 __device__ __forceinline__ float na_momentum(float g, float& b, float mu, int lerp_form, int nesterov) {
@@ -122,28 +146,39 @@ extern "C" int muon_nesterov_normalize_noalloc(const void* grad, int32_t grad_dt
                                                int32_t nesterov, void* stream) {
     if (grad == nullptr || momentum == nullptr || x0 == nullptr) return MUON_ERR_ARG;
     if (grad_dtype != MUON_GRAD_BF16 && grad_dtype != MUON_GRAD_F32) return MUON_ERR_ARG;
+    // the three buffers are read and written element by element in one pass: they must not alias
+    if (static_cast<const void*>(momentum) == static_cast<const void*>(x0)) return MUON_ERR_ARG;
+    if (grad_dtype == MUON_GRAD_F32 && (grad == static_cast<const void*>(momentum) || grad == static_cast<const void*>(x0)))
+        return MUON_ERR_ARG;
     if (rows < 1 || cols < 1) return MUON_ERR_SHAPE;
+    // reject sizes beyond the scratch before any product that could overflow
+    const int64_t max_side = (int64_t)kNoallocTile * kNoallocMaxTiles;
+    if (rows > max_side || cols > max_side) return MUON_ERR_SHAPE;
     const int64_t tiles_r = (rows + kNoallocTile - 1) / kNoallocTile;
     const int64_t tiles_c = (cols + kNoallocTile - 1) / kNoallocTile;
-    if (tiles_r * tiles_c > kNoallocMaxTiles) {
+    if (tiles_r > kNoallocMaxTiles / tiles_c) {
         fprintf(stderr,
-                "muon_nesterov_normalize_noalloc: %lld x %lld needs %lld tiles of 64 x 64; the static scratch "
-                "holds %d\n",
-                (long long)rows, (long long)cols, (long long)(tiles_r * tiles_c), kNoallocMaxTiles);
+                "muon_nesterov_normalize_noalloc: %lld x %lld needs more than %d tiles of 64 x 64 (the static "
+                "scratch's limit)\n",
+                (long long)rows, (long long)cols, kNoallocMaxTiles);
         return MUON_ERR_SHAPE;
     }
+    // an error left over from the caller's earlier work is not this call's: report it as such
+    if (cudaGetLastError() != cudaSuccess) return MUON_ERR_CUDA;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MUON_ERR_CUDA;
     float* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_setup_mu);
-        if (g_scratch_dev[dev] == nullptr) {
+        const CUcontext ctx = current_context();
+        if (g_scratch_dev[dev] == nullptr || ctx != g_scratch_ctx[dev]) {
             void* ptr = nullptr;
             if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
                 cudaGetLastError();
                 return MUON_ERR_CUDA;
             }
             g_scratch_dev[dev] = static_cast<float*>(ptr);
+            g_scratch_ctx[dev] = ctx;
         }
         scratch = g_scratch_dev[dev];
     }
@@ -162,7 +197,9 @@ extern "C" int muon_nesterov_normalize_noalloc(const void* grad, int32_t grad_dt
     p.nesterov = nesterov;
     const int ntiles = (int)(tiles_r * tiles_c);
     k_na_momentum<<<ntiles, 256, 0, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return MUON_ERR_CUDA;
     k_na_norm<<<1, 256, 0, s>>>(scratch, ntiles);
+    if (cudaGetLastError() != cudaSuccess) return MUON_ERR_CUDA;
     const int64_t n = rows * cols;
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;

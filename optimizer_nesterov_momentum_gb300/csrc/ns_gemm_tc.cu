@@ -45,7 +45,12 @@
 // c = ||X0|| <= 1) that keeps them near unit size whatever the gradient's norm;
 // the folded P' = a I + P of the later iterations is stored unscaled.
 // Every wait is bounded (2 s); on a timeout the kernel sets the status word,
-// lets copies and MMAs in flight finish, frees TMEM and returns.
+// lets copies and MMAs in flight finish, frees TMEM and returns.  After an
+// abort no role re-arms an mbarrier whose copy might still be in flight: the
+// producer's stages come back only through MMA commits (which follow landed
+// copies), and the epilogue loader stops issuing as soon as it sees the abort
+// flag (the epilogue may then release input slots without waiting for them);
+// both drain the copies they issued before the CTA exits.
 #include "muon_internal.h"
 #include "ptx_sm103.cuh"
 
@@ -221,8 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     }
                 }
             }
-            if (!ok) {
-                // let every copy already issued land before the CTA can exit
+            if (!ok || *abort_flag) {
+                // after an abort the MMA may not have consumed the last copies: let every
+                // copy already issued land before the CTA can exit
 #pragma unroll
                 for (int s = 0; s < STAGES; ++s)
                     if (issued[s]) mbar_wait_drain(&full[s], issued_phase[s], 100000000ull);
@@ -238,6 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
+            // test only: wait on an mbarrier nothing arrives on (mma_done is armed only on the
+            // abort path, which needs any == true) until the bounded wait gives up
+            if (p.debug_stall) ok = mbar_wait(mma_done, 0u, abort_flag, p.status);
             const uint32_t a_base = smem_u32(sA);
             const uint32_t b_base = smem_u32(sB);
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
@@ -313,6 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                         ok = false;
                         break;
                     }
+                    // after an abort the epilogue hands slots back without waiting for their
+                    // copies: re-arming one could overlap a copy still landing, so stop here
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
                     mbar_arrive_expect_tx(&ein_full[slot], C::IN_BYTES);
                     uint8_t* dst = sI + slot * C::IN_BYTES;
                     tma_load_3d(dst, &p.map_ein[g], &ein_full[slot], tj * BN + c * C::CHUNK, ti * kBM, idx);
@@ -327,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
                     }
                 }
             }
-            if (!ok) {
+            if (!ok || *abort_flag) {
+                // every slot's last copy must have landed before the CTA can exit
 #pragma unroll
                 for (int s = 0; s < C::ISLOTS; ++s)
                     if (issued[s]) mbar_wait_drain(&ein_full[s], issued_phase[s], 100000000ull);

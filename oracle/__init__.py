@@ -16,6 +16,7 @@ from .muon_oracle import (
     NS_COEFFS,
     NORM_EPS,
     V_FLOOR,
+    FP32_MAX,
     OracleConfig,
     MuonOracle,
     bf16_round,
@@ -28,7 +29,6 @@ from .muon_oracle import (
     frobenius_normalise,
     newton_schulz,
     newton_schulz_closed_form,
-    newton_schulz_mixed,
     zeropower_via_newtonschulz5,
     normuon_scale,
     shape_scale,
@@ -50,6 +50,7 @@ __all__ = [
     "NS_COEFFS",
     "NORM_EPS",
     "V_FLOOR",
+    "FP32_MAX",
     "OracleConfig",
     "MuonOracle",
     "bf16_round",
@@ -62,7 +63,6 @@ __all__ = [
     "frobenius_normalise",
     "newton_schulz",
     "newton_schulz_closed_form",
-    "newton_schulz_mixed",
     "zeropower_via_newtonschulz5",
     "normuon_scale",
     "shape_scale",

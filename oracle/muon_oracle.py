@@ -43,12 +43,22 @@ design notes):
   mean of the squared update is taken along the longer side; square matrices
   use rows.  ``v <- lerp(v, r, 1 - beta2)`` from v = 0, no bias correction,
   lane scale ``rsqrt(max(v, 1e-10))``, then the scaled update is rescaled to
-  the Frobenius norm it had before the lane scaling.
+  the Frobenius norm it had before the lane scaling.  The same write-up says
+  the early attention reshape makes NorMuon act per column (per output
+  dimension); ``OracleConfig.normuon_lanes`` = "rows" / "cols" selects one
+  lane per row / per column of each matrix as stored instead.
 * Weight decay is decoupled: ``p <- p * (1 - lr*lr_mul*wd*wd_mul)`` before
   the update.
 * NorMuon mode scales the update by ``lr * lr_mul``; plain-Muon mode by
   ``lr * lr_mul * max(1, rows/cols)^0.5`` (rows/cols of the matrix as the
   optimizer sees it, i.e. after the bank split).
+
+Failure handling (not from the pages, which give none; the library's
+definition, mirrored here): a momentum element whose new value is not finite
+in the fp32 buffer keeps its previous value and makes the direction u
+non-finite there; a matrix whose u has a non-finite element, or whose
+||u||_F^2 exceeds the fp32 range, is skipped for the step (parameters and
+second moment unchanged).
 """
 
 from __future__ import annotations
@@ -63,6 +73,8 @@ NS_COEFFS: Tuple[float, float, float] = (3.4445, -4.7750, 2.0315)
 NORM_EPS: float = 1e-7
 # Floor under the second moment before the rsqrt (reading; the pages give none).
 V_FLOOR: float = 1e-10
+# Largest finite fp32 value: the momentum buffer and the squared norm of u are fp32.
+FP32_MAX: float = 3.4028234663852886e38
 
 
 # ---------------------------------------------------------------------------
@@ -203,40 +215,6 @@ def newton_schulz(x: np.ndarray, steps: int = 5, coeffs=None, form: str = "page"
     return x
 
 
-def newton_schulz_mixed(x: np.ndarray, steps: int = 5, coeffs=None) -> np.ndarray:
-    """Diagnostic: the iteration with the rounding points of the mixed-precision
-    tensor-core implementation (not a definition of the method).
-
-    The first iteration reads bf16-rounded operands of an fp32 iterate (the
-    normalised input, held as a bf16 hi + lo pair), stores A and P = b A + c A A
-    in bf16 and rounds its result to fp16.  Every later iteration holds X, A
-    and P in fp16 and folds its a X term into the polynomial: P' = a I + b A +
-    c A A is rounded once and X' = P' X.  The stored arrays are divided by a
-    fixed per-matrix scale -- X by c = ||X0|| <= 1, A and the first P by c^2,
-    P' not at all (X' / c = P' X / c) -- so that an input far below unit norm
-    keeps its precision in fp16; in exact arithmetic the scale cancels.
-    Products accumulate exactly.  Used only to size the rounding error of tiny
-    matrices, where a relative Frobenius error is dominated by a handful of
-    singular values and can exceed the 2e-2 bound that holds for the workloads.
-    """
-    f32 = lambda v: np.asarray(v, dtype=np.float32).astype(np.float64)
-    x = f32(x)
-    cs = float(np.linalg.norm(x)) or 1.0
-    c2 = cs * cs
-    xs = None  # the stored fp16 iterate X / c of the later iterations
-    for k, (a, b, c) in enumerate(_coeff_list(coeffs, steps)):
-        if k == 0:
-            xb = bf16_round(x)
-            A = bf16_round((xb @ xb.T) / c2)
-            P = bf16_round(b * A + (c * c2) * (A @ A))
-            xs = fp16_round((a * x + c2 * (P @ xb)) / cs)
-        else:
-            A = fp16_round(xs @ xs.T)
-            P = fp16_round(c2 * (b * A + (c * c2) * (A @ A)) + a * np.eye(A.shape[0]))
-            xs = fp16_round(P @ xs)
-    return cs * xs
-
-
 def zeropower_via_newtonschulz5(g: np.ndarray, steps: int = 5, eps: float = NORM_EPS, coeffs=None,
                                 form: str = "page", bf16: bool = False) -> np.ndarray:
     """The [50B] orthogonalisation of one matrix, result in the input's orientation."""
@@ -278,17 +256,19 @@ def newton_schulz_closed_form(x: np.ndarray, steps: int = 5, coeffs=None) -> np.
 # ---------------------------------------------------------------------------
 
 def normuon_scale(o_wide: np.ndarray, v: np.ndarray, beta2: float, norm_preserve: bool = True,
-                  v_floor: float = V_FLOOR) -> Tuple[np.ndarray, np.ndarray]:
+                  v_floor: float = V_FLOOR, lanes: str = "rows") -> Tuple[np.ndarray, np.ndarray]:
     """One NorMuon update of the per-lane second moment and the scaled update.
 
-    ``o_wide`` is m x n with m <= n; lanes are its rows ([FixMuonLR]: mean
-    along the longer dimension, then a per-lane rsqrt).  Returns
-    ``(o_scaled, v_new)``.
+    ``o_wide`` is m x n with m <= n.  With ``lanes="rows"`` the lanes are its
+    rows ([FixMuonLR]: mean along the longer dimension, then a per-lane
+    rsqrt); with ``lanes="cols"`` they are its columns (mean along the
+    shorter dimension).  Returns ``(o_scaled, v_new)``.
     """
-    r = np.mean(o_wide * o_wide, axis=1)                  # mean square along the long side
+    axis = {"rows": 1, "cols": 0}[lanes]
+    r = np.mean(o_wide * o_wide, axis=axis)               # mean square across each lane
     v_new = v + (1.0 - beta2) * (r - v)                   # v.lerp_(r, 1 - beta2)
     q = 1.0 / np.sqrt(np.maximum(v_new, v_floor))         # per-lane rsqrt
-    o_scaled = o_wide * q[:, None]
+    o_scaled = o_wide * (q[:, None] if axis == 1 else q[None, :])
     if norm_preserve:
         before = np.sqrt(np.sum(o_wide * o_wide))
         after = np.sqrt(np.sum(o_scaled * o_scaled))
@@ -333,6 +313,7 @@ class OracleConfig:
     ns_form: str = "page"
     ns_impl: str = "iterate"  # or "closed_form" (exact spectral value; large matrices)
     bf16: bool = False
+    normuon_lanes: str = "short_side"  # or "rows" / "cols" of each matrix as stored
 
 
 @dataclass
@@ -340,10 +321,11 @@ class SubRecord:
     """Intermediates of one optimizer matrix (after the bank split)."""
 
     u: np.ndarray          # Nesterov direction, original orientation
-    o: np.ndarray          # Newton-Schulz output, wide orientation
-    o_scaled: np.ndarray   # after NorMuon (== o in plain mode), wide orientation
+    o: Optional[np.ndarray]         # Newton-Schulz output, wide orientation (None when skipped)
+    o_scaled: Optional[np.ndarray]  # after NorMuon (== o in plain mode), wide orientation
     v: Optional[np.ndarray]
     transposed: bool
+    skipped: bool = False  # the direction was not finite: parameters and v left unchanged
 
 
 class MuonOracle:
@@ -361,8 +343,17 @@ class MuonOracle:
         self.v = []
         for (r, c, split, *_rest) in self.shapes:
             sr, sc = r, c // split
-            self.v.append([np.zeros(min(sr, sc)) for _ in range(split)])
+            nl = max(sr, sc) if self.lane_cols(sr, sc) else min(sr, sc)
+            self.v.append([np.zeros(nl) for _ in range(split)])
         self.records: List[List[SubRecord]] = []
+
+    def lane_cols(self, rows: int, cols: int) -> bool:
+        """Whether the NorMuon lanes of a rows x cols matrix are the columns of its wide orientation."""
+        transposed = rows > cols
+        lanes = self.cfg.normuon_lanes
+        if lanes not in ("short_side", "rows", "cols"):
+            raise ValueError(lanes)
+        return (lanes == "rows" and transposed) or (lanes == "cols" and not transposed)
 
     def reset(self):
         """Zero the momentum and second-moment buffers ([FixMuonLR] change 2, reset())."""
@@ -379,13 +370,27 @@ class MuonOracle:
         for i, (r, c, split, lr_mul, wd_mul) in enumerate(self.shapes):
             g = np.asarray(grads[i], dtype=np.float64)
             p = np.asarray(params[i], dtype=np.float64)
-            self.momentum[i] = momentum_update(self.momentum[i], g, cfg.momentum, cfg.lerp_form)
-            u = nesterov_direction(g, self.momentum[i], cfg.momentum, cfg.lerp_form, cfg.nesterov)
+            new_buf = momentum_update(self.momentum[i], g, cfg.momentum, cfg.lerp_form)
+            # an element whose new value is not finite in the fp32 buffer keeps its old value
+            with np.errstate(invalid="ignore", over="ignore"):
+                kept = np.isfinite(new_buf) & (np.abs(new_buf) <= FP32_MAX)
+            self.momentum[i] = np.where(kept, new_buf, self.momentum[i])
+            with np.errstate(invalid="ignore", over="ignore"):
+                u = nesterov_direction(g, self.momentum[i], cfg.momentum, cfg.lerp_form, cfg.nesterov)
+            u = np.where(kept, u, np.nan)
             mode = self.split_modes[i]
             subs_u = split_matrix(u, split, mode)
             subs_p = split_matrix(p, split, mode)
             new_subs, recs = [], []
             for q, (su, sp) in enumerate(zip(subs_u, subs_p)):
+                with np.errstate(invalid="ignore", over="ignore"):
+                    bad = not np.all(np.isfinite(su)) or not np.sum(su * su) <= FP32_MAX
+                if bad:
+                    # skipped for this step: parameters and second moment unchanged
+                    new_subs.append(sp.copy())
+                    vrec = self.v[i][q].copy() if cfg.normuon else None
+                    recs.append(SubRecord(su, None, None, vrec, su.shape[0] > su.shape[1], skipped=True))
+                    continue
                 rnd = bf16_round if cfg.bf16 else _id
                 x = frobenius_normalise(rnd(su), cfg.eps, rnd)
                 x, transposed = orient_wide(x)
@@ -394,7 +399,9 @@ class MuonOracle:
                 else:
                     o = newton_schulz(x, cfg.ns_steps, cfg.ns_coeffs, cfg.ns_form, cfg.bf16)
                 if cfg.normuon:
-                    o_scaled, self.v[i][q] = normuon_scale(o, self.v[i][q], cfg.beta2, cfg.norm_preserve)
+                    lanes = "cols" if self.lane_cols(*su.shape) else "rows"
+                    o_scaled, self.v[i][q] = normuon_scale(o, self.v[i][q], cfg.beta2, cfg.norm_preserve,
+                                                           lanes=lanes)
                     scale = 1.0
                     vrec = self.v[i][q].copy()
                 else:

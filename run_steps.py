@@ -3,8 +3,8 @@
 A minimal driver for profilers (one muon_step per iteration, no CUDA graphs,
 no timing, no oracle), e.g.
 
-    python -m optimizer_nesterov_momentum_gb300.run_steps --workload gpt2-124m --steps 2
-    python -m optimizer_nesterov_momentum_gb300.run_steps --adam gpt2-124m-adam --steps 3
+    python run_steps.py --workload gpt2-124m --steps 2
+    python run_steps.py --adam gpt2-124m-adam --steps 3
 """
 
 from __future__ import annotations
@@ -13,7 +13,7 @@ import argparse
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 

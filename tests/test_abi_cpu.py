@@ -45,10 +45,43 @@ def test_struct_layouts_match_header():
 
     assert ctypes.sizeof(_abi.muon_shape) == 32
     assert _abi.muon_config.lr_mul.offset == 48
-    assert ctypes.sizeof(_abi.muon_config) == 72
+    assert _abi.muon_config.normuon_lanes.offset == 72
+    assert ctypes.sizeof(_abi.muon_config) == 80
     assert ctypes.sizeof(_abi.muon_schedule) == 40
     assert [getattr(_abi.muon_schedule, f).offset for f, _ in _abi.muon_schedule._fields_] == [0, 4, 8, 16, 24, 28, 32]
     assert ctypes.sizeof(_abi.muon_adam_tensor) == 16 and ctypes.sizeof(_abi.muon_adam_config) == 16
+
+
+def test_struct_layouts_match_a_c_compiler(tmp_path):
+    """Every field offset and struct size of the ctypes mirrors, against what a C
+    compiler makes of include/*.h."""
+    import shutil
+    import subprocess
+
+    from optimizer_nesterov_momentum_gb300 import _abi
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"muon_shape": _abi.muon_shape, "muon_config": _abi.muon_config,
+               "muon_schedule": _abi.muon_schedule, "muon_adam_tensor": _abi.muon_adam_tensor,
+               "muon_adam_config": _abi.muon_adam_config}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "muon.h"', '#include "muon_adam.h"',
+             'int main(void) {']
+    expect = []
+    for name, cls in structs.items():
+        lines.append(f'  printf("%zu\\n", sizeof({name}));')
+        expect.append(ctypes.sizeof(cls))
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("%zu\\n", offsetof({name}, {field}));')
+            expect.append(getattr(cls, field).offset)
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got == expect
 
 
 def test_config_default(lib):
@@ -167,3 +200,29 @@ def test_missing_library_fails_loudly(tmp_path):
             _abi.load_library(str(tmp_path / "absent.so"))
     finally:
         _abi._lib = saved
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host(lib):
+    """Checked before any CUDA call, so no device is needed (the pointers are never used)."""
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    f = lib.muon_nesterov_normalize_noalloc
+    g, m, x = 0x10000, 0x20000, 0x30000
+    assert f(None, 0, m, x, 8, 8, 0.95, 1, 1, None) == A.MUON_ERR_ARG
+    assert f(g, 0, None, x, 8, 8, 0.95, 1, 1, None) == A.MUON_ERR_ARG
+    assert f(g, 2, m, x, 8, 8, 0.95, 1, 1, None) == A.MUON_ERR_ARG
+    assert f(g, 0, m, m, 8, 8, 0.95, 1, 1, None) == A.MUON_ERR_ARG          # x0 aliases the momentum
+    assert f(m, A.MUON_GRAD_F32, m, x, 8, 8, 0.95, 1, 1, None) == A.MUON_ERR_ARG  # fp32 grad aliases it
+    assert f(g, 0, m, x, 0, 8, 0.95, 1, 1, None) == A.MUON_ERR_SHAPE
+    assert f(g, 0, m, x, 16384, 16385, 0.95, 1, 1, None) == A.MUON_ERR_SHAPE  # 256 x 257 tiles
+    assert f(g, 0, m, x, 1 << 40, 1 << 40, 0.95, 1, 1, None) == A.MUON_ERR_SHAPE  # would overflow a product
+    assert f(g, 0, m, x, 1, (1 << 22) + 1, 0.95, 1, 1, None) == A.MUON_ERR_SHAPE
+
+
+def test_normuon_lanes_is_validated(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    cfg = A.muon_config_default()
+    assert cfg.normuon_lanes == A.MUON_LANES_SHORT_SIDE
+    cfg.normuon_lanes = 3
+    assert _create(lib, [A.muon_shape(64, 256, 0, 1, 0)], cfg) == A.MUON_ERR_ARG

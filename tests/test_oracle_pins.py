@@ -124,16 +124,6 @@ def test_closed_form_matches_iteration(m, n):
     assert _rel(oracle.newton_schulz_closed_form(x, 2, table), oracle.newton_schulz(x, 2, table)) < 1e-9
 
 
-def test_mixed_precision_emulation_is_close_to_fp64():
-    # The mixed-precision diagnostic must stay an approximation of the same
-    # map: within bf16 accuracy of the closed form on a well-conditioned matrix.
-    rng = np.random.default_rng(31)
-    x = _rand_with_spectrum(rng, 48, 96, np.linspace(0.2, 1.0, 48)) * 0.7
-    ref = oracle.newton_schulz(x, steps=5)
-    emu = oracle.newton_schulz_mixed(x, steps=5)
-    assert 1e-4 < _rel(emu, ref) < 5e-2
-
-
 def test_classic_newton_schulz_converges_to_polar_factor():
     rng = np.random.default_rng(11)
     s = np.linspace(0.05, 1.0, 24)
@@ -261,6 +251,84 @@ def test_normuon_constant_update_second_moment_and_norm():
 def test_normuon_zero_update_gives_zero():
     out, v = oracle.normuon_scale(np.zeros((4, 8)), np.zeros(4), 0.95)
     assert np.all(out == 0) and np.all(v == 0)
+
+
+def test_normuon_column_lanes_hand_example_transposed():
+    # The 2 x 4 hand example, transposed: with one lane per column of the 4 x 2
+    # matrix the lanes, v and the scaled update are those of the example, transposed.
+    kv = _load_kv("normuon_hand_2x4.txt")
+    o = _matrix(kv["O"])
+    out, v = oracle.normuon_scale(o.T.copy(), np.zeros(2), float(kv["beta2"]), lanes="cols")
+    assert np.allclose(v, [float(x) for x in kv["v"].split()], rtol=0, atol=1e-15)
+    expect = _matrix(kv["O_prime_over_sqrt_5_8"]) * math.sqrt(5 / 8)
+    assert np.allclose(out, expect.T, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("lanes", ["short_side", "rows", "cols"])
+@pytest.mark.parametrize("rows,cols", [(12, 6), (6, 12), (8, 8)])
+def test_normuon_lane_choice_per_matrix(lanes, rows, cols):
+    # Whatever orientation the iteration runs in, "rows" / "cols" must give one lane per
+    # row / column of the matrix as the caller stores it, and "short_side" one per row of
+    # the short side: checked against normuon_scale applied to the stored orientation.
+    rng = np.random.default_rng(13)
+    g = rng.standard_normal((rows, cols))
+    cfg = oracle.OracleConfig(lr=0.03, normuon_lanes=lanes, beta2=0.9)
+    orc = oracle.MuonOracle([(rows, cols, 1, 1.0, 1.0)], cfg)
+    orc.step([np.zeros((rows, cols))], [g])
+    rec = orc.records[0][0]
+    o_stored = rec.o.T if rec.transposed else rec.o
+    axis = {"short_side": "rows" if rows <= cols else "cols", "rows": "rows", "cols": "cols"}[lanes]
+    out, v = oracle.normuon_scale(o_stored, np.zeros(rows if axis == "rows" else cols), 0.9, lanes=axis)
+    got = rec.o_scaled.T if rec.transposed else rec.o_scaled
+    assert _rel(got, out) < 1e-14 and _rel(rec.v, v) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# non-finite gradients (the library's own failure handling; the pages give none)
+# ---------------------------------------------------------------------------
+
+def test_nonfinite_gradient_skips_only_its_matrix():
+    rng = np.random.default_rng(14)
+    shapes = [(6, 10, 1, 1.0, 1.0), (10, 6, 1, 1.0, 1.0), (4, 16, 2, 1.0, 1.0)]
+    params = [rng.standard_normal((r, c)) for r, c, *_ in shapes]
+    g0 = [rng.standard_normal((r, c)) for r, c, *_ in shapes]
+    g1 = [x.copy() for x in g0]
+    g1[0][2, 3] = np.nan
+    g1[2][3, 9] = np.inf   # the second half of the contiguous bank split (rows 2-3)
+    cfg = oracle.OracleConfig(lr=0.03)
+    bad = oracle.MuonOracle(shapes, cfg)
+    good = oracle.MuonOracle(shapes, cfg)
+    bad.step(params, g0)
+    good.step(params, g0)
+    mom0 = [m.copy() for m in bad.momentum]
+    v0 = [[v.copy() for v in vs] for vs in bad.v]
+    out = bad.step(params, g1)
+    ref = good.step(params, g0)
+    # matrix 0 and the second block of matrix 2 are skipped, all else steps as usual
+    assert np.array_equal(out[0], params[0])
+    assert np.array_equal(bad.v[0][0], v0[0][0]) and bad.records[0][0].skipped
+    assert _rel(out[1], ref[1]) == 0.0 and not bad.records[1][0].skipped
+    assert [r.skipped for r in bad.records[2]] == [False, True]
+    assert np.array_equal(out[2][2:], params[2][2:]) and np.array_equal(out[2][:2], ref[2][:2])
+    # the momentum keeps its old value exactly at the non-finite elements only
+    assert bad.momentum[0][2, 3] == mom0[0][2, 3]
+    mask = np.ones_like(g1[0], dtype=bool)
+    mask[2, 3] = False
+    assert np.array_equal(bad.momentum[0][mask], good.momentum[0][mask])
+    assert bad.momentum[2][3, 9] == mom0[2][3, 9]
+
+
+def test_momentum_overflow_keeps_the_old_value():
+    # mul/add form: mu * b + g beyond the fp32 range is not stored, and the matrix is skipped
+    cfg = oracle.OracleConfig(lr=0.03, lerp_form=False)
+    orc = oracle.MuonOracle([(2, 4, 1, 1.0, 1.0)], cfg)
+    orc.momentum[0][...] = 3.0e38
+    g = np.full((2, 4), 1.0)
+    g[1, 1] = 3.0e38
+    p = np.ones((2, 4))
+    out = orc.step([p], [g])
+    assert orc.momentum[0][1, 1] == 3.0e38 and orc.records[0][0].skipped
+    assert np.array_equal(out[0], p)
 
 
 # ---------------------------------------------------------------------------

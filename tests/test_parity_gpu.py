@@ -353,3 +353,84 @@ def test_graph_capture_replay_matches_eager():
     torch.cuda.synchronize()
     for a, b in zip(pe, pg):
         assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------- caller row strides
+
+def _guarded(rows, cols, ld, dtype, sentinel, guard_rows=8):
+    """A rows x cols view with row stride ld inside a buffer of sentinels: guard_rows
+    full rows before and after it and ld - cols columns after every row.  8 guard
+    rows keep the view's first element 16-byte aligned for 2- and 4-byte types."""
+    buf = torch.full((rows + 2 * guard_rows, ld), sentinel, dtype=dtype, device="cuda")
+    view = buf[guard_rows:guard_rows + rows, :cols]
+    mask = torch.ones_like(buf, dtype=torch.bool)
+    mask[guard_rows:guard_rows + rows, :cols] = False
+    return buf, view, mask
+
+
+@pytest.mark.parametrize("pad", [8, 3])
+def test_strided_caller_buffers_with_guard_bands(pad):
+    """Parameters and gradients as row-strided views (ld = cols + pad) inside sentinel-filled
+    buffers: parity with the oracle, and not one sentinel changed.  pad = 8 keeps the 8-wide
+    vector path where cols allows it; pad = 3 forces the scalar path everywhere.  A bank split
+    into column blocks is included (a contiguous split needs ld == cols)."""
+    shapes = [Shape(96, 200), Shape(200, 96), Shape(130, 300), Shape(64, 512, split=4, split_mode="columns"),
+              Shape(256, 512)]
+    lds = [s.cols + pad for s in shapes]
+    params, grads = _inputs(shapes, 2, seed=51)
+    p_sent, g_sent = 12345.0, -777.0
+    p_bufs, p_views, p_masks = zip(*[_guarded(s.rows, s.cols, ld, torch.float32, p_sent) for s, ld in zip(shapes, lds)])
+    for v, p0 in zip(p_views, params):
+        v.copy_(p0.cuda())
+    g_store = [_guarded(s.rows, s.cols, ld, torch.bfloat16, g_sent) for s, ld in zip(shapes, lds)]
+
+    def grads_gpu_fn(step, grads_cpu):
+        out = []
+        for (buf, view, mask), g in zip(g_store, grads_cpu):
+            view.copy_(g.cuda())
+            out.append(view)
+        return out
+
+    opt = make_optimizer(shapes, ld=lds, lr=0.03, weight_decay=0.01)
+    errs, _, _ = run_parity(shapes, params, grads, lr=0.03, weight_decay=0.01, opt=opt, params_gpu=list(p_views),
+                            grads_gpu_fn=grads_gpu_fn)
+    errs.assert_within()
+    torch.cuda.synchronize()
+    for buf, mask in zip(p_bufs, p_masks):
+        assert torch.all(buf[mask] == p_sent)
+    for buf, _, mask in g_store:
+        assert torch.all(buf[mask] == g_sent)
+
+
+# ----------------------------------------------------------------- NorMuon lanes
+
+@pytest.mark.parametrize("lanes", ["rows", "cols"])
+def test_normuon_lane_axis_flag(lanes):
+    """One second-moment entry per row (or per column) of every matrix as stored, instead of
+    per row of the short side: tall, wide and square matrices on both kernel families."""
+    shapes = [Shape(128, 384), Shape(384, 128), Shape(192, 192), Shape(256, 512), Shape(512, 256),
+              Shape(256, 1024, split=4)]
+    params, grads = _inputs(shapes, 3, seed=61)
+    errs, opt, _ = run_parity(shapes, params, grads, lr=0.03, normuon_lanes=lanes)
+    errs.assert_within()
+    for k in range(opt.num_matrices()):
+        info = opt.matrix_info(k)
+        assert info["lanes"] == (info["rows"] if lanes == "rows" else info["cols"])
+
+
+# ----------------------------------------------------------------- non-finite gradients
+
+def test_nonfinite_gradients_skip_only_their_matrices():
+    """A NaN in one matrix's gradient and an infinity in one block of a split bank: those two
+    matrices keep their parameters and second moment, their momentum keeps its old value at
+    the bad elements, every other matrix steps as usual, the step reports
+    MUON_ERR_NONFINITE, and the next step with finite gradients is normal again."""
+    shapes = [Shape(128, 384), Shape(384, 128), Shape(256, 1024, split=4), Shape(256, 512)]
+    params, grads = _inputs(shapes, 3, seed=71, grad_dtype="f32")
+    grads[1][0][5, 7] = float("nan")
+    # the contiguous split views the [256, 1024] bank as four [256, 256] blocks of consecutive
+    # memory: parent rows 128..191 hold the third block
+    grads[1][2][130, 11] = float("inf")
+    grads[1][2][131, 600] = float("-inf")
+    errs, _, _ = run_parity(shapes, params, grads, lr=0.03, grad_dtype="f32")
+    errs.assert_within()
