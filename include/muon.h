@@ -267,12 +267,14 @@ int muon_set_state(muon_handle h, int32_t which, int32_t index, const void* src,
 /* ---- test support ----------------------------------------------------------
  *
  * For failure-handling tests only; no part of the optimizer step uses it.
- * Makes the next muon_step's first polynomial launch (a one-SM tcgen05 kernel)
- * wait on an mbarrier that nothing arrives on, so that its bounded wait gives
- * up after about 2 s: the kernel then sets the status word, lets the copies it
- * issued land, frees its TMEM and returns, and the step leaves the parameters
- * and second moment unchanged (see "Errors").  One-shot.  MUON_ERR_ARG when
- * gemm_engine is not MUON_GEMM_TCGEN05. */
+ * Makes the next muon_step's first one-SM polynomial launch (a tcgen05 kernel
+ * that serves the matrices whose sides are not multiples of 256) wait on an
+ * mbarrier that nothing arrives on, so that its bounded wait gives up after
+ * about 2 s: the kernel then sets the status word, lets the copies it issued
+ * land, frees its TMEM and returns, and the step leaves the parameters and
+ * second moment unchanged (see "Errors").  One-shot.  MUON_ERR_ARG when
+ * gemm_engine is not MUON_GEMM_TCGEN05 or when every matrix of the handle
+ * tiles by 256 (no one-SM polynomial runs). */
 int muon_debug_inject_stall(muon_handle h);
 
 /* ---- allocation-free entry point ------------------------------------------

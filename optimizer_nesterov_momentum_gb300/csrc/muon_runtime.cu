@@ -42,8 +42,8 @@ cudaError_t ns_gemm_tc_configure();
 cudaError_t ns_update_pair_configure();
 cudaError_t launch_ns_update_pair(const GemmParams&, bool, int, cudaStream_t);
 cudaError_t ns_gram_pair_configure();
-template <bool F16>
-cudaError_t launch_ns_gram_pair(const GemmParams&, int, cudaStream_t);
+template <int MODE, bool F16>
+cudaError_t launch_ns_sym_pair(const GemmParams&, int, cudaStream_t);
 template <int MODE, bool F16>
 cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
 template <int MODE>
@@ -80,9 +80,11 @@ struct Group {
     // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
+    CUtensorMap map_a_mn;      // 64 x 64 boxes of A: the MN-major right operand of the SM-pair polynomial
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
     CUtensorMap map_x_w32[2];  // 32 x 32 boxes, 64-byte swizzle: stores of the SM-pair update's warps
-    CUtensorMap map_a_w32;     // the same for A (SM-pair Gram)
+    CUtensorMap map_a_w32;     // the same for A (SM-pair Gram stores, SM-pair polynomial's b A input)
+    CUtensorMap map_p_w32;     // and for P (SM-pair polynomial stores)
     CUtensorMap map_u_hi_w32, map_u_lo_w32;  // and for u's halves (first SM-pair update)
 };
 
@@ -117,7 +119,8 @@ struct muon_s {
     std::vector<int64_t> mom_off;       // per parent, offset into momentum arena (floats)
     int32_t n_elem_tiles = 0;
     int32_t n_colwork = 0;              // (sub, slab) blocks of k_col_sumsq (column lanes only)
-    bool stall_next = false;            // muon_debug_inject_stall: the next step's first polynomial stalls
+    bool stall_next = false;            // muon_debug_inject_stall: the next step's first one-SM polynomial stalls
+    int stall_chunk = -1;               // the launch chunk whose polynomial runs on one SM per tile
     // device memory
     void* arena = nullptr;
     size_t arena_bytes = 0;
@@ -642,7 +645,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                   encode_bf16_3d(enc, &g.map_a_k, g.a16, g.m, g.m, g.count, g.lda, kBM) &&
                   encode_bf16_3d(enc, &g.map_p_k, g.p16, g.m, g.m, g.count, g.lda, kBM) &&
                   encode_bf16_3d(enc, &g.map_u_k256, g.u16, g.n, g.m, g.count, g.ldx, 2 * kBM) &&
-                  encode_bf16_3d(enc, &g.map_a_k256, g.a16, g.m, g.m, g.count, g.lda, 2 * kBM);
+                  encode_bf16_3d(enc, &g.map_a_k256, g.a16, g.m, g.m, g.count, g.lda, 2 * kBM) &&
+                  encode_bf16_3d(enc, &g.map_a_mn, g.a16, g.m, g.m, g.count, g.lda, 64);
         for (int b = 0; b < 2 && ok; ++b)
             ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
                  encode_bf16_3d(enc, &g.map_x_k256[b], g.x16[b], g.n, g.m, g.count, g.ldx, 2 * kBM) &&
@@ -653,6 +657,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                            g.ldx, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         ok = ok &&
              encode_3d(enc, &g.map_a_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.a16, g.m, g.m, g.count, g.lda, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_3d(enc, &g.map_p_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.p16, g.m, g.m, g.count, g.lda, 32, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_3d(enc, &g.map_u_hi_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.u16, g.n, g.m, g.count, g.ldx, 32,
                        32, CU_TENSOR_MAP_SWIZZLE_64B) &&
@@ -761,6 +767,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 } else if (mode == MODE_GRAM) {
                     gp.tiles = h->d_gemm_tiles + ch.gram_off;
                     gp.ntiles = ch.gram_n;
+                } else if (mode == MODE_POLY && ch.spg_n > 0) {
+                    // the polynomial on SM pairs: the same 256 x 256 tiles (J >= I) as the Gram
+                    gp.tiles = h->d_gemm_tiles + ch.spg_off;
+                    gp.ntiles = ch.spg_n;
+                    gp.pair = 1;
                 } else if (mode == MODE_POLY) {
                     gp.tiles = h->d_gemm_tiles + ch.poly_off;
                     gp.ntiles = ch.poly_n;
@@ -798,9 +809,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         G.opr16 = xin16;
                     } else if (mode == MODE_POLY) {
                         gp.map_a[sl] = g.map_a_k;
-                        gp.map_b[sl] = g.map_a_k256;
-                        gp.map_ein[sl] = g.map_a_k;
-                        gp.map_out[sl] = g.map_p_k;
+                        gp.map_b[sl] = gp.pair ? g.map_a_mn : g.map_a_k256;
+                        gp.map_ein[sl] = gp.pair ? g.map_a_w32 : g.map_a_k;
+                        gp.map_out[sl] = gp.pair ? g.map_p_w32 : g.map_p_k;
                         gp.map_out2[sl] = g.map_p_mir;
                         G.out16 = g.p16;
                         G.opl16 = g.a16;
@@ -855,7 +866,7 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
             for (int c = 0; c < nch; ++c) {
                 const GemmParams* gpp = &h->gparams[((size_t)it * nch + c) * 3 + mode];
                 GemmParams stalled;
-                if (h->stall_next && it == 0 && c == 0 && mode == MODE_POLY &&
+                if (h->stall_next && it == 0 && c == h->stall_chunk && mode == MODE_POLY &&
                     h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
                     // test only (muon_debug_inject_stall): this launch's MMA issuers wait on an
                     // mbarrier that nothing arrives on until their bounded wait gives up
@@ -871,11 +882,15 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                     const bool f16 = it > 0;
                     cudaError_t e = cudaSuccess;
                     if (mode == MODE_GRAM && gp.pair)
-                        e = f16 ? launch_ns_gram_pair<true>(gp, h->num_sms, s) : launch_ns_gram_pair<false>(gp, h->num_sms, s);
+                        e = f16 ? launch_ns_sym_pair<MODE_GRAM, true>(gp, h->num_sms, s)
+                                : launch_ns_sym_pair<MODE_GRAM, false>(gp, h->num_sms, s);
                     else if (mode == MODE_GRAM)
                         e = f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, s)
                                 : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, s);
-                    if (mode == MODE_POLY)
+                    if (mode == MODE_POLY && gp.pair)
+                        e = f16 ? launch_ns_sym_pair<MODE_POLY, true>(gp, h->num_sms, s)
+                                : launch_ns_sym_pair<MODE_POLY, false>(gp, h->num_sms, s);
+                    else if (mode == MODE_POLY)
                         e = f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
                                 : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s);
                     if (mode == MODE_UPDATE)
@@ -1147,6 +1162,12 @@ int muon_debug_inject_stall(muon_handle h) {
     if (rc) return rc;
     if (h->cfg.gemm_engine != MUON_GEMM_TCGEN05)
         return fail(h, MUON_ERR_ARG, "the stall is injected into a tensor-core kernel (gemm_engine TCGEN05 only)");
+    // the stall goes into the one-SM polynomial kernel: a chunk of groups that do not tile by 256
+    h->stall_chunk = -1;
+    for (int c = 0; c < (int)h->chunks.size() && h->stall_chunk < 0; ++c)
+        if (h->chunks[c].spg_n == 0) h->stall_chunk = c;
+    if (h->stall_chunk < 0)
+        return fail(h, MUON_ERR_ARG, "no matrix of this handle runs the one-SM polynomial (every shape tiles by 256)");
     h->stall_next = true;
     return MUON_OK;
 }

@@ -1,22 +1,33 @@
-// The Gram product of the Newton-Schulz iteration on SM pairs ("modded-nanogpt
-// 50B-token" write-up, section "Muon from the source"):
+// The two symmetric products of the Newton-Schulz iteration on SM pairs
+// ("modded-nanogpt 50B-token" write-up, section "Muon from the source",
+// grouped as X <- a X + (b A + c A^2) X):
 //
-//   A = sc * X X^T      (sc = (s / c)^2 on the first iteration, else 1)
+//   MODE_GRAM   A = sc * X X^T        (sc = (s / c)^2 on the first iteration, else 1)
+//   MODE_POLY   P = b A + c A A       (A symmetric, so A A = A A^T: the same product
+//                                      as the Gram with A's rows for X's; from the
+//                                      second iteration on the epilogue adds a to
+//                                      the diagonal: P' = a I + P)
 //
 // with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) issued by CTA 0 of a
 // two-CTA cluster.  A pair tile is the 256 x 256 block (I, J), J >= I, of the
-// symmetric result.  CTA r stages rows 256 I + 128 r .. + 127 of X (the left
-// operand's half) and rows 256 J + 128 r .. + 127 (the right operand's half,
-// both K-major), so an off-diagonal tile stages 32 KB per SM per 64-deep
-// k-block and a diagonal tile, whose two halves are the same rows, 16 KB.
-// CTA r's TMEM receives rows 128 r .. + 127 of the tile.
+// symmetric result.  CTA r stages rows 256 I + 128 r .. + 127 of the operand
+// (the left operand's half, K-major) and the right operand's half: for the
+// Gram, rows 256 J + 128 r .. + 127 of X (K-major); for the polynomial,
+// columns 256 J + 128 r .. + 127 of A (MN-major: A is symmetric, so its
+// columns are its rows, and the tensor cores take an MN-major right operand
+// at full rate where two K-major operands of a short K ran the MMAs at about
+// half rate).  An off-diagonal tile stages 32 KB per SM per 64-deep k-block;
+// a diagonal Gram tile, whose two halves are the same rows, 16 KB.  CTA r's
+// TMEM receives rows 128 r .. + 127 of the tile.
 //
 // The epilogue works warp by warp: warp (quad, half) owns TMEM lanes
 // 32 quad .. + 31 and columns 32 half .. + 31 of each 64-column chunk, i.e.
 // four 32 x 32 blocks per tile.  It stores each block, and for an
 // off-diagonal tile (I < J) also its transpose at (J, I), from its own ring of
 // shared-memory slots; a diagonal tile is computed whole (both triangles) and
-// stored once.  No barrier spans warps.
+// stored once.  The polynomial's b A term comes from A's own 32 x 32 blocks,
+// which each warp TMA-loads two blocks ahead into a private two-slot ring.
+// No barrier spans warps.
 //
 // Warp 0: TMA producer (both CTAs), warp 1: pair-wide TMEM allocation (both)
 // and the MMA issuer (CTA 0), warps 2-9: epilogue (both).  All mbarrier waits
@@ -34,32 +45,44 @@ constexpr int kSymStage = 2 * kSymRows;  // left half | right half
 constexpr int kBlk = 32 * 32 * 2;        // one 32 x 32 16-bit block (64-byte rows, 64-byte swizzle)
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
-
-constexpr int kGramStages = 6;
 constexpr int kOutSlots = 2;  // per warp: blocks and mirrors in flight
-constexpr int kGramSmem = kGramStages * kSymStage + kEpiWarps * kOutSlots * kBlk + 1024 + 512;
-static_assert(kGramSmem <= 232448, "shared memory budget");
+
+template <int MODE>
+struct SymPairCfg {
+    static constexpr bool POLY = MODE == MODE_POLY;
+    // the polynomial gives up one stage for its per-warp input ring (two 32 x 32 blocks of A)
+    static constexpr int STAGES = POLY ? 5 : 6;
+    static constexpr int IN_SLOTS = POLY ? 2 : 0;
+    static constexpr int SMEM = STAGES * kSymStage + kEpiWarps * (kOutSlots + IN_SLOTS) * kBlk + 1024 + 512;
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
 
 }  // namespace
 
 using namespace pair;
 
-template <bool F16>
+template <int MODE, bool F16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
-    k_ns_gram_pair(const __grid_constant__ GemmParams p) {
-    constexpr int STAGES = kGramStages;
-    constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/false, F16);
+    k_ns_sym_pair(const __grid_constant__ GemmParams p) {
+    using C = SymPairCfg<MODE>;
+    constexpr int STAGES = C::STAGES;
+    // the polynomial's right operand is MN-major (columns of the symmetric A)
+    constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/C::POLY, F16);
+    // the polynomial of the second and later iterations adds a to the diagonal of P
+    constexpr bool FOLD = C::POLY && F16;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sS = smem;                                   // STAGES x (left | right)
     uint8_t* sO = sS + STAGES * kSymStage;                // per warp kOutSlots blocks
-    uint64_t* full = reinterpret_cast<uint64_t*>(sO + kEpiWarps * kOutSlots * kBlk);  // CTA 0's are used
+    uint8_t* sI = sO + kEpiWarps * kOutSlots * kBlk;      // POLY: per warp IN_SLOTS blocks of A
+    uint64_t* full = reinterpret_cast<uint64_t*>(sI + kEpiWarps * C::IN_SLOTS * kBlk);  // CTA 0's are used
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;   // [2]
     uint64_t* tempty = tfull + 2;       // [2] CTA 0's: 8 warps of each CTA arrive
     uint64_t* mma_done = tempty + 2;    // abort path only
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* in_full = mma_done + 1;   // POLY: [kEpiWarps][2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_full + 2 * kEpiWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* pair_ok = abort_flag + 1;
 
@@ -79,6 +102,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             mbar_init(&tempty[a], 2 * kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&in_full[i], 1);
         *tmem_slot = kNoTmem;
         *abort_flag = 0;
         *pair_ok = 0;
@@ -109,7 +133,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ operand producer (both CTAs)
         if (lane == 0 && run) {
-            for (int g = 0; g < p.ngroups; ++g) tma_prefetch_desc(&p.map_a[g]);
+            for (int g = 0; g < p.ngroups; ++g) {
+                tma_prefetch_desc(&p.map_a[g]);
+                if (C::POLY) tma_prefetch_desc(&p.map_b[g]);
+            }
             const uint32_t full0 = cluster_addr(&full[0], 0);
             int stage = 0;
             uint32_t phase = 0;
@@ -117,9 +144,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = p.tiles[t];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
-                const int K = p.grp[g].n;
+                const int K = C::POLY ? p.grp[g].m : p.grp[g].n;
                 const int nkb = (K + kBK - 1) / kBK;
-                const bool diag = ti == tj;
+                const bool diag = !C::POLY && ti == tj;  // a diagonal Gram tile stages one set of rows
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
@@ -129,7 +156,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     const uint32_t bar = full0 + (uint32_t)(stage * 8);
                     uint8_t* dst = sS + stage * kSymStage;
                     tma_load_3d_pair(dst, &p.map_a[g], bar, kb * kBK, ti * 256 + (int)rank * kBM, idx);
-                    if (!diag) tma_load_3d_pair(dst + kSymRows, &p.map_a[g], bar, kb * kBK, tj * 256 + (int)rank * kBM, idx);
+                    if (C::POLY) {
+                        // columns 256 J + 128 r .. + 127 of A for k-block rows kb: two 64-column boxes
+                        const int col = tj * 256 + (int)rank * 128;
+                        tma_load_3d_pair(dst + kSymRows, &p.map_b[g], bar, col, kb * kBK, idx);
+                        tma_load_3d_pair(dst + kSymRows + 64 * kBK * 2, &p.map_b[g], bar, col + 64, kb * kBK, idx);
+                    } else if (!diag) {
+                        tma_load_3d_pair(dst + kSymRows, &p.map_a[g], bar, kb * kBK, tj * 256 + (int)rank * kBM, idx);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -149,9 +183,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             const uint32_t s_base = smem_u32(sS);
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = p.tiles[t];
-                const int K = p.grp[tile.x].n;
+                const int K = C::POLY ? p.grp[tile.x].m : p.grp[tile.x].n;
                 const int nkb = (K + kBK - 1) / kBK;
-                const bool diag = tile.z == tile.w;
+                const bool diag = !C::POLY && tile.z == tile.w;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -169,7 +203,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t adesc = make_sdesc_sw128(a_st + kk * 32, 16, 1024);
-                        const uint64_t bdesc = make_sdesc_sw128(b_st + kk * 32, 16, 1024);
+                        // K-major right operand: 32 bytes further per 16-deep step; MN-major
+                        // (polynomial): 16 rows of 128 bytes further, 8 KB between 64-column boxes
+                        const uint64_t bdesc = C::POLY ? make_sdesc_sw128(b_st + kk * (16 * 128), 64 * kBK * 2, 1024)
+                                                       : make_sdesc_sw128(b_st + kk * 32, 16, 1024);
                         umma_f16_pair(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
                         any = true;
                     }
@@ -197,23 +234,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
         const int half = ew >> 2;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         uint8_t* wout = sO + ew * (kOutSlots * kBlk);
+        uint8_t* win = sI + ew * (C::IN_SLOTS * kBlk);  // POLY: slot c & 1 holds A's block of chunk c
+        uint64_t* ibar = &in_full[2 * ew];
         const uint32_t tempty0 = cluster_addr(&tempty[0], 0);
         int acc = 0;
         uint32_t acc_phase = 0;
         int nout = 0;  // output slots used so far (one bulk group each)
+        uint32_t in_phase[2] = {0u, 0u};
+        bool in_pending[2] = {false, false};
+        if (C::POLY && lane == 0)
+            for (int g = 0; g < p.ngroups; ++g) tma_prefetch_desc(&p.map_ein[g]);
         for (int t = pr; run && t < p.ntiles; t += npairs) {
             const int4 tile = p.tiles[t];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             const bool diag = ti == tj;
             const int row0 = ti * 256 + (int)rank * kBM + quad * 32;  // this warp's first row
+            // POLY: A's block of chunk c at (row0, this warp's columns of chunk c), lane 0 issues
+            auto load_in = [&](int c, int sl) {
+                mbar_arrive_expect_tx(&ibar[sl], kBlk);
+                tma_load_3d(win + sl * kBlk, &p.map_ein[g], &ibar[sl], tj * 256 + c * 64 + half * 32, row0, idx);
+                in_pending[sl] = true;
+            };
+            if (C::POLY && lane == 0) {
+                load_in(0, 0);  // before the accumulator is ready
+                load_in(1, 1);
+            }
             mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
             tc_fence_after();
             uint32_t raw[2][32];
             const uint32_t t_acc = tbase + (uint32_t)(acc * 256) + lane_off + (uint32_t)(half * 32);
+            // the iterate is stored as X / c (c = ||X0||): the first Gram scales u u^T by (s / c)^2;
+            // A A carries a factor c^2 against the stored A / c^2
+            const float cs = p.iter_scale[G.sub0 + idx];
+            const float c2 = cs * cs;
             float scale = 1.f;
-            if (p.first) {
-                const float s = p.norm_scale[G.sub0 + idx] / p.iter_scale[G.sub0 + idx];
+            if (!C::POLY && p.first) {
+                const float s = p.norm_scale[G.sub0 + idx] / cs;
                 scale = s * s;
             }
 #pragma unroll
@@ -231,9 +288,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     }
                 }
                 const int col0 = tj * 256 + c * 64 + half * 32;  // this block's first column
+                float v[32];
+                if (C::POLY) {
+                    // P / c^2 = b (A / c^2) + c c^2 (A / c^2)^2 ; from the second iteration on
+                    // P' = a I + c^2 (P / c^2), stored unscaled
+                    const int sl = c & 1;
+                    mbar_wait(&ibar[sl], in_phase[sl], abort_flag, p.status);
+                    in_phase[sl] ^= 1u;
+                    in_pending[sl] = false;
+                    uint4 aw[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        aw[jj] = *reinterpret_cast<const uint4*>(win + sl * kBlk + sw64((uint32_t)lane, (uint32_t)jj));
+                    const int dcol = row0 + lane - col0;  // this lane's diagonal element, if in the block
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t ws[4] = {aw[jj].x, aw[jj].y, aw[jj].z, aw[jj].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int e = 8 * jj + 2 * h;
+                            const float a0 = x2f<F16>((uint16_t)(ws[h] & 0xFFFFu));
+                            const float a1 = x2f<F16>((uint16_t)(ws[h] >> 16));
+                            float p0 = fmaf(p.cb, a0, (p.cc * c2) * __uint_as_float(raw[c & 1][e]));
+                            float p1 = fmaf(p.cb, a1, (p.cc * c2) * __uint_as_float(raw[c & 1][e + 1]));
+                            if (FOLD) {
+                                p0 = c2 * p0 + (e == dcol ? p.ca : 0.f);
+                                p1 = c2 * p1 + (e + 1 == dcol ? p.ca : 0.f);
+                            }
+                            v[e] = p0;
+                            v[e + 1] = p1;
+                        }
+                    }
+                    // The slot goes back to the copy engine only after every lane has used what it
+                    // read (the loads are complete) and ordered those reads before the async
+                    // proxy's write: otherwise, under heavy shared-memory traffic, the next block's
+                    // copy could land before a lane's read of this one is served.
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && c + 2 < 4) load_in(c + 2, sl);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = scale * __uint_as_float(raw[c & 1][e]);
+                }
                 uint16_t b[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) b[e] = f2x<F16>(scale * __uint_as_float(raw[c & 1][e]));
+                for (int e = 0; e < 32; ++e) b[e] = f2x<F16>(v[e]);
 
                 // this block at (row0, col0)
                 {
@@ -278,6 +377,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (C::POLY && lane == 0) {
+            // input copies of an aborted run still in flight must land before the CTA exits
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl)
+                if (in_pending[sl]) mbar_wait_drain(&ibar[sl], in_phase[sl], 100000000ull);
+        }
         if (lane == 0) bulk_wait<0>();
     }
 
@@ -298,23 +403,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     }
 }
 
+template <int MODE, bool F16>
+static cudaError_t configure_sym() {
+    return cudaFuncSetAttribute(k_ns_sym_pair<MODE, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SymPairCfg<MODE>::SMEM);
+}
+
 cudaError_t ns_gram_pair_configure() {
-    cudaError_t e = cudaFuncSetAttribute(k_ns_gram_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_ns_gram_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGramSmem);
+    cudaError_t e = configure_sym<MODE_GRAM, false>();
+    if (e == cudaSuccess) e = configure_sym<MODE_GRAM, true>();
+    if (e == cudaSuccess) e = configure_sym<MODE_POLY, false>();
+    if (e == cudaSuccess) e = configure_sym<MODE_POLY, true>();
     return e;
 }
 
 // p.tiles: 256 x 256 tiles {group slot, index, tile row I, tile column J >= I} (units of 256).
-template <bool F16>
-cudaError_t launch_ns_gram_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
+// MODE_GRAM: p.map_a = 128-row boxes of the iterate (K = n); MODE_POLY: of A (K = m), with
+// p.map_b = A's 64 x 64 boxes (the MN-major right operand) and p.map_ein = A's 32 x 32 boxes
+// for the b A term.  p.map_out: 32 x 32 boxes of the result.
+template <int MODE, bool F16>
+cudaError_t launch_ns_sym_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
     const int pairs = p.ntiles < num_sms / 2 ? p.ntiles : num_sms / 2;
-    k_ns_gram_pair<F16><<<2 * pairs, kSymThreads, kGramSmem, stream>>>(p);
+    k_ns_sym_pair<MODE, F16><<<2 * pairs, kSymThreads, SymPairCfg<MODE>::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_ns_gram_pair<false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gram_pair<true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_GRAM, false>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
 
 }  // namespace muon

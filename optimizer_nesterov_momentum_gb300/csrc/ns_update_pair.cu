@@ -298,8 +298,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         lw[jj] = *reinterpret_cast<const uint4*>(win + sl * 2 * kWarpSlot + kWarpSlot +
                                                                  sw64((uint32_t)lane, (uint32_t)jj));
                     }
-                    __syncwarp();  // every lane has read the slot
-                    if (lane == 0 && c + 2 < 4) load_in(c + 2, sl);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
                         const uint32_t hs[4] = {hw[jj].x, hw[jj].y, hw[jj].z, hw[jj].w};
@@ -319,6 +317,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                             }
                         }
                     }
+                    // the slot goes back to the copy engine only after every lane has used what it
+                    // read and ordered those reads before the async proxy's write
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && c + 2 < 4) load_in(c + 2, sl);
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
