@@ -511,14 +511,20 @@ def run_ours(args):
     ns_tflops = model["ns_flops"] / (ns_ms * 1e-3) / 1e12
     total_stage = sum(stage_ms.values())
     dom = max(("momentum", "apply", "gram", "poly", "update"), key=lambda k: kern[k]["ms"])
+    # DRAM traffic per launch of the dominant kernel, from the single-pass ncu capture summarised in
+    # profiles/dram_traffic_<workload>.md (a line "traffic_bytes_per_launch <stage> <bytes>")
     traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    tr_path = os.path.join(ROOT, "profiles", f"dram_traffic_{wl.name}.md")
     if os.path.exists(tr_path):
         with open(tr_path) as f:
-            traffic = json.load(f).get(wl.name, {}).get(dom)
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and parts[0] == "traffic_bytes_per_launch" and parts[1] == dom:
+                    traffic = float(parts[2])
     d = kern[dom]
     roofline = {"bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"],
                 "frac": d["frac"], "traffic": traffic, "kernel": dom,
+                "algorithmic_bytes_per_launch": d.get("bytes_per_launch", d.get("algorithmic_per_launch")),
                 "peak_source": f"{peak_src} ({'hbm_gbs' if d['unit'] == 'GB/s' else tc_key})",
                 "share_of_step": d["ms"] / total_stage}
     if d["unit"] == "TFLOP/s":

@@ -144,9 +144,11 @@ template <int CAP, bool GRAD_F32>
 __global__ void __launch_bounds__(256, 6) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float su[kTile][kTile + 1];
     __shared__ float red[8];
-    if (*p.status & kStatusFatal) return;  // an earlier step failed: leave the momentum as it is
+    // the status word is loaded alongside the tile and descriptor loads and tested after them
+    const int fatal = *p.status & kStatusFatal;
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
+    if (fatal) return;  // an earlier step failed: leave the momentum as it is (uniform over the block)
     const int r0 = tile.y, c0 = tile.z;
     const float mu = p.hp[HP_MU];
     const int tr = threadIdx.x >> 3, tc = threadIdx.x & 7;
@@ -311,18 +313,29 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
 template <int CAP>
 __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float so[kTile][kTile + 1];
-    if (*p.status & kStatusFatal) return;  // a Newton-Schulz launch failed: keep the caller's parameters
+    // Everything a block needs before its data loads sits on a chain of dependent loads
+    // (tile -> matrix descriptor -> parameter pointer); the status word, the hyper-parameters
+    // and the skip flag are loaded alongside, and tested only once the data loads are in
+    // flight, so they add no latency of their own.
+    const int fatal = *p.status & kStatusFatal;  // a Newton-Schulz launch failed: keep the parameters
+    const float lr = p.hp[HP_LR], wd = p.hp[HP_WD];
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
-    if (*d.skip) return;                   // this matrix's direction was not finite
     const int r0 = tile.y, c0 = tile.z;
     const int tr = threadIdx.x >> 3, tc = threadIdx.x & 7;
-    const float decay = 1.f - p.hp[HP_LR] * d.lr_mul * p.hp[HP_WD] * d.wd_mul;
     float* P = p.ptr.param[d.parent] + d.grad_off;
+    // lanes along the caller's columns (rows of a transposed matrix's wide orientation, or the
+    // wide columns of an untransposed one), else along its rows
+    const bool per_col = d.transposed != d.lane_cols;
 
-    // loads of both row passes first
-    float pv[2][8], o[2][8];
+    // loads of both row passes first; the lane factors are per column (the same eight for both
+    // passes) or per row (one per pass)
+    float pv[2][8], o[2][8], fcol[8], frow[2] = {0.f, 0.f};
     bool act[2];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fcol[e] = 0.f;
+    if (per_col && c0 + tc * 8 < d.cols && r0 + tr < d.rows)
+        for (int e = 0; e < 8; ++e) fcol[e] = (c0 + tc * 8 + e < d.cols) ? d.lane[c0 + tc * 8 + e] : 0.f;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
         const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
@@ -343,8 +356,11 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
                 else
                     for (int e = 0; e < 8 && c + e < d.cols; ++e) o[pass][e] = h2f(src[e]);
             }
+            if (!per_col) frow[pass] = d.lane[r];
         }
     }
+    const int skip = *d.skip;  // this matrix's direction was not finite
+    if (fatal || skip) return;  // uniform over the block, before any barrier or store
 
     if (d.transposed) {
         // O is stored in the wide orientation: stage its tile transposed through shared memory
@@ -374,24 +390,15 @@ __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemPa
         }
     }
 
+    const float decay = 1.f - lr * d.lr_mul * wd * d.wd_mul;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
         if (!act[pass]) continue;
         const int r = r0 + pass * 32 + tr, c = c0 + tc * 8;
         float* pp = P + (int64_t)r * d.ld + c;
-        // lanes along the caller's columns (rows of a transposed matrix's wide
-        // orientation, or the wide columns of an untransposed one), else along its rows
-        float f[8];
-        if (d.transposed != d.lane_cols) {
-            for (int e = 0; e < 8; ++e) f[e] = (c + e < d.cols) ? d.lane[c + e] : 0.f;
-        } else {
-            const float fr = d.lane[r];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = fr;
-        }
         float out[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) out[e] = fmaf(-f[e], o[pass][e], pv[pass][e] * decay);
+        for (int e = 0; e < 8; ++e) out[e] = fmaf(-(per_col ? fcol[e] : frow[pass]), o[pass][e], pv[pass][e] * decay);
         if (d.vec) {
             store8_f32(pp, out);
         } else {
