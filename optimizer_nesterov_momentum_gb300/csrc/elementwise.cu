@@ -33,6 +33,7 @@
 
 namespace muon {
 
+// Sum over the block (up to 32 warps; red holds one float per warp).
 __device__ __forceinline__ float block_sum_256(float v, float* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -269,8 +270,10 @@ __global__ void __launch_bounds__(256) k_col_sumsq(const __grid_constant__ ColSu
     }
 }
 
-__global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ LaneParams p) {
-    __shared__ float red[8];
+constexpr int kLaneThreads = 1024;  // one block per matrix, one thread per lane up to 1024 lanes
+
+__global__ void __launch_bounds__(kLaneThreads) k_lane_stats(const __grid_constant__ LaneParams p) {
+    __shared__ float red[32];
     const SubDesc& d = p.subs[blockIdx.x];
     // a failed step (fatal status) or a non-finite direction: the second moment stays as it is
     if ((*p.status & kStatusFatal) || *d.skip) return;
@@ -279,20 +282,14 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
     const int nl = d.lane_cols ? d.n : d.m;     // lanes
     if (!p.normuon) {
         const float f = eff * d.shape_scale * cs;
-        for (int i = threadIdx.x; i < nl; i += 256) d.lane[i] = f;
+        for (int i = threadIdx.x; i < nl; i += kLaneThreads) d.lane[i] = f;
         return;
     }
     const float beta2 = p.hp[HP_BETA2];
     const float inv_len = 1.f / (float)(d.lane_cols ? d.m : d.n);  // the mean runs across the lanes' length
-    const int nslab = (d.m + kTile - 1) / kTile;
     float before = 0.f, after = 0.f;
-    for (int i = threadIdx.x; i < nl; i += 256) {
-        float rs = 0.f;
-        if (d.lane_cols) {
-            for (int t = 0; t < nslab; ++t) rs += d.colsq[(int64_t)t * d.n + i];
-        } else {
-            for (int t = 0; t < 2 * d.ntile_n; ++t) rs += d.rowsq[(int64_t)i * d.ntile_n * 2 + t];
-        }
+    // v <- lerp(v, r, 1 - beta2) and the lane's rsqrt, given the lane's sum of O^2 (stored scale)
+    auto lane_update = [&](int i, float rs) {
         rs *= cs * cs;
         const float r = rs * inv_len;
         const float v0 = d.v[i];
@@ -302,12 +299,22 @@ __global__ void __launch_bounds__(256) k_lane_stats(const __grid_constant__ Lane
         d.lane[i] = q;
         before += rs;
         after = fmaf(rs, q * q, after);
+    };
+    // one thread per lane; the partial sums are stored part-major ([part][lane]), so neighbouring
+    // threads read neighbouring words, and each lane adds its parts in a fixed order
+    const int nparts = d.lane_cols ? (d.m + kTile - 1) / kTile : 2 * d.ntile_n;
+    const float* parts = d.lane_cols ? d.colsq : d.rowsq;
+    for (int i = threadIdx.x; i < nl; i += kLaneThreads) {
+        float rs = 0.f;
+#pragma unroll 4
+        for (int t = 0; t < nparts; ++t) rs += parts[(int64_t)t * nl + i];
+        lane_update(i, rs);
     }
     const float sb = block_sum_256(before, red);
     const float sa = block_sum_256(after, red);
     const float gamma = p.norm_preserve ? sqrtf(sb) / fmaxf(sqrtf(sa), kVFloor) : 1.f;
     const float f = eff * gamma * cs;
-    for (int i = threadIdx.x; i < nl; i += 256) d.lane[i] *= f;
+    for (int i = threadIdx.x; i < nl; i += kLaneThreads) d.lane[i] *= f;
 }
 
 template <int CAP>
@@ -501,7 +508,7 @@ cudaError_t launch_col_sumsq(const ColSumParams& p, cudaStream_t s) {
 
 cudaError_t launch_lane_stats(const LaneParams& p, cudaStream_t s) {
     if (p.nsubs <= 0) return cudaSuccess;
-    k_lane_stats<<<p.nsubs, 256, 0, s>>>(p);
+    k_lane_stats<<<p.nsubs, kLaneThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -11,8 +11,9 @@
 //       a16 / p16   A = X X^T and P = b A + c A A, m x m: bf16 in the first
 //                   iteration (on u), fp16 after (S5, S6); from the second
 //                   iteration on p16 holds P' = a I + P, unscaled
-//       rowsq       per (row, 256-column tile, column half) sums of O^2 from the
-//                   last iteration (S8)
+//       rowsq       per (256-column tile, column half, row) sums of O^2 from the
+//                   last iteration (S8), part-major so that one thread per row
+//                   reads (and the epilogue writes) neighbouring words
 //       colsq       column lanes only: per (64-row slab, column) sums of O^2
 //       v           second moment, fp32, one per lane (S8): [m] when the lanes are
 //                   the rows of the wide orientation (the default), [n] when they
@@ -80,7 +81,7 @@ struct SubDesc {
     uint16_t* u16;        // hi half of u (bf16(u))
     uint16_t* ulo16;      // lo half of u (bf16(u - hi))
     const uint16_t* o16;  // final Newton-Schulz output (fp16), m x n, row stride ldx
-    float* rowsq;         // m x ntile_n x 2
+    float* rowsq;         // (ntile_n x 2) x m, part-major
     float* colsq;         // lane_cols: ceil(m / 64) x n
     float* v;             // one per lane
     float* lane;          // one per lane
@@ -118,7 +119,7 @@ struct GemmGroup {
     uint16_t* x16_out;       // update: the next iterate / final O (fp16)
     const uint16_t* a16;     // poly epilogue: A (also simt operand)
     uint16_t* out16;         // gram: A, poly: P
-    float* rowsq;            // update, last iteration: per-row sums of O^2 (m * ntile_n * 2 per matrix)
+    float* rowsq;            // update, last iteration: per-row sums of O^2 ([ntile_n * 2][m] per matrix)
     const uint16_t* opl16;   // simt: left operand base (gram: X, poly: A, update: P)
     const uint16_t* opr16;   // simt: right operand base (gram: X, poly: A, update: X)
 };

@@ -111,9 +111,9 @@ __global__ void __launch_bounds__(256) k_rowsq_simt(const __grid_constant__ Gemm
         const float v = h2f(o[j]);  // O is fp16
         s = fmaf(v, v, s);
     }
-    float* out = G.rowsq + (((int64_t)idx * G.m + row) * G.ntile_n + t) * 2;  // (row, tile, half) layout
-    out[0] = s;
-    out[1] = 0.f;
+    float* out = G.rowsq + (int64_t)idx * G.ntile_n * 2 * G.m;  // [tile, half][row] layout
+    out[(int64_t)(t * 2) * G.m + row] = s;
+    out[(int64_t)(t * 2 + 1) * G.m + row] = 0.f;
 }
 
 template <int MODE>

@@ -546,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             }
             if (MODE == MODE_UPDATE && p.want_rowsq) {
                 const int row = ti * kBM + (int)r;
-                if (row < G.m) G.rowsq[(((int64_t)idx * G.m + row) * G.ntile_n + tj) * 2 + half] = sumsq;
+                if (row < G.m)  // part-major: [matrix][256-column tile, half][row]
+                    G.rowsq[((int64_t)idx * G.ntile_n * 2 + tj * 2 + half) * G.m + row] = sumsq;
             }
             tc_fence_before();
             __syncwarp();

@@ -356,7 +356,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             }
             if (p.want_rowsq) {
                 const int row = row0 + lane;
-                if (row < G.m) G.rowsq[(((int64_t)idx * G.m + row) * G.ntile_n + tj) * 2 + half] = sumsq;
+                if (row < G.m)  // part-major: [matrix][256-column tile, half][row]
+                    G.rowsq[((int64_t)idx * G.ntile_n * 2 + tj * 2 + half) * G.m + row] = sumsq;
             }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
