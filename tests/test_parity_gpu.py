@@ -393,8 +393,8 @@ def _guarded(rows, cols, ld, dtype, sentinel, guard_rows=8):
     return buf, view, mask
 
 
-@pytest.mark.parametrize("pad", [8, 3])
-def test_strided_caller_buffers_with_guard_bands(pad):
+@pytest.mark.parametrize("pad,grad_dtype", [(8, "bf16"), (3, "bf16"), (8, "f32"), (3, "f32")])
+def test_strided_caller_buffers_with_guard_bands(pad, grad_dtype):
     """Parameters and gradients as row-strided views (ld = cols + pad) inside sentinel-filled
     buffers: parity with the oracle, and not one sentinel changed.  pad = 8 keeps the 8-wide
     vector path where cols allows it; pad = 3 forces the scalar path everywhere.  A bank split
@@ -402,12 +402,13 @@ def test_strided_caller_buffers_with_guard_bands(pad):
     shapes = [Shape(96, 200), Shape(200, 96), Shape(130, 300), Shape(64, 512, split=4, split_mode="columns"),
               Shape(256, 512)]
     lds = [s.cols + pad for s in shapes]
-    params, grads = _inputs(shapes, 2, seed=51)
+    params, grads = _inputs(shapes, 2, seed=51, grad_dtype=grad_dtype)
     p_sent, g_sent = 12345.0, -777.0
+    gdt = torch.bfloat16 if grad_dtype == "bf16" else torch.float32
     p_bufs, p_views, p_masks = zip(*[_guarded(s.rows, s.cols, ld, torch.float32, p_sent) for s, ld in zip(shapes, lds)])
     for v, p0 in zip(p_views, params):
         v.copy_(p0.cuda())
-    g_store = [_guarded(s.rows, s.cols, ld, torch.bfloat16, g_sent) for s, ld in zip(shapes, lds)]
+    g_store = [_guarded(s.rows, s.cols, ld, gdt, g_sent) for s, ld in zip(shapes, lds)]
 
     def grads_gpu_fn(step, grads_cpu):
         out = []
@@ -416,9 +417,9 @@ def test_strided_caller_buffers_with_guard_bands(pad):
             out.append(view)
         return out
 
-    opt = make_optimizer(shapes, ld=lds, lr=0.03, weight_decay=0.01)
+    opt = make_optimizer(shapes, ld=lds, lr=0.03, weight_decay=0.01, grad_dtype=grad_dtype)
     errs, _, _ = run_parity(shapes, params, grads, lr=0.03, weight_decay=0.01, opt=opt, params_gpu=list(p_views),
-                            grads_gpu_fn=grads_gpu_fn)
+                            grads_gpu_fn=grads_gpu_fn, grad_dtype=grad_dtype)
     errs.assert_within()
     torch.cuda.synchronize()
     for buf, mask in zip(p_bufs, p_masks):
@@ -429,14 +430,15 @@ def test_strided_caller_buffers_with_guard_bands(pad):
 
 # ----------------------------------------------------------------- NorMuon lanes
 
-@pytest.mark.parametrize("lanes", ["rows", "cols"])
-def test_normuon_lane_axis_flag(lanes):
+@pytest.mark.parametrize("lanes,engine", [("rows", "tcgen05"), ("cols", "tcgen05"), ("cols", "simt")])
+def test_normuon_lane_axis_flag(lanes, engine):
     """One second-moment entry per row (or per column) of every matrix as stored, instead of
-    per row of the short side: tall, wide and square matrices on both kernel families."""
+    per row of the short side: tall, wide and square matrices on both tensor-core kernel families,
+    and on the CUDA-core cross-check engine."""
     shapes = [Shape(128, 384), Shape(384, 128), Shape(192, 192), Shape(256, 512), Shape(512, 256),
               Shape(256, 1024, split=4)]
     params, grads = _inputs(shapes, 3, seed=61)
-    errs, opt, _ = run_parity(shapes, params, grads, lr=0.03, normuon_lanes=lanes)
+    errs, opt, _ = run_parity(shapes, params, grads, lr=0.03, normuon_lanes=lanes, gemm_engine=engine)
     errs.assert_within()
     for k in range(opt.num_matrices()):
         info = opt.matrix_info(k)
