@@ -89,6 +89,10 @@ struct Group {
 };
 
 struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
+    // Every tile list below is followed by the same tiles with the matrix order reversed
+    // within each cost class (at offset off + n): successive GEMM launches alternate
+    // between the two orders, so that each starts on the matrices its predecessor wrote
+    // last, which are the ones most likely still in L2.
     int32_t ng = 0;
     int32_t gi[kMaxGroupsPerLaunch] = {};  // the chunk's groups (indices into muon_s::groups)
     int32_t gram_off = 0, gram_n = 0;
@@ -552,6 +556,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             o = (int32_t)gemm_tiles.size();
             for (auto& x : v) gemm_tiles.push_back(x.t);
             n = (int32_t)v.size();
+            for (size_t i = 0; i < v.size();) {  // the reversed copy, cost classes kept in order
+                size_t j = i;
+                while (j < v.size() && v[j].cost == v[i].cost) ++j;
+                for (size_t k = j; k > i; --k) gemm_tiles.push_back(v[k - 1].t);
+                i = j;
+            }
         };
         std::vector<T> gram, poly, upd;
         for (int sl = 0; sl < ch.ng; ++sl) {
@@ -760,28 +770,29 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 gp.f16 = it > 0;
                 gp.want_rowsq = last && cfg.normuon;
                 gp.status = h->status;
+                // launches alternate between each list and its reversed copy (Gram, polynomial
+                // and update are three launches per iteration, so the order flips every launch)
+                const bool rev = ((3 * it + mode) & 1) != 0;
+                auto pick = [&](int32_t off, int32_t n) {
+                    gp.tiles = h->d_gemm_tiles + off + (rev ? n : 0);
+                    gp.ntiles = n;
+                };
                 if (mode == MODE_GRAM && ch.spg_n > 0) {
-                    gp.tiles = h->d_gemm_tiles + ch.spg_off;
-                    gp.ntiles = ch.spg_n;
+                    pick(ch.spg_off, ch.spg_n);
                     gp.pair = 1;
                 } else if (mode == MODE_GRAM) {
-                    gp.tiles = h->d_gemm_tiles + ch.gram_off;
-                    gp.ntiles = ch.gram_n;
+                    pick(ch.gram_off, ch.gram_n);
                 } else if (mode == MODE_POLY && ch.spg_n > 0) {
                     // the polynomial on SM pairs: the same 256 x 256 tiles (J >= I) as the Gram
-                    gp.tiles = h->d_gemm_tiles + ch.spg_off;
-                    gp.ntiles = ch.spg_n;
+                    pick(ch.spg_off, ch.spg_n);
                     gp.pair = 1;
                 } else if (mode == MODE_POLY) {
-                    gp.tiles = h->d_gemm_tiles + ch.poly_off;
-                    gp.ntiles = ch.poly_n;
+                    pick(ch.poly_off, ch.poly_n);
                 } else if (ch.pair_n > 0) {
-                    gp.tiles = h->d_gemm_tiles + ch.pair_off;
-                    gp.ntiles = ch.pair_n;
+                    pick(ch.pair_off, ch.pair_n);
                     gp.pair = 1;
                 } else {
-                    gp.tiles = h->d_gemm_tiles + ch.upd_off;
-                    gp.ntiles = ch.upd_n;
+                    pick(ch.upd_off, ch.upd_n);
                 }
                 for (int sl = 0; sl < ch.ng; ++sl) {
                     const Group& g = h->groups[ch.gi[sl]];

@@ -188,8 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) issued[s] = false;
             bool ok = true;
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = blockIdx.x < p.ntiles ? p.tiles[blockIdx.x] : make_int4(0, 0, 0, 0);
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + gridDim.x < p.ntiles) tile_nx = p.tiles[t + gridDim.x];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 const int K = (MODE == MODE_GRAM) ? p.grp[g].n : p.grp[g].m;
                 const int nkb = (K + kBK - 1) / kBK;
@@ -249,8 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
             if (p.debug_stall) ok = mbar_wait(mma_done, 0u, abort_flag, p.status);
             const uint32_t a_base = smem_u32(sA);
             const uint32_t b_base = smem_u32(sB);
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = blockIdx.x < p.ntiles ? p.tiles[blockIdx.x] : make_int4(0, 0, 0, 0);
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + gridDim.x < p.ntiles) tile_nx = p.tiles[t + gridDim.x];
                 const int g = tile.x;
                 const int K = (MODE == MODE_GRAM) ? p.grp[g].n : p.grp[g].m;
                 const int nkb = (K + kBK - 1) / kBK;
@@ -313,8 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
 #pragma unroll
             for (int s = 0; s < C::ISLOTS; ++s) issued[s] = false;
             bool ok = true;
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = blockIdx.x < p.ntiles ? p.tiles[blockIdx.x] : make_int4(0, 0, 0, 0);
             for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + gridDim.x < p.ntiles) tile_nx = p.tiles[t + gridDim.x];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 for (int c = 0; c < C::NCHUNK; ++c) {
                     if (C::SYM && !sym_chunk_live(ti, tj, c)) continue;
@@ -367,8 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
         // threads always meet at the same named barriers.  Each thread waits on the
         // mbarriers itself; the one barrier per chunk orders the staging writes before
         // the store thread's bulk stores.
+        // the tile list is read one tile ahead: no role waits on global memory between tiles
+        int4 tile_nx = blockIdx.x < p.ntiles ? p.tiles[blockIdx.x] : make_int4(0, 0, 0, 0);
         for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-            const int4 tile = p.tiles[t];
+            const int4 tile = tile_nx;
+            if (t + gridDim.x < p.ntiles) tile_nx = p.tiles[t + gridDim.x];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);

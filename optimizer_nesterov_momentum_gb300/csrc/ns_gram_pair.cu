@@ -14,9 +14,8 @@
 // (the left operand's half, K-major) and the right operand's half: for the
 // Gram, rows 256 J + 128 r .. + 127 of X (K-major); for the polynomial,
 // columns 256 J + 128 r .. + 127 of A (MN-major: A is symmetric, so its
-// columns are its rows, and the tensor cores take an MN-major right operand
-// at full rate where two K-major operands of a short K ran the MMAs at about
-// half rate).  An off-diagonal tile stages 32 KB per SM per 64-deep k-block;
+// columns are its rows; the tensor cores read either layout at the same
+// rate).  An off-diagonal tile stages 32 KB per SM per 64-deep k-block;
 // a diagonal Gram tile, whose two halves are the same rows, 16 KB.  CTA r's
 // TMEM receives rows 128 r .. + 127 of the tile.
 //
@@ -141,8 +140,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = pr < p.ntiles ? p.tiles[pr] : make_int4(0, 0, 0, 0);
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 const int K = C::POLY ? p.grp[g].m : p.grp[g].n;
                 const int nkb = (K + kBK - 1) / kBK;
@@ -181,8 +183,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true, any = false;
             const uint32_t s_base = smem_u32(sS);
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = pr < p.ntiles ? p.tiles[pr] : make_int4(0, 0, 0, 0);
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int K = C::POLY ? p.grp[tile.x].m : p.grp[tile.x].n;
                 const int nkb = (K + kBK - 1) / kBK;
                 const bool diag = !C::POLY && tile.z == tile.w;
@@ -192,26 +197,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tbase + (uint32_t)(acc * 256);
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                // Stages are taken two at a time: both waits first, then eight MMAs back to
+                // back.  A wait between every four MMAs leaves the tensor pipe idle for part of
+                // each k-block; eight in a row keep it busy.
+                for (int kb = 0; kb < nkb; kb += 2) {
+                    const int nst = kb + 1 < nkb ? 2 : 1;
+                    int st1 = stage + 1;
+                    uint32_t ph1 = phase;
+                    if (st1 == STAGES) {
+                        st1 = 0;
+                        ph1 ^= 1u;
+                    }
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
+                        (nst == 2 && !mbar_wait(&full[st1], ph1, abort_flag, p.status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_st = s_base + stage * kSymStage;
-                    const uint32_t b_st = diag ? a_st : a_st + kSymRows;  // a diagonal tile's halves are the same rows
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t adesc = make_sdesc_sw128(a_st + kk * 32, 16, 1024);
-                        // K-major right operand: 32 bytes further per 16-deep step; MN-major
-                        // (polynomial): 16 rows of 128 bytes further, 8 KB between 64-column boxes
-                        const uint64_t bdesc = C::POLY ? make_sdesc_sw128(b_st + kk * (16 * 128), 64 * kBK * 2, 1024)
-                                                       : make_sdesc_sw128(b_st + kk * 32, 16, 1024);
-                        umma_f16_pair(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                        any = true;
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < nst) {
+                            const int st = h ? st1 : stage;
+                            const uint32_t a_st = s_base + st * kSymStage;
+                            const uint32_t b_st = diag ? a_st : a_st + kSymRows;  // a diagonal tile's halves are the same rows
+                            // the stage's descriptors; a 16-deep step adds to the start-address field
+                            // (16-byte units): 32 bytes along a K-major operand, 16 rows of 128 bytes
+                            // along the MN-major one (polynomial; 8 KB between its 64-column boxes)
+                            const uint64_t ad = make_sdesc_sw128(a_st, 16, 1024);
+                            const uint64_t bd = C::POLY ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
+                                                        : make_sdesc_sw128(b_st, 16, 1024);
+                            constexpr uint64_t b_step = C::POLY ? 128 : 2;
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                umma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + b_step * (uint64_t)kk, IDESC,
+                                              (kb | h | kk) != 0 ? 1u : 0u);
+                            any = true;
+                            umma_commit_pair(&empty[st]);
+                        }
                     }
-                    umma_commit_pair(&empty[stage]);
-                    if (++stage == STAGES) {
+                    stage = st1;
+                    phase = ph1;
+                    if (nst == 2 && ++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -244,8 +270,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
         bool in_pending[2] = {false, false};
         if (C::POLY && lane == 0)
             for (int g = 0; g < p.ngroups; ++g) tma_prefetch_desc(&p.map_ein[g]);
+        // the tile list is read one tile ahead: no role waits on global memory between tiles
+        int4 tile_nx = pr < p.ntiles ? p.tiles[pr] : make_int4(0, 0, 0, 0);
         for (int t = pr; run && t < p.ntiles; t += npairs) {
-            const int4 tile = p.tiles[t];
+            const int4 tile = tile_nx;
+            if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             const bool diag = ti == tj;

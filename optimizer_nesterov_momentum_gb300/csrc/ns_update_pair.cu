@@ -145,8 +145,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = pair < p.ntiles ? p.tiles[pair] : make_int4(0, 0, 0, 0);
             for (int t = pair; t < p.ntiles && ok; t += npairs) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 const int nkb = (p.grp[g].m + kBK - 1) / kBK;
                 const int row0 = ti * 2 * kBM + (int)rank * kBM;
@@ -179,30 +182,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             bool ok = true;
             const uint32_t a_base = smem_u32(sA);
             const uint32_t b_base = smem_u32(sB);
+            // the tile list is read one tile ahead: no role waits on global memory between tiles
+            int4 tile_nx = pair < p.ntiles ? p.tiles[pair] : make_int4(0, 0, 0, 0);
             for (int t = pair; t < p.ntiles && ok; t += npairs) {
-                const int4 tile = p.tiles[t];
+                const int4 tile = tile_nx;
+                if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int nkb = (p.grp[tile.x].m + kBK - 1) / kBK;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                // Stages are taken two at a time: both waits first, then eight MMAs back to
+                // back.  A wait between every four MMAs leaves the tensor pipe idle for part of
+                // each k-block; eight in a row keep it busy.
+                for (int kb = 0; kb < nkb; kb += 2) {
+                    const int nst = kb + 1 < nkb ? 2 : 1;
+                    int st1 = stage + 1;
+                    uint32_t ph1 = phase;
+                    if (st1 == kPairStages) {
+                        st1 = 0;
+                        ph1 ^= 1u;
+                    }
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
+                        (nst == 2 && !mbar_wait(&full[st1], ph1, abort_flag, p.status))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t adesc = make_sdesc_sw128(a_base + stage * kPairA + kk * 32, 16, 1024);
-                        const uint64_t bdesc =
-                            make_sdesc_sw128(b_base + stage * kPairB + kk * (16 * 128), 64 * kBK * 2, 1024);
-                        umma_f16_pair(tacc[acc], adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
-                        mma_any = true;
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < nst) {
+                            const int st = h ? st1 : stage;
+                            // the stage's descriptors; a 16-deep step adds to the start-address field
+                            // (16-byte units): 32 bytes along K-major A, 16 rows of 128 bytes along
+                            // MN-major B
+                            const uint64_t ad = make_sdesc_sw128(a_base + st * kPairA, 16, 1024);
+                            const uint64_t bd = make_sdesc_sw128(b_base + st * kPairB, 64 * kBK * 2, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                umma_f16_pair(tacc[acc], ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128),
+                                              C::IDESC, (kb | h | kk) != 0 ? 1u : 0u);
+                            mma_any = true;
+                            umma_commit_pair(&empty[st]);
+                        }
                     }
-                    umma_commit_pair(&empty[stage]);
-                    if (++stage == kPairStages) {
+                    stage = st1;
+                    phase = ph1;
+                    if (nst == 2 && ++stage == kPairStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -241,8 +268,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 tma_prefetch_desc(&p.map_ein[g]);
                 tma_prefetch_desc(&p.map_ein2[g]);
             }
+        // the tile list is read one tile ahead: no role waits on global memory between tiles
+        int4 tile_nx = pair < p.ntiles ? p.tiles[pair] : make_int4(0, 0, 0, 0);
         for (int t = pair; run && t < p.ntiles; t += npairs) {
-            const int4 tile = p.tiles[t];
+            const int4 tile = tile_nx;
+            if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
             const int row0 = ti * 2 * kBM + (int)rank * kBM + quad * 32;  // this warp's first row
