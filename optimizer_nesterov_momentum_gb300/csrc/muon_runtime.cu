@@ -79,6 +79,7 @@ struct Group {
     // TMA descriptors: bf16 operand boxes (64 x 128, 64 x 64), 32 x 128 boxes of
     // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
+    CUtensorMap map_x_mn128[2];  // X as MN-major boxes 128 rows deep (the SM-pair folded update's 128-deep k-blocks)
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_a_mn;      // 64 x 64 boxes of A: the MN-major right operand of the SM-pair polynomial
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
@@ -661,6 +662,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             ok = encode_bf16_3d(enc, &g.map_x_k[b], g.x16[b], g.n, g.m, g.count, g.ldx, kBM) &&
                  encode_bf16_3d(enc, &g.map_x_k256[b], g.x16[b], g.n, g.m, g.count, g.ldx, 2 * kBM) &&
                  encode_bf16_3d(enc, &g.map_x_mn[b], g.x16[b], g.n, g.m, g.count, g.ldx, 64) &&
+                 encode_bf16_3d(enc, &g.map_x_mn128[b], g.x16[b], g.n, g.m, g.count, g.ldx, 128) &&
                  encode_3d(enc, &g.map_x_o32[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
                            g.ldx, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
                  encode_3d(enc, &g.map_x_w32[b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.x16[b], g.n, g.m, g.count,
@@ -829,7 +831,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         G.opr16 = g.a16;
                     } else {
                         gp.map_a[sl] = g.map_p_k;
-                        gp.map_b[sl] = first ? g.map_u_mn : g.map_x_mn[in_buf];
+                        // the folded update on SM pairs takes 128-deep k-blocks (16 KB boxes of X)
+                        gp.map_b[sl] = first ? g.map_u_mn : (gp.pair ? g.map_x_mn128[in_buf] : g.map_x_mn[in_buf]);
                         // first update: u hi | lo in 32-column boxes, X1 out in 32-column boxes;
                         // later updates (a on the diagonal of P): no input, X' out in 64-column boxes
                         gp.map_ein[sl] = gp.pair ? g.map_u_hi_w32 : g.map_u_hi;

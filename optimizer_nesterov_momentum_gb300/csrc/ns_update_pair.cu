@@ -9,9 +9,9 @@
 // columns 128 r .. 128 r + 127 of its right operand (X rows, MN-major), and its
 // own TMEM receives its 128 rows of the product.  The MMA, issued by CTA 0
 // (M = 256, N = 256, K = 16), reads both CTAs' shared memory.  Each SM thus
-// stages 32 KB per 64-deep k-block for the same 4.2 MFLOP that a one-SM
-// 128 x 256 tile stages 48 KB for: the update's mainloop is bound by how fast
-// shared memory fills, so this is 1.5x the math per staged byte.
+// stages 32 KB per 64 of depth for the same 4.2 MFLOP that a one-SM 128 x 256
+// tile stages 48 KB for: the update's mainloop is bound by how fast shared
+// memory fills, so this is 1.5x the math per staged byte.
 //
 // Warp roles (320 threads per CTA, one CTA per SM):
 //   warp 0     TMA producer (both CTAs): loads its own halves into its own
@@ -41,9 +41,6 @@ namespace muon {
 namespace {
 
 constexpr int kPairThreads = 320;
-constexpr int kPairA = kBM * kBK * 2;    // 16 KB: this CTA's 128 rows of P'
-constexpr int kPairB = 128 * kBK * 2;    // 16 KB: this CTA's 128 columns of X (two 64-column blocks)
-constexpr int kPairStage = kPairA + kPairB;
 constexpr int kWarpSlot = 32 * 32 * 2;   // one warp's 32 x 32 16-bit block (64-byte rows, 64-byte swizzle)
 constexpr int kWarpSlots = 2;            // output staging slots per epilogue warp
 constexpr int kPairEpiWarps = 8;
@@ -54,11 +51,22 @@ constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
 // hi + lo pair: bf16 operands, and each warp reads its 32 x 32 blocks of u's hi and
 // lo halves for the a u term (two chunks ahead, by TMA).  Otherwise the folded
 // fp16 update, which reads nothing.
+//
+// A stage holds one BK-deep k-block: this CTA's 128 rows of P' as BK / 64 K-major
+// boxes of 128 x 64, and its 128 columns of X as two MN-major boxes of BK x 64.  The
+// folded update takes 128-deep k-blocks: every copy is then a 16 KB box, which the
+// copy engine moves faster per byte than the 8 KB boxes of 64-deep ones.  The first
+// iteration keeps 64-deep k-blocks, because its epilogue input ring leaves room for
+// only 128 KB of stages.
 template <bool HILO>
 struct UpdPairCfg {
-    static constexpr int STAGES = HILO ? 4 : 6;
+    static constexpr int BK = HILO ? 64 : 128;
+    static constexpr int A_BYTES = kBM * BK * 2;
+    static constexpr int B_BYTES = 128 * BK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = HILO ? 4 : 3;
     static constexpr int IN_WARP = HILO ? 2 * 2 * kWarpSlot : 0;  // two chunks in flight, hi and lo
-    static constexpr int SMEM = STAGES * kPairStage + kPairOutBytes + kPairEpiWarps * IN_WARP + 1024 + 512;
+    static constexpr int SMEM = STAGES * STAGE + kPairOutBytes + kPairEpiWarps * IN_WARP + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory budget");
     static constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/true, /*fp16=*/!HILO);
 };
@@ -72,11 +80,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     k_ns_update_pair(const __grid_constant__ GemmParams p) {
     using C = UpdPairCfg<HILO>;
     constexpr int kPairStages = C::STAGES;
+    constexpr int BK = C::BK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = sA + kPairStages * kPairA;
-    uint8_t* sO = sB + kPairStages * kPairB;
+    uint8_t* sB = sA + kPairStages * C::A_BYTES;
+    uint8_t* sO = sB + kPairStages * C::B_BYTES;
     uint8_t* sI = sO + kPairOutBytes;  // HILO: per warp two chunks of (hi | lo) blocks
     uint64_t* full = reinterpret_cast<uint64_t*>(sI + kPairEpiWarps * C::IN_WARP);  // CTA 0's are used
     uint64_t* empty = full + kPairStages;
@@ -151,7 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
-                const int nkb = (p.grp[g].m + kBK - 1) / kBK;
+                const int nkb = (p.grp[g].m + BK - 1) / BK;
                 const int row0 = ti * 2 * kBM + (int)rank * kBM;
                 const int col0 = tj * 256 + (int)rank * 128;
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -159,11 +168,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPairStage);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE);
                     const uint32_t bar = full0 + (uint32_t)(stage * 8);
-                    tma_load_3d_pair(sA + stage * kPairA, &p.map_a[g], bar, kb * kBK, row0, idx);
-                    tma_load_3d_pair(sB + stage * kPairB, &p.map_b[g], bar, col0, kb * kBK, idx);
-                    tma_load_3d_pair(sB + stage * kPairB + 64 * kBK * 2, &p.map_b[g], bar, col0 + 64, kb * kBK, idx);
+#pragma unroll
+                    for (int ks = 0; ks < BK / 64; ++ks)
+                        tma_load_3d_pair(sA + stage * C::A_BYTES + ks * (kBM * 128), &p.map_a[g], bar, kb * BK + ks * 64,
+                                         row0, idx);
+                    tma_load_3d_pair(sB + stage * C::B_BYTES, &p.map_b[g], bar, col0, kb * BK, idx);
+                    tma_load_3d_pair(sB + stage * C::B_BYTES + BK * 128, &p.map_b[g], bar, col0 + 64, kb * BK, idx);
                     if (++stage == kPairStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -187,49 +199,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             for (int t = pair; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
-                const int nkb = (p.grp[tile.x].m + kBK - 1) / kBK;
+                const int nkb = (p.grp[tile.x].m + BK - 1) / BK;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                // Stages are taken two at a time: both waits first, then eight MMAs back to
-                // back.  A wait between every four MMAs leaves the tensor pipe idle for part of
-                // each k-block; eight in a row keep it busy.
-                for (int kb = 0; kb < nkb; kb += 2) {
-                    const int nst = kb + 1 < nkb ? 2 : 1;
-                    int st1 = stage + 1;
-                    uint32_t ph1 = phase;
-                    if (st1 == kPairStages) {
-                        st1 = 0;
-                        ph1 ^= 1u;
-                    }
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
-                        (nst == 2 && !mbar_wait(&full[st1], ph1, abort_flag, p.status))) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // the stage's descriptors; a 16-deep step adds to the start-address field
+                    // (16-byte units): 32 bytes along a 64-wide K-major box of A (16 KB to the
+                    // next box), 16 rows of 128 bytes along MN-major B (BK rows per 64-column box)
+                    const uint64_t ad = make_sdesc_sw128(a_base + stage * C::A_BYTES, 16, 1024);
+                    const uint64_t bd = make_sdesc_sw128(b_base + stage * C::B_BYTES, BK * 128, 1024);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h < nst) {
-                            const int st = h ? st1 : stage;
-                            // the stage's descriptors; a 16-deep step adds to the start-address field
-                            // (16-byte units): 32 bytes along K-major A, 16 rows of 128 bytes along
-                            // MN-major B
-                            const uint64_t ad = make_sdesc_sw128(a_base + st * kPairA, 16, 1024);
-                            const uint64_t bd = make_sdesc_sw128(b_base + st * kPairB, 64 * kBK * 2, 1024);
-#pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk)
-                                umma_f16_pair(tacc[acc], ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128),
-                                              C::IDESC, (kb | h | kk) != 0 ? 1u : 0u);
-                            mma_any = true;
-                            umma_commit_pair(&empty[st]);
-                        }
-                    }
-                    stage = st1;
-                    phase = ph1;
-                    if (nst == 2 && ++stage == kPairStages) {
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_f16_pair(tacc[acc], ad + (uint64_t)((kk >> 2) * (kBM * 128 / 16) + (kk & 3) * 2),
+                                      bd + (uint64_t)(kk * 128), C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    mma_any = true;
+                    umma_commit_pair(&empty[stage]);
+                    if (++stage == kPairStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
