@@ -94,6 +94,21 @@ typedef enum { MUON_GRAD_BF16 = 0, MUON_GRAD_F32 = 1 } muon_grad_dtype;
 #define MUON_LANES_ROWS 1        /* one lane per row of the matrix as stored (mean over its columns) */
 #define MUON_LANES_COLS 2        /* one lane per column of the matrix as stored (mean over its rows) */
 
+/* Order of the Newton-Schulz work (muon_config.ns_form).  The iteration of the
+ * "modded-nanogpt 50B-token" write-up (section "Muon from the source") is
+ * X <- a X + (b A + c A^2) X with A = X X^T.  STANDARD computes exactly that every
+ * iteration.  GRAM_PAIRS gives the same result in exact arithmetic for matrices whose
+ * sides tile by 256 with n >= 2m: after the first iteration it takes iterations two
+ * at a time, forming A_k = X_k X_k^T once, the pair's second Gram matrix as
+ * A_{k+1} = (A_k P_k) P_k with P_k = a I + b A_k + c A_k^2, and the pair's output as
+ * X_{k+2} = (P_{k+1} P_k) X_k: one m x n Gram matrix and one update per pair instead
+ * of two of each, for three m x m products.  A single iteration left at the end, and
+ * every other matrix, runs in the standard form.  Rounding differs from STANDARD at
+ * the level of the 16-bit operands; every pair restarts from a freshly formed Gram
+ * matrix, which keeps the error at the standard form's level. */
+#define MUON_NS_STANDARD 0
+#define MUON_NS_GRAM_PAIRS 1
+
 #define MUON_MAX_MATRICES 1024   /* parameter matrices per handle */
 #define MUON_MAX_NS_STEPS 16
 
@@ -127,11 +142,13 @@ typedef struct {
     const float* ns_coeffs;/* host array [ns_steps * 3] of (a, b, c) per iteration, or NULL
                               for (3.4445, -4.7750, 2.0315) every iteration; copied */
     int32_t normuon_lanes; /* MUON_LANES_*: the second moment's lanes (NorMuon only) */
+    int32_t ns_form;       /* MUON_NS_*: order of the Newton-Schulz products */
 } muon_config;
 
 /* Fills *cfg with: lr 0.02, momentum 0.95, beta2 0.95, weight_decay 0, ns_steps 5,
  * nesterov 1, lerp_form 1, normuon 1, norm_preserve 1, grad_dtype BF16,
- * gemm_engine TCGEN05, NULL arrays, normuon_lanes MUON_LANES_SHORT_SIDE. */
+ * gemm_engine TCGEN05, NULL arrays, normuon_lanes MUON_LANES_SHORT_SIDE,
+ * ns_form MUON_NS_GRAM_PAIRS.  Layout: 80 bytes, ns_form at offset 76. */
 void muon_config_default(muon_config* cfg);
 
 /* Builds the execution plan for `n_mats` matrices on CUDA device `device`:
@@ -227,9 +244,18 @@ int muon_workspace_bytes(muon_handle h, int64_t* out);
 /* Number of kernel launches one muon_step enqueues. */
 int muon_launch_count(muon_handle h, int32_t* out);
 
+/* The work one muon_step does per stage, as planned at create time: flops[k]
+ * the algorithmic flops of stage k (symmetric products counted once per
+ * element of their upper triangle: m(m+1)n for a Gram matrix, m^2(m+1) for an
+ * m x m product; 2 m^2 n for an update), bytes[k] its algorithmic DRAM bytes
+ * (each operand read once, each result written once, at its stored width),
+ * launches[k] its kernel launches.  Host arrays of MUON_NUM_STAGES entries;
+ * any of them may be NULL. */
+int muon_stage_work(muon_handle h, int64_t* flops, int64_t* bytes, int32_t* launches);
+
 /* ---- stage timing (benchmarks) -------------------------------------------- */
 
-/* Stages of one step, in launch order. */
+/* Stages of one step. */
 #define MUON_STAGE_MOMENTUM 0    /* S1-S3 + norm partials (k_momentum) */
 #define MUON_STAGE_NORM 1        /* S4 scale per matrix (k_norm_scale) */
 #define MUON_STAGE_GRAM 2        /* S5, all iterations summed */
@@ -237,7 +263,8 @@ int muon_launch_count(muon_handle h, int32_t* out);
 #define MUON_STAGE_UPDATE 4      /* S7, all iterations summed */
 #define MUON_STAGE_LANE 5        /* S8 + S9 factors (k_lane_stats) */
 #define MUON_STAGE_APPLY 6       /* S10 (k_apply) */
-#define MUON_NUM_STAGES 7
+#define MUON_STAGE_PRODUCT 7     /* the m x m products of Gram pairs (MUON_NS_GRAM_PAIRS) */
+#define MUON_NUM_STAGES 8
 
 /* enable != 0: every later muon_step records CUDA events around each launch
  * on its stream (creates the events on first use; no device allocation). */

@@ -22,6 +22,8 @@ from ._abi import (  # noqa: F401  (re-exported names of the C ABI)
     MUON_LANES_COLS,
     MUON_LANES_ROWS,
     MUON_LANES_SHORT_SIDE,
+    MUON_NS_GRAM_PAIRS,
+    MUON_NS_STANDARD,
     MUON_SPLIT_COLUMNS,
     MUON_SPLIT_CONTIGUOUS,
     MUON_STATE_DIRECTION,
@@ -66,14 +68,17 @@ class Muon:
     "bf16" or "f32"; ``gemm_engine`` is "tcgen05" (the product path) or
     "simt" (a slow cross-check engine for debugging); ``normuon_lanes`` is
     "short_side" (default: one second-moment entry per row of the short side),
-    "rows" or "cols" (per row / per column of each matrix as stored).
+    "rows" or "cols" (per row / per column of each matrix as stored);
+    ``ns_form`` is "gram_pairs" (default: wide matrices take the Newton-Schulz
+    iterations after the first two at a time in Gram space) or "standard" (every
+    iteration as the write-ups order it; see MUON_NS_* in include/muon.h).
     """
 
     def __init__(self, specs: Sequence, *, lr: float = 0.02, momentum: float = 0.95, beta2: float = 0.95,
                  weight_decay: float = 0.0, ns_steps: int = 5, nesterov: bool = True, lerp_form: bool = True,
                  normuon: bool = True, norm_preserve: bool = True, grad_dtype: str = "bf16",
                  gemm_engine: str = "tcgen05", ns_coeffs: Optional[Sequence[Sequence[float]]] = None,
-                 normuon_lanes: str = "short_side", device: Optional[int] = None):
+                 normuon_lanes: str = "short_side", ns_form: str = "gram_pairs", device: Optional[int] = None):
         import torch
 
         self.specs = [s if isinstance(s, MatrixSpec) else MatrixSpec(*s) for s in specs]
@@ -90,6 +95,7 @@ class Muon:
         cfg.gemm_engine = {"tcgen05": MUON_GEMM_TCGEN05, "simt": MUON_GEMM_SIMT}[gemm_engine]
         cfg.normuon_lanes = {"short_side": MUON_LANES_SHORT_SIDE, "rows": MUON_LANES_ROWS,
                              "cols": MUON_LANES_COLS}[normuon_lanes]
+        cfg.ns_form = {"standard": MUON_NS_STANDARD, "gram_pairs": MUON_NS_GRAM_PAIRS}[ns_form]
         n = len(self.specs)
         self._lr_mul = (ctypes.c_float * n)(*[s.lr_mul for s in self.specs])
         self._wd_mul = (ctypes.c_float * n)(*[s.wd_mul for s in self.specs])
@@ -186,6 +192,10 @@ class Muon:
 
     def set_profiling(self, enable: bool) -> None:
         _abi.muon_set_profiling(self.handle, enable)
+
+    def stage_work(self) -> dict:
+        """Per stage: (algorithmic flops, algorithmic DRAM bytes, launches) of one step."""
+        return _abi.muon_stage_work(self.handle)
 
     def stage_times(self) -> dict:
         """Device ms per stage of the most recent profiled step."""

@@ -34,6 +34,8 @@ MUON_GEMM_SIMT = 1
 MUON_LANES_SHORT_SIDE = 0
 MUON_LANES_ROWS = 1
 MUON_LANES_COLS = 2
+MUON_NS_STANDARD = 0
+MUON_NS_GRAM_PAIRS = 1
 MUON_MAX_MATRICES = 1024
 MUON_MAX_NS_STEPS = 16
 
@@ -42,7 +44,7 @@ MUON_STATE_SECOND_MOMENT = 1
 MUON_STATE_ORTHO = 2
 MUON_STATE_DIRECTION = 3
 
-MUON_STAGE_NAMES = ("momentum", "norm_scale", "gram", "poly", "update", "lane_stats", "apply")
+MUON_STAGE_NAMES = ("momentum", "norm_scale", "gram", "poly", "update", "lane_stats", "apply", "product")
 MUON_NUM_STAGES = len(MUON_STAGE_NAMES)
 
 # Every entry point declared in include/muon.h.
@@ -62,6 +64,7 @@ EXPORTED = (
     "muon_matrix_info",
     "muon_workspace_bytes",
     "muon_launch_count",
+    "muon_stage_work",
     "muon_set_profiling",
     "muon_get_stage_times",
     "muon_get_state",
@@ -130,6 +133,7 @@ class muon_config(ctypes.Structure):
         ("wd_mul", POINTER(c_float)),
         ("ns_coeffs", POINTER(c_float)),
         ("normuon_lanes", c_int32),
+        ("ns_form", c_int32),
     ]
 
 
@@ -168,6 +172,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.muon_matrix_info.argtypes = [c_void_p, c_int32, POINTER(c_int64)]
     lib.muon_workspace_bytes.argtypes = [c_void_p, POINTER(c_int64)]
     lib.muon_launch_count.argtypes = [c_void_p, POINTER(c_int32)]
+    lib.muon_stage_work.argtypes = [c_void_p, POINTER(c_int64), POINTER(c_int64), POINTER(c_int32)]
     lib.muon_set_schedule.argtypes = [c_void_p, POINTER(muon_schedule), c_int64, c_void_p]
     lib.muon_get_step.argtypes = [c_void_p, POINTER(c_int64), c_void_p]
     lib.muon_adam_config_default.argtypes = [POINTER(muon_adam_config)]
@@ -287,6 +292,15 @@ def muon_launch_count(h) -> int:
     out = c_int32()
     _check(load_library().muon_launch_count(h, ctypes.byref(out)), h)
     return out.value
+
+
+def muon_stage_work(h):
+    """Per stage name: (algorithmic flops, algorithmic DRAM bytes, launches) of one step."""
+    fl = (c_int64 * MUON_NUM_STAGES)()
+    by = (c_int64 * MUON_NUM_STAGES)()
+    ln = (c_int32 * MUON_NUM_STAGES)()
+    _check(load_library().muon_stage_work(h, fl, by, ln), h)
+    return {name: (fl[k], by[k], ln[k]) for k, name in enumerate(MUON_STAGE_NAMES)}
 
 
 def muon_set_profiling(h, enable: bool) -> None:

@@ -71,6 +71,12 @@ struct Group {
     uint16_t* x16[2] = {nullptr, nullptr};
     uint16_t* a16 = nullptr;
     uint16_t* p16 = nullptr;
+    // Gram-pair iterations (muon_config.ns_form): the second polynomial of a pair and
+    // T = A P', whose buffer then holds Q = P'' P'
+    int32_t gs = 0;
+    int32_t final_buf = 0;  // the iterate buffer that ends up holding the last output
+    uint16_t* pb16 = nullptr;
+    uint16_t* t16 = nullptr;
     float* rowsq = nullptr;
     float* v = nullptr;
     float* lane = nullptr;
@@ -80,6 +86,9 @@ struct Group {
     // the iterate's hi and lo halves for the update epilogue, mirror boxes of A / P
     CUtensorMap map_u_k, map_u_mn, map_x_k[2], map_x_mn[2], map_a_k, map_p_k;
     CUtensorMap map_x_mn128[2];  // X as MN-major boxes 128 rows deep (the SM-pair folded update's 128-deep k-blocks)
+    // Gram-pair groups: P as the MN-major right operand of the plain products, the
+    // second polynomial and T (or Q) as 128-row K-major left operands, and their stores
+    CUtensorMap map_p_mn, map_pb_k, map_pb_w32, map_t_k, map_t_w32;
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_a_mn;      // 64 x 64 boxes of A: the MN-major right operand of the SM-pair polynomial
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
@@ -101,6 +110,21 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     int32_t upd_off = 0, upd_n = 0;
     int32_t pair_off = 0, pair_n = 0;  // 256 x 256 update tiles for SM pairs (0: chunk not eligible)
     int32_t spg_off = 0, spg_n = 0;    // 256 x 256 Gram tiles (J >= I) for SM pairs
+    // the same lists restricted to the groups that iterate in the standard form, and (symmetric
+    // tiles) to the Gram-pair groups
+    int32_t pair_std_off = 0, pair_std_n = 0;
+    int32_t spg_std_off = 0, spg_std_n = 0;
+    int32_t spg_gs_off = 0, spg_gs_n = 0;
+};
+
+// One Newton-Schulz launch of the step, in order.
+struct Launch {
+    int32_t stage;  // MUON_STAGE_*
+    int32_t mode;   // GemmMode
+    int32_t chunk;
+    int32_t it;     // Newton-Schulz iteration
+    int32_t pair;   // SM-pair kernels
+    int32_t f16;    // fp16 operands (iterations after the first)
 };
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -142,8 +166,13 @@ struct muon_s {
     int2* d_colwork = nullptr;
     int4* d_elem_tiles = nullptr;
     int4* d_gemm_tiles = nullptr;
-    // pre-built GEMM parameter blocks: [iteration][chunk][mode]
+    // the Newton-Schulz launches of one step and their pre-built parameter blocks
+    std::vector<Launch> plan;
     std::vector<GemmParams> gparams;
+    // algorithmic work of one step per stage (muon_stage_work)
+    int64_t work_flops[MUON_NUM_STAGES] = {};
+    int64_t work_bytes[MUON_NUM_STAGES] = {};
+    int32_t work_launches[MUON_NUM_STAGES] = {};
     std::string last_error;
     // profiling: one event before every launch plus one at the end
     bool profiling = false;
@@ -249,13 +278,47 @@ cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* gra
     return run_elem<1024>(h, params, grads, apply, s);
 }
 
+// What a group does in one Newton-Schulz iteration.  Standard form (the write-ups'
+// order of operations): A = X X^T, P' = a I + b A + c A^2 (the first iteration keeps a
+// out of P and adds a u in the update), X <- P' X.  Gram-pair groups run the first
+// iteration in the standard form and then take the rest two at a time in Gram space:
+// with A_k = X_k X_k^T and P'_k a polynomial in A_k, X_{k+1} = P'_k X_k gives
+// A_{k+1} = P'_k A_k P'_k = (A_k P'_k) P'_k and X_{k+2} = (P'_{k+1} P'_k) X_k, so a pair
+// of iterations forms one Gram matrix and one update instead of two of each, for three
+// m x m products.  A single iteration left at the end runs in the standard form.
+enum GroupOp { OP_NONE, OP_GRAM, OP_POLY, OP_POLY_B, OP_PLAIN_T, OP_PLAIN_A, OP_PLAIN_Q, OP_UPD, OP_UPD_Q };
+enum Phase { PH_GRAM, PH_POLY, PH_PLAIN1, PH_PLAIN2, PH_UPDATE, PH_COUNT };
+
+GroupOp group_op(const Group& g, int it, int steps, int phase) {
+    int kind = 0;  // 0: standard, 1: first of a Gram pair, 2: second of a pair
+    if (g.gs && it > 0) {
+        const int pos = (it - 1) % 2;
+        kind = pos == 1 ? 2 : (it + 1 < steps ? 1 : 0);
+    }
+    switch (phase) {
+        case PH_GRAM: return kind == 2 ? OP_NONE : OP_GRAM;
+        case PH_POLY: return kind == 2 ? OP_POLY_B : OP_POLY;
+        case PH_PLAIN1: return kind == 1 ? OP_PLAIN_T : (kind == 2 ? OP_PLAIN_Q : OP_NONE);
+        case PH_PLAIN2: return kind == 1 ? OP_PLAIN_A : OP_NONE;
+        default: return kind == 1 ? OP_NONE : (kind == 2 ? OP_UPD_Q : OP_UPD);
+    }
+}
+
+// The iterate buffer that holds the last output: the first iteration writes buffer 0
+// and every later update flips it.
+int final_buffer(const Group& g, int steps) {
+    int cur = 0;
+    for (int it = 1; it < steps; ++it)
+        if (group_op(g, it, steps, PH_UPDATE) != OP_NONE) cur ^= 1;
+    return cur;
+}
+
 int launches_per_step(const muon_s* h) {
     // k_momentum, k_norm_scale, k_lane_stats, k_apply + the Newton-Schulz products
     // (+ k_schedule_advance while a schedule is installed)
     const int sched = h->schedule_on ? 1 : 0;
     const int colsum = h->n_colwork > 0 ? 1 : 0;  // k_col_sumsq for column lanes
-    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05)
-        return sched + colsum + 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps;
+    if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) return sched + colsum + 4 + (int)h->plan.size();
     const int per_iter = 3 * (int)h->groups.size();
     const int rowsq = h->cfg.normuon ? (int)h->groups.size() : 0;  // extra pass after the last update
     return sched + colsum + 4 + per_iter * h->cfg.ns_steps + rowsq;
@@ -288,6 +351,7 @@ void muon_config_default(muon_config* cfg) {
     cfg->grad_dtype = MUON_GRAD_BF16;
     cfg->gemm_engine = MUON_GEMM_TCGEN05;
     cfg->normuon_lanes = MUON_LANES_SHORT_SIDE;
+    cfg->ns_form = MUON_NS_GRAM_PAIRS;
 }
 
 const char* muon_error_string(int code) {
@@ -334,6 +398,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     if (cfg.normuon_lanes != MUON_LANES_SHORT_SIDE && cfg.normuon_lanes != MUON_LANES_ROWS &&
         cfg.normuon_lanes != MUON_LANES_COLS)
         return fail(nullptr, MUON_ERR_ARG, "bad normuon_lanes");
+    if (cfg.ns_form != MUON_NS_STANDARD && cfg.ns_form != MUON_NS_GRAM_PAIRS)
+        return fail(nullptr, MUON_ERR_ARG, "bad ns_form");
 
     // ---- shapes -> split matrices (host-only validation first)
     struct Pending {
@@ -433,6 +499,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         }
         sub_group[k] = it->second;
     }
+    // wide groups that tile by 256 take their iterations in Gram pairs (n >= 2m: a pair then
+    // saves more than its three m x m products cost)
+    for (Group& g : h->groups)
+        g.gs = cfg.ns_form == MUON_NS_GRAM_PAIRS && cfg.gemm_engine == MUON_GEMM_TCGEN05 && cfg.ns_steps >= 3 &&
+               g.m % 256 == 0 && g.n % 256 == 0 && g.n >= 2 * g.m;
     std::vector<size_t> order(pend.size());
     for (size_t k = 0; k < order.size(); ++k) order[k] = k;
     std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) { return sub_group[a] < sub_group[b]; });
@@ -478,7 +549,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     h->n_elem_tiles = (int32_t)elem_tiles.size();
     const size_t o_norm_part = take(sizeof(float) * elem_tiles.size());
     const size_t o_mom = take(sizeof(float) * (size_t)mom_total);
-    std::vector<size_t> go_ulo, go_u16, go_x16[2], go_a16, go_p16, go_rowsq, go_v, go_lane, go_colsq;
+    std::vector<size_t> go_ulo, go_u16, go_x16[2], go_a16, go_p16, go_pb16, go_t16, go_rowsq, go_v, go_lane, go_colsq;
     for (auto& g : h->groups) {
         g.count = 0;
         g.lane_stride = g.m;
@@ -508,6 +579,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         }
         go_a16.push_back(take(ae * 2));
         go_p16.push_back(take(ae * 2));
+        go_pb16.push_back(g.gs ? take(ae * 2) : 0);
+        go_t16.push_back(g.gs ? take(ae * 2) : 0);
         go_rowsq.push_back(take((size_t)g.count * g.m * g.ntile_n * 2 * 4));
         go_v.push_back(take((size_t)g.count * g.lane_stride * 4));
         go_lane.push_back(take((size_t)g.count * g.lane_stride * 4));
@@ -593,22 +666,49 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             pair_fit = pair_fit && g.m % 256 == 0 && g.n % 256 == 0;
         }
         if (pair_fit) {
-            std::vector<T> pr;
-            for (int sl = 0; sl < ch.ng; ++sl) {
-                const Group& g = h->groups[ch.gi[sl]];
-                for (int idx = 0; idx < g.count; ++idx)
-                    for (int ti = 0; ti < g.m / 256; ++ti)
-                        for (int tj = 0; tj < g.n / 256; ++tj) pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+            // which: 0 every group, 1 the standard-form groups, 2 the Gram-pair groups
+            auto member = [&](int sl, int which) {
+                const bool gs = h->groups[ch.gi[sl]].gs != 0;
+                return which == 0 || (which == 1 && !gs) || (which == 2 && gs);
+            };
+            auto upd_list = [&](int which, int32_t& o, int32_t& n) {
+                std::vector<T> pr;
+                for (int sl = 0; sl < ch.ng; ++sl) {
+                    if (!member(sl, which)) continue;
+                    const Group& g = h->groups[ch.gi[sl]];
+                    for (int idx = 0; idx < g.count; ++idx)
+                        for (int ti = 0; ti < g.m / 256; ++ti)
+                            for (int tj = 0; tj < g.n / 256; ++tj)
+                                pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+                }
+                emit(pr, o, n);
+            };
+            auto sym_list = [&](int which, int32_t& o, int32_t& n) {
+                std::vector<T> sg;
+                for (int sl = 0; sl < ch.ng; ++sl) {
+                    if (!member(sl, which)) continue;
+                    const Group& g = h->groups[ch.gi[sl]];
+                    for (int idx = 0; idx < g.count; ++idx)
+                        for (int ti = 0; ti < g.m / 256; ++ti)
+                            for (int tj = ti; tj < g.m / 256; ++tj)
+                                sg.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
+                }
+                emit(sg, o, n);
+            };
+            upd_list(0, ch.pair_off, ch.pair_n);
+            sym_list(0, ch.spg_off, ch.spg_n);
+            bool any_gs = false;
+            for (int sl = 0; sl < ch.ng; ++sl) any_gs = any_gs || member(sl, 2);
+            if (any_gs) {
+                upd_list(1, ch.pair_std_off, ch.pair_std_n);
+                sym_list(1, ch.spg_std_off, ch.spg_std_n);
+                sym_list(2, ch.spg_gs_off, ch.spg_gs_n);
+            } else {
+                ch.pair_std_off = ch.pair_off;
+                ch.pair_std_n = ch.pair_n;
+                ch.spg_std_off = ch.spg_off;
+                ch.spg_std_n = ch.spg_n;
             }
-            emit(pr, ch.pair_off, ch.pair_n);
-            std::vector<T> sg;
-            for (int sl = 0; sl < ch.ng; ++sl) {
-                const Group& g = h->groups[ch.gi[sl]];
-                for (int idx = 0; idx < g.count; ++idx)
-                    for (int ti = 0; ti < g.m / 256; ++ti)
-                        for (int tj = ti; tj < g.m / 256; ++tj) sg.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.n});
-            }
-            emit(sg, ch.spg_off, ch.spg_n);
         }
         h->chunks.push_back(ch);
     }
@@ -647,6 +747,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         }
         g.a16 = reinterpret_cast<uint16_t*>(base + go_a16[gi]);
         g.p16 = reinterpret_cast<uint16_t*>(base + go_p16[gi]);
+        g.pb16 = g.gs ? reinterpret_cast<uint16_t*>(base + go_pb16[gi]) : nullptr;
+        g.t16 = g.gs ? reinterpret_cast<uint16_t*>(base + go_t16[gi]) : nullptr;
+        g.final_buf = final_buffer(g, cfg.ns_steps);
         g.rowsq = reinterpret_cast<float*>(base + go_rowsq[gi]);
         g.v = reinterpret_cast<float*>(base + go_v[gi]);
         g.lane = reinterpret_cast<float*>(base + go_lane[gi]);
@@ -683,6 +786,14 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                        kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_bf16_3d(enc, &g.map_a_mir, g.a16, g.m, g.m, g.count, g.lda, 64) &&
              encode_bf16_3d(enc, &g.map_p_mir, g.p16, g.m, g.m, g.count, g.lda, 64);
+        if (ok && g.gs)
+            ok = encode_bf16_3d(enc, &g.map_p_mn, g.p16, g.m, g.m, g.count, g.lda, 64) &&
+                 encode_bf16_3d(enc, &g.map_pb_k, g.pb16, g.m, g.m, g.count, g.lda, kBM) &&
+                 encode_bf16_3d(enc, &g.map_t_k, g.t16, g.m, g.m, g.count, g.lda, kBM) &&
+                 encode_3d(enc, &g.map_pb_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.pb16, g.m, g.m, g.count, g.lda,
+                           32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+                 encode_3d(enc, &g.map_t_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.t16, g.m, g.m, g.count, g.lda,
+                           32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
         if (!ok) {
             cudaFree(h->arena);
             delete h;
@@ -691,7 +802,6 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
     }
 
     // ---- sub descriptors (group order)
-    const int last_buf = (cfg.ns_steps - 1) % 2;
     std::vector<int> idx_in_group(h->groups.size(), 0);
     for (int sidx = 0; sidx < nsubs; ++sidx) {
         const Pending& pd = pend[order[sidx]];
@@ -723,7 +833,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         const int64_t xo = (int64_t)gi * g.m * g.ldx;
         d.u16 = g.u16 + xo;
         d.ulo16 = g.ulo16 + xo;
-        d.o16 = g.x16[last_buf] + xo;
+        d.o16 = g.x16[g.final_buf] + xo;
         d.rowsq = g.rowsq + (int64_t)gi * g.m * g.ntile_n * 2;
         d.v = g.v + (int64_t)gi * g.lane_stride;
         d.lane = g.lane + (int64_t)gi * g.lane_stride;
@@ -753,98 +863,205 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         return fail(nullptr, MUON_ERR_CUDA, "upload / kernel configuration failed");
     }
 
-    // ---- GEMM parameter blocks: [iteration][chunk][mode]
-    for (int it = 0; it < cfg.ns_steps; ++it) {
-        const bool first = it == 0, last = it == cfg.ns_steps - 1;
-        const int in_buf = (it - 1) % 2, out_buf = it % 2;
-        for (const Chunk& ch : h->chunks) {
-            for (int mode = 0; mode < 3; ++mode) {
-                GemmParams gp;
-                memset(&gp, 0, sizeof(gp));
-                gp.ngroups = ch.ng;
-                gp.norm_scale = h->norm_scale;
-                gp.iter_scale = h->iter_scale;
-                gp.ca = h->coeffs[3 * it + 0];
-                gp.cb = h->coeffs[3 * it + 1];
-                gp.cc = h->coeffs[3 * it + 2];
-                gp.first = first;
-                gp.last = last;
-                gp.f16 = it > 0;
-                gp.want_rowsq = last && cfg.normuon;
-                gp.status = h->status;
-                // launches alternate between each list and its reversed copy (Gram, polynomial
-                // and update are three launches per iteration, so the order flips every launch)
-                const bool rev = ((3 * it + mode) & 1) != 0;
-                auto pick = [&](int32_t off, int32_t n) {
-                    gp.tiles = h->d_gemm_tiles + off + (rev ? n : 0);
-                    gp.ntiles = n;
-                };
-                if (mode == MODE_GRAM && ch.spg_n > 0) {
-                    pick(ch.spg_off, ch.spg_n);
-                    gp.pair = 1;
-                } else if (mode == MODE_GRAM) {
-                    pick(ch.gram_off, ch.gram_n);
-                } else if (mode == MODE_POLY && ch.spg_n > 0) {
-                    // the polynomial on SM pairs: the same 256 x 256 tiles (J >= I) as the Gram
-                    pick(ch.spg_off, ch.spg_n);
-                    gp.pair = 1;
-                } else if (mode == MODE_POLY) {
-                    pick(ch.poly_off, ch.poly_n);
-                } else if (ch.pair_n > 0) {
-                    pick(ch.pair_off, ch.pair_n);
-                    gp.pair = 1;
-                } else {
-                    pick(ch.upd_off, ch.upd_n);
-                }
-                for (int sl = 0; sl < ch.ng; ++sl) {
-                    const Group& g = h->groups[ch.gi[sl]];
-                    GemmGroup& G = gp.grp[sl];
-                    G.m = g.m;
-                    G.n = g.n;
-                    G.ldx = g.ldx;
-                    G.lda = g.lda;
-                    G.ntile_n = g.ntile_n;
-                    G.sub0 = g.sub0;
-                    G.x_stride = (int64_t)g.m * g.ldx;
-                    G.a_stride = (int64_t)g.m * g.lda;
-                    const uint16_t* xin16 = first ? g.u16 : g.x16[in_buf];
-                    G.xlo_in = first ? g.ulo16 : nullptr;  // the first update reads u as hi + lo
-                    G.x16_out = g.x16[out_buf];
-                    G.a16 = g.a16;
-                    G.rowsq = g.rowsq;
-                    if (mode == MODE_GRAM) {
-                        gp.map_a[sl] = first ? g.map_u_k : g.map_x_k[in_buf];
-                        gp.map_b[sl] = first ? g.map_u_k256 : g.map_x_k256[in_buf];
-                        gp.map_out[sl] = gp.pair ? g.map_a_w32 : g.map_a_k;
-                        gp.map_out2[sl] = g.map_a_mir;
-                        G.out16 = g.a16;
-                        G.opl16 = xin16;
-                        G.opr16 = xin16;
-                    } else if (mode == MODE_POLY) {
-                        gp.map_a[sl] = g.map_a_k;
-                        gp.map_b[sl] = gp.pair ? g.map_a_mn : g.map_a_k256;
-                        gp.map_ein[sl] = gp.pair ? g.map_a_w32 : g.map_a_k;
-                        gp.map_out[sl] = gp.pair ? g.map_p_w32 : g.map_p_k;
-                        gp.map_out2[sl] = g.map_p_mir;
-                        G.out16 = g.p16;
-                        G.opl16 = g.a16;
-                        G.opr16 = g.a16;
-                    } else {
-                        gp.map_a[sl] = g.map_p_k;
-                        // the folded update on SM pairs takes 128-deep k-blocks (16 KB boxes of X)
-                        gp.map_b[sl] = first ? g.map_u_mn : (gp.pair ? g.map_x_mn128[in_buf] : g.map_x_mn[in_buf]);
-                        // first update: u hi | lo in 32-column boxes, X1 out in 32-column boxes;
-                        // later updates (a on the diagonal of P): no input, X' out in 64-column boxes
-                        gp.map_ein[sl] = gp.pair ? g.map_u_hi_w32 : g.map_u_hi;
-                        gp.map_ein2[sl] = gp.pair ? g.map_u_lo_w32 : g.map_u_lo;
-                        gp.map_out[sl] = gp.pair ? g.map_x_w32[out_buf] : (first ? g.map_x_o32[out_buf] : g.map_x_k[out_buf]);
-                        G.opl16 = g.p16;
-                        G.opr16 = xin16;
-                    }
-                }
-                h->gparams.push_back(gp);
+    // ---- the Newton-Schulz launch plan: per iteration the Gram, polynomial, plain-product
+    // and update phases, each one launch per chunk whose groups have work in that phase
+    {
+        const int steps = cfg.ns_steps;
+        std::vector<int> cur(h->groups.size(), 0);      // iterate buffer holding the current X (after the first iteration)
+        std::vector<int> nlaunch(h->chunks.size(), 0);  // per chunk: launches so far (alternating tile order)
+        auto add_work = [&](int stage, const Group& g, GroupOp op, bool first) {
+            const double m = g.m, n = g.n;
+            double fl = 0, by = 0;
+            switch (op) {
+                case OP_GRAM: fl = m * (m + 1) * n; by = 2 * m * n + 2 * m * m; break;
+                case OP_POLY:
+                case OP_POLY_B: fl = m * m * (m + 1); by = 4 * m * m; break;
+                case OP_PLAIN_T:
+                case OP_PLAIN_A:
+                case OP_PLAIN_Q: fl = m * m * (m + 1); by = 6 * m * m; break;
+                case OP_UPD: fl = 2 * m * m * n; by = 2 * m * m + (first ? 6 : 4) * m * n; break;
+                case OP_UPD_Q: fl = 2 * m * m * n; by = 2 * m * m + 4 * m * n; break;
+                default: break;
             }
+            h->work_flops[stage] += (int64_t)(fl * g.count);
+            h->work_bytes[stage] += (int64_t)(by * g.count);
+        };
+        for (int it = 0; it < steps; ++it) {
+            const bool first = it == 0, last = it == steps - 1;
+            for (int ph = 0; ph < PH_COUNT; ++ph) {
+                for (int c = 0; c < (int)h->chunks.size(); ++c) {
+                    const Chunk& ch = h->chunks[c];
+                    const bool pairs = ch.spg_n > 0;  // the chunk tiles by 256: SM-pair kernels
+                    GemmParams gp;
+                    memset(&gp, 0, sizeof(gp));
+                    gp.ngroups = ch.ng;
+                    gp.norm_scale = h->norm_scale;
+                    gp.iter_scale = h->iter_scale;
+                    gp.ca = h->coeffs[3 * it + 0];
+                    gp.cb = h->coeffs[3 * it + 1];
+                    gp.cc = h->coeffs[3 * it + 2];
+                    gp.first = first;
+                    gp.last = last;
+                    gp.f16 = it > 0;
+                    gp.want_rowsq = ph == PH_UPDATE && last && cfg.normuon;
+                    gp.status = h->status;
+                    gp.pair = pairs ? 1 : 0;
+                    int n_in = 0, n_in_gs = 0, n_gs = 0;
+                    GroupOp ops[kMaxGroupsPerLaunch];
+                    for (int sl = 0; sl < ch.ng; ++sl) {
+                        const Group& g = h->groups[ch.gi[sl]];
+                        const int cb = cur[ch.gi[sl]], nb = first ? 0 : cur[ch.gi[sl]] ^ 1;
+                        GemmGroup& G = gp.grp[sl];
+                        G.m = g.m;
+                        G.n = g.n;
+                        G.ldx = g.ldx;
+                        G.lda = g.lda;
+                        G.ntile_n = g.ntile_n;
+                        G.sub0 = g.sub0;
+                        G.x_stride = (int64_t)g.m * g.ldx;
+                        G.a_stride = (int64_t)g.m * g.lda;
+                        G.a16 = g.a16;
+                        G.rowsq = g.rowsq;
+                        const uint16_t* xin16 = first ? g.u16 : g.x16[cb];
+                        const GroupOp op = group_op(g, it, steps, ph);
+                        ops[sl] = op;
+                        n_gs += g.gs ? 1 : 0;
+                        // every slot carries valid descriptors (the kernels prefetch all of them);
+                        // the group's own operation below replaces them
+                        gp.map_a[sl] = g.map_a_k;
+                        gp.map_b[sl] = g.map_a_mn;
+                        gp.map_ein[sl] = g.map_a_w32;
+                        gp.map_ein2[sl] = g.map_a_w32;
+                        gp.map_out[sl] = g.map_a_w32;
+                        gp.map_out2[sl] = g.map_a_mir;
+                        if (op == OP_NONE) continue;
+                        ++n_in;
+                        n_in_gs += g.gs ? 1 : 0;
+                        switch (op) {
+                            case OP_GRAM:
+                                gp.map_a[sl] = first ? g.map_u_k : g.map_x_k[cb];
+                                gp.map_b[sl] = first ? g.map_u_k256 : g.map_x_k256[cb];
+                                gp.map_out[sl] = pairs ? g.map_a_w32 : g.map_a_k;
+                                gp.map_out2[sl] = g.map_a_mir;
+                                G.out16 = g.a16;
+                                G.opl16 = xin16;
+                                G.opr16 = xin16;
+                                break;
+                            case OP_POLY:
+                            case OP_POLY_B:  // the second polynomial of a Gram pair keeps the first one's P
+                                gp.map_a[sl] = g.map_a_k;
+                                gp.map_b[sl] = pairs ? g.map_a_mn : g.map_a_k256;
+                                gp.map_ein[sl] = pairs ? g.map_a_w32 : g.map_a_k;
+                                gp.map_out[sl] = op == OP_POLY_B ? g.map_pb_w32 : (pairs ? g.map_p_w32 : g.map_p_k);
+                                gp.map_out2[sl] = g.map_p_mir;
+                                G.out16 = op == OP_POLY_B ? g.pb16 : g.p16;
+                                G.opl16 = g.a16;
+                                G.opr16 = g.a16;
+                                break;
+                            case OP_PLAIN_T:  // T = A P'
+                                gp.map_a[sl] = g.map_a_k;
+                                gp.map_b[sl] = g.map_p_mn;
+                                gp.map_out[sl] = g.map_t_w32;
+                                G.out16 = g.t16;
+                                G.opl16 = g.a16;
+                                G.opr16 = g.p16;
+                                break;
+                            case OP_PLAIN_A:  // A <- T P'
+                                gp.map_a[sl] = g.map_t_k;
+                                gp.map_b[sl] = g.map_p_mn;
+                                gp.map_out[sl] = g.map_a_w32;
+                                G.out16 = g.a16;
+                                G.opl16 = g.t16;
+                                G.opr16 = g.p16;
+                                break;
+                            case OP_PLAIN_Q:  // Q = P'' P' (into T's buffer)
+                                gp.map_a[sl] = g.map_pb_k;
+                                gp.map_b[sl] = g.map_p_mn;
+                                gp.map_out[sl] = g.map_t_w32;
+                                G.out16 = g.t16;
+                                G.opl16 = g.pb16;
+                                G.opr16 = g.p16;
+                                break;
+                            case OP_UPD:
+                                gp.map_a[sl] = g.map_p_k;
+                                // the folded update on SM pairs takes 128-deep k-blocks (16 KB boxes of X)
+                                gp.map_b[sl] = first ? g.map_u_mn : (pairs ? g.map_x_mn128[cb] : g.map_x_mn[cb]);
+                                // first update: u hi | lo in 32-column boxes, X1 out in 32-column boxes;
+                                // later updates (a on the diagonal of P): no input, X' out in 64-column boxes
+                                gp.map_ein[sl] = pairs ? g.map_u_hi_w32 : g.map_u_hi;
+                                gp.map_ein2[sl] = pairs ? g.map_u_lo_w32 : g.map_u_lo;
+                                gp.map_out[sl] = pairs ? g.map_x_w32[nb] : (first ? g.map_x_o32[nb] : g.map_x_k[nb]);
+                                G.xlo_in = first ? g.ulo16 : nullptr;  // the first update reads u as hi + lo
+                                G.x16_out = g.x16[nb];
+                                G.opl16 = g.p16;
+                                G.opr16 = xin16;
+                                break;
+                            case OP_UPD_Q:  // X_{k+2} = Q X_k
+                                gp.map_a[sl] = g.map_t_k;
+                                gp.map_b[sl] = g.map_x_mn128[cb];
+                                gp.map_out[sl] = g.map_x_w32[nb];
+                                G.x16_out = g.x16[nb];
+                                G.opl16 = g.t16;
+                                G.opr16 = xin16;
+                                break;
+                            default: break;
+                        }
+                    }
+                    if (n_in == 0) continue;
+                    // the tile list of the groups that take part
+                    const bool all_in = n_in == ch.ng;
+                    const bool std_only = n_in_gs == 0 && n_in == ch.ng - n_gs;
+                    const bool rev = (nlaunch[c]++ & 1) != 0;
+                    auto pick = [&](int32_t off, int32_t n) {
+                        gp.tiles = h->d_gemm_tiles + off + (rev ? n : 0);
+                        gp.ntiles = n;
+                    };
+                    int mode = ph == PH_GRAM ? MODE_GRAM
+                                             : (ph == PH_POLY ? MODE_POLY : (ph == PH_UPDATE ? MODE_UPDATE : MODE_PLAIN));
+                    if (pairs) {
+                        if (mode == MODE_UPDATE)
+                            pick(all_in ? ch.pair_off : ch.pair_std_off, all_in ? ch.pair_n : ch.pair_std_n);
+                        else if (all_in)
+                            pick(ch.spg_off, ch.spg_n);
+                        else if (std_only)
+                            pick(ch.spg_std_off, ch.spg_std_n);
+                        else
+                            pick(ch.spg_gs_off, ch.spg_gs_n);
+                    } else {
+                        pick(mode == MODE_GRAM ? ch.gram_off : (mode == MODE_POLY ? ch.poly_off : ch.upd_off),
+                             mode == MODE_GRAM ? ch.gram_n : (mode == MODE_POLY ? ch.poly_n : ch.upd_n));
+                    }
+                    const int stage = mode == MODE_GRAM ? MUON_STAGE_GRAM
+                                                        : (mode == MODE_POLY ? MUON_STAGE_POLY
+                                                                             : (mode == MODE_UPDATE ? MUON_STAGE_UPDATE
+                                                                                                    : MUON_STAGE_PRODUCT));
+                    for (int sl = 0; sl < ch.ng; ++sl)
+                        if (ops[sl] != OP_NONE) add_work(stage, h->groups[ch.gi[sl]], ops[sl], first);
+                    h->work_launches[stage]++;
+                    h->plan.push_back(Launch{stage, mode, c, it, pairs ? 1 : 0, it > 0 ? 1 : 0});
+                    h->gparams.push_back(gp);
+                }
+            }
+            // groups that updated now hold their iterate in the other buffer
+            for (size_t gi = 0; gi < h->groups.size(); ++gi)
+                if (group_op(h->groups[gi], it, steps, PH_UPDATE) != OP_NONE) cur[gi] = first ? 0 : cur[gi] ^ 1;
         }
+        for (size_t gi = 0; gi < h->groups.size(); ++gi)
+            if (cur[gi] != h->groups[gi].final_buf) {
+                cudaFree(h->arena);
+                delete h;
+                return fail(nullptr, MUON_ERR_CUDA, "internal error: iterate buffer bookkeeping");
+            }
+        // the elementwise stages' algorithmic bytes: momentum reads g and the buffer and writes
+        // the buffer and u's hi and lo halves; apply reads O (fp16) and p and writes p
+        int64_t elems = 0;
+        for (const muon_shape& sh : h->shapes) elems += sh.rows * sh.cols;
+        h->work_bytes[MUON_STAGE_MOMENTUM] = elems * ((cfg.grad_dtype == MUON_GRAD_BF16 ? 2 : 4) + 4 + 4 + 2 + 2);
+        h->work_bytes[MUON_STAGE_APPLY] = elems * (2 + 4 + 4);
+        h->work_launches[MUON_STAGE_MOMENTUM] = 1;
+        h->work_launches[MUON_STAGE_NORM] = 1;
+        h->work_launches[MUON_STAGE_LANE] = 1 + (h->n_colwork > 0 ? 1 : 0);
+        h->work_launches[MUON_STAGE_APPLY] = 1;
     }
 
     {
@@ -874,52 +1091,52 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
     NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale, h->iter_scale, h->status};
     MUON_CUDA(h, mark(h, MUON_STAGE_NORM, s));
     MUON_CUDA(h, launch_norm_scale(np, s));
-    const int nch = (int)h->chunks.size();
-    for (int it = 0; it < h->cfg.ns_steps; ++it) {
-        for (int mode = 0; mode < 3; ++mode) {
-            for (int c = 0; c < nch; ++c) {
-                const GemmParams* gpp = &h->gparams[((size_t)it * nch + c) * 3 + mode];
-                GemmParams stalled;
-                if (h->stall_next && it == 0 && c == h->stall_chunk && mode == MODE_POLY &&
-                    h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
-                    // test only (muon_debug_inject_stall): this launch's MMA issuers wait on an
-                    // mbarrier that nothing arrives on until their bounded wait gives up
-                    stalled = *gpp;
-                    stalled.debug_stall = 1;
-                    gpp = &stalled;
-                    h->stall_next = false;
-                }
-                const GemmParams& gp = *gpp;
-                MUON_CUDA(h, mark(h, MUON_STAGE_GRAM + mode, s));
-                if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
-                    // the first iteration works on bf16 u; later ones on the fp16 iterate
-                    const bool f16 = it > 0;
-                    cudaError_t e = cudaSuccess;
-                    if (mode == MODE_GRAM && gp.pair)
-                        e = f16 ? launch_ns_sym_pair<MODE_GRAM, true>(gp, h->num_sms, s)
-                                : launch_ns_sym_pair<MODE_GRAM, false>(gp, h->num_sms, s);
-                    else if (mode == MODE_GRAM)
-                        e = f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, s)
-                                : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, s);
-                    if (mode == MODE_POLY && gp.pair)
-                        e = f16 ? launch_ns_sym_pair<MODE_POLY, true>(gp, h->num_sms, s)
-                                : launch_ns_sym_pair<MODE_POLY, false>(gp, h->num_sms, s);
-                    else if (mode == MODE_POLY)
-                        e = f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
-                                : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s);
-                    if (mode == MODE_UPDATE)
-                        e = gp.pair ? launch_ns_update_pair(gp, !f16, h->num_sms, s)
-                                    : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
-                                           : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s));
-                    MUON_CUDA(h, e);
-                } else {
-                    for (int sl = 0; sl < gp.ngroups; ++sl) {
-                        const int cnt = h->groups[h->chunks[c].gi[sl]].count;
-                        if (mode == MODE_GRAM) MUON_CUDA(h, launch_ns_gemm_simt<MODE_GRAM>(gp, sl, cnt, s));
-                        if (mode == MODE_POLY) MUON_CUDA(h, launch_ns_gemm_simt<MODE_POLY>(gp, sl, cnt, s));
-                        if (mode == MODE_UPDATE) MUON_CUDA(h, launch_ns_gemm_simt<MODE_UPDATE>(gp, sl, cnt, s));
-                    }
-                }
+    for (size_t k = 0; k < h->plan.size(); ++k) {
+        const Launch& L = h->plan[k];
+        const GemmParams* gpp = &h->gparams[k];
+        GemmParams stalled;
+        if (h->stall_next && L.it == 0 && L.chunk == h->stall_chunk && L.mode == MODE_POLY &&
+            h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
+            // test only (muon_debug_inject_stall): this launch's MMA issuers wait on an
+            // mbarrier that nothing arrives on until their bounded wait gives up
+            stalled = *gpp;
+            stalled.debug_stall = 1;
+            gpp = &stalled;
+            h->stall_next = false;
+        }
+        const GemmParams& gp = *gpp;
+        MUON_CUDA(h, mark(h, L.stage, s));
+        if (h->cfg.gemm_engine == MUON_GEMM_TCGEN05) {
+            // the first iteration works on bf16 u; later ones on the fp16 iterate
+            const bool f16 = L.f16 != 0;
+            cudaError_t e = cudaSuccess;
+            switch (L.mode) {
+                case MODE_GRAM:
+                    e = L.pair ? (f16 ? launch_ns_sym_pair<MODE_GRAM, true>(gp, h->num_sms, s)
+                                      : launch_ns_sym_pair<MODE_GRAM, false>(gp, h->num_sms, s))
+                               : (f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, s)
+                                      : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, s));
+                    break;
+                case MODE_POLY:
+                    e = L.pair ? (f16 ? launch_ns_sym_pair<MODE_POLY, true>(gp, h->num_sms, s)
+                                      : launch_ns_sym_pair<MODE_POLY, false>(gp, h->num_sms, s))
+                               : (f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
+                                      : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s));
+                    break;
+                case MODE_PLAIN: e = launch_ns_sym_pair<MODE_PLAIN, true>(gp, h->num_sms, s); break;
+                default:
+                    e = L.pair ? launch_ns_update_pair(gp, !f16, h->num_sms, s)
+                               : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
+                                      : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s));
+                    break;
+            }
+            MUON_CUDA(h, e);
+        } else {
+            for (int sl = 0; sl < gp.ngroups; ++sl) {
+                const int cnt = h->groups[h->chunks[L.chunk].gi[sl]].count;
+                if (L.mode == MODE_GRAM) MUON_CUDA(h, launch_ns_gemm_simt<MODE_GRAM>(gp, sl, cnt, s));
+                if (L.mode == MODE_POLY) MUON_CUDA(h, launch_ns_gemm_simt<MODE_POLY>(gp, sl, cnt, s));
+                if (L.mode == MODE_UPDATE) MUON_CUDA(h, launch_ns_gemm_simt<MODE_UPDATE>(gp, sl, cnt, s));
             }
         }
     }
@@ -1039,6 +1256,7 @@ int muon_destroy(muon_handle h) {
     h->alive = false;  // the host object stays as a tombstone so stale handles are recognised
     h->gparams.clear();
     h->gparams.shrink_to_fit();
+    h->plan.clear();
     return MUON_OK;
 }
 
@@ -1082,12 +1300,23 @@ int muon_launch_count(muon_handle h, int32_t* out) {
     return MUON_OK;
 }
 
+int muon_stage_work(muon_handle h, int64_t* flops, int64_t* bytes, int32_t* launches) {
+    int rc = check_handle(h);
+    if (rc) return rc;
+    for (int k = 0; k < MUON_NUM_STAGES; ++k) {
+        if (flops) flops[k] = h->work_flops[k];
+        if (bytes) bytes[k] = h->work_bytes[k];
+        if (launches) launches[k] = h->work_launches[k];
+    }
+    return MUON_OK;
+}
+
 int muon_set_profiling(muon_handle h, int32_t enable) {
     int rc = check_handle(h);
     if (rc) return rc;
     MUON_CUDA(h, cudaSetDevice(h->device));
     if (enable && h->events.empty()) {
-        const int n = 4 + 3 * (int)h->chunks.size() * h->cfg.ns_steps + 1;
+        const int n = 4 + (int)h->plan.size() + 1;
         h->events.resize(n);
         h->event_stage.assign(n, -1);
         for (int k = 0; k < n; ++k) MUON_CUDA(h, cudaEventCreate(&h->events[k]));

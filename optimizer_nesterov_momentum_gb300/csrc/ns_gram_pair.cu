@@ -7,6 +7,10 @@
 //                                      as the Gram with A's rows for X's; from the
 //                                      second iteration on the epilogue adds a to
 //                                      the diagonal: P' = a I + P)
+//   MODE_PLAIN  C = L R               (L, R symmetric polynomials in one Gram matrix,
+//                                      so they commute and C is symmetric: the
+//                                      Gram-space products T = A P', A = T P' and
+//                                      Q = P'' P')
 //
 // with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) issued by CTA 0 of a
 // two-CTA cluster.  A pair tile is the 256 x 256 block (I, J), J >= I, of the
@@ -49,6 +53,7 @@ constexpr int kOutSlots = 2;  // per warp: blocks and mirrors in flight
 template <int MODE>
 struct SymPairCfg {
     static constexpr bool POLY = MODE == MODE_POLY;
+    static constexpr bool MNB = MODE != MODE_GRAM;  // right operand MN-major (columns of a symmetric matrix)
     // the polynomial gives up one stage for its per-warp input ring (two 32 x 32 blocks of A)
     static constexpr int STAGES = POLY ? 5 : 6;
     static constexpr int IN_SLOTS = POLY ? 2 : 0;
@@ -65,8 +70,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     k_ns_sym_pair(const __grid_constant__ GemmParams p) {
     using C = SymPairCfg<MODE>;
     constexpr int STAGES = C::STAGES;
-    // the polynomial's right operand is MN-major (columns of the symmetric A)
-    constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/C::POLY, F16);
+    // the polynomial's and the plain product's right operand is MN-major (columns of a
+    // symmetric matrix)
+    constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/C::MNB, F16);
     // the polynomial of the second and later iterations adds a to the diagonal of P
     constexpr bool FOLD = C::POLY && F16;
 
@@ -134,7 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
         if (lane == 0 && run) {
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_a[g]);
-                if (C::POLY) tma_prefetch_desc(&p.map_b[g]);
+                if (C::MNB) tma_prefetch_desc(&p.map_b[g]);
             }
             const uint32_t full0 = cluster_addr(&full[0], 0);
             int stage = 0;
@@ -146,9 +152,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
-                const int K = C::POLY ? p.grp[g].m : p.grp[g].n;
+                const int K = C::MNB ? p.grp[g].m : p.grp[g].n;
                 const int nkb = (K + kBK - 1) / kBK;
-                const bool diag = !C::POLY && ti == tj;  // a diagonal Gram tile stages one set of rows
+                const bool diag = MODE == MODE_GRAM && ti == tj;  // a diagonal Gram tile stages one set of rows
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
@@ -158,8 +164,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     const uint32_t bar = full0 + (uint32_t)(stage * 8);
                     uint8_t* dst = sS + stage * kSymStage;
                     tma_load_3d_pair(dst, &p.map_a[g], bar, kb * kBK, ti * 256 + (int)rank * kBM, idx);
-                    if (C::POLY) {
-                        // columns 256 J + 128 r .. + 127 of A for k-block rows kb: two 64-column boxes
+                    if (C::MNB) {
+                        // columns 256 J + 128 r .. + 127 of the right operand for k-block rows kb:
+                        // two 64-column boxes
                         const int col = tj * 256 + (int)rank * 128;
                         tma_load_3d_pair(dst + kSymRows, &p.map_b[g], bar, col, kb * kBK, idx);
                         tma_load_3d_pair(dst + kSymRows + 64 * kBK * 2, &p.map_b[g], bar, col + 64, kb * kBK, idx);
@@ -188,9 +195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
-                const int K = C::POLY ? p.grp[tile.x].m : p.grp[tile.x].n;
+                const int K = C::MNB ? p.grp[tile.x].m : p.grp[tile.x].n;
                 const int nkb = (K + kBK - 1) / kBK;
-                const bool diag = !C::POLY && tile.z == tile.w;
+                const bool diag = MODE == MODE_GRAM && tile.z == tile.w;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -222,11 +229,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                             const uint32_t b_st = diag ? a_st : a_st + kSymRows;  // a diagonal tile's halves are the same rows
                             // the stage's descriptors; a 16-deep step adds to the start-address field
                             // (16-byte units): 32 bytes along a K-major operand, 16 rows of 128 bytes
-                            // along the MN-major one (polynomial; 8 KB between its 64-column boxes)
+                            // along an MN-major one (8 KB between its 64-column boxes)
                             const uint64_t ad = make_sdesc_sw128(a_st, 16, 1024);
-                            const uint64_t bd = C::POLY ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
-                                                        : make_sdesc_sw128(b_st, 16, 1024);
-                            constexpr uint64_t b_step = C::POLY ? 128 : 2;
+                            const uint64_t bd = C::MNB ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
+                                                       : make_sdesc_sw128(b_st, 16, 1024);
+                            constexpr uint64_t b_step = C::MNB ? 128 : 2;
 #pragma unroll
                             for (int kk = 0; kk < kBK / 16; ++kk)
                                 umma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + b_step * (uint64_t)kk, IDESC,
@@ -443,13 +450,15 @@ cudaError_t ns_gram_pair_configure() {
     if (e == cudaSuccess) e = configure_sym<MODE_GRAM, true>();
     if (e == cudaSuccess) e = configure_sym<MODE_POLY, false>();
     if (e == cudaSuccess) e = configure_sym<MODE_POLY, true>();
+    if (e == cudaSuccess) e = configure_sym<MODE_PLAIN, true>();
     return e;
 }
 
 // p.tiles: 256 x 256 tiles {group slot, index, tile row I, tile column J >= I} (units of 256).
 // MODE_GRAM: p.map_a = 128-row boxes of the iterate (K = n); MODE_POLY: of A (K = m), with
 // p.map_b = A's 64 x 64 boxes (the MN-major right operand) and p.map_ein = A's 32 x 32 boxes
-// for the b A term.  p.map_out: 32 x 32 boxes of the result.
+// for the b A term; MODE_PLAIN: p.map_a = 128-row boxes of L, p.map_b = 64 x 64 boxes of R
+// (K = m).  p.map_out: 32 x 32 boxes of the result.
 template <int MODE, bool F16>
 cudaError_t launch_ns_sym_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
@@ -462,5 +471,6 @@ template cudaError_t launch_ns_sym_pair<MODE_GRAM, false>(const GemmParams&, int
 template cudaError_t launch_ns_sym_pair<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_ns_sym_pair<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_ns_sym_pair<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_PLAIN, true>(const GemmParams&, int, cudaStream_t);
 
 }  // namespace muon

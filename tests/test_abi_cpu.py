@@ -46,6 +46,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(_abi.muon_shape) == 32
     assert _abi.muon_config.lr_mul.offset == 48
     assert _abi.muon_config.normuon_lanes.offset == 72
+    assert _abi.muon_config.ns_form.offset == 76
     assert ctypes.sizeof(_abi.muon_config) == 80
     assert ctypes.sizeof(_abi.muon_schedule) == 40
     assert [getattr(_abi.muon_schedule, f).offset for f, _ in _abi.muon_schedule._fields_] == [0, 4, 8, 16, 24, 28, 32]
@@ -226,3 +227,31 @@ def test_normuon_lanes_is_validated(lib):
     assert cfg.normuon_lanes == A.MUON_LANES_SHORT_SIDE
     cfg.normuon_lanes = 3
     assert _create(lib, [A.muon_shape(64, 256, 0, 1, 0)], cfg) == A.MUON_ERR_ARG
+
+
+def test_ns_form_is_validated(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    cfg = A.muon_config_default()
+    assert cfg.ns_form == A.MUON_NS_GRAM_PAIRS
+    cfg.ns_form = 2
+    assert _create(lib, [A.muon_shape(64, 256, 0, 1, 0)], cfg) == A.MUON_ERR_ARG
+
+
+def test_stage_names_follow_the_header():
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    hdr = open(os.path.join(ROOT, "include", "muon.h")).read()
+    ids = {}
+    for line in hdr.splitlines():
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == "#define" and parts[1].startswith("MUON_STAGE_"):
+            ids[parts[1]] = int(parts[2])
+        if len(parts) >= 3 and parts[0] == "#define" and parts[1] == "MUON_NUM_STAGES":
+            assert int(parts[2]) == A.MUON_NUM_STAGES
+    names = {"MUON_STAGE_MOMENTUM": "momentum", "MUON_STAGE_NORM": "norm_scale", "MUON_STAGE_GRAM": "gram",
+             "MUON_STAGE_POLY": "poly", "MUON_STAGE_UPDATE": "update", "MUON_STAGE_LANE": "lane_stats",
+             "MUON_STAGE_APPLY": "apply", "MUON_STAGE_PRODUCT": "product"}
+    assert set(ids) == set(names)
+    for macro, k in ids.items():
+        assert A.MUON_STAGE_NAMES[k] == names[macro]

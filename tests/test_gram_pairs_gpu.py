@@ -1,0 +1,89 @@
+"""GPU parity of the Gram-pair order of the Newton-Schulz work (MUON_NS_GRAM_PAIRS).
+
+For wide matrices that tile by 256 (n >= 2m) the iterations after the first run two
+at a time in Gram space: one Gram matrix and one update per pair plus three m x m
+products, equal to the iteration in exact arithmetic (pinned in fp64 by
+tests/test_oracle_pins.py).  Here the CUDA path in that order is held to the same
+tolerances against the fp64 oracle as the standard order, on the three spectra of
+the synthetic workloads, for ns_steps from 3 to 6 (a pair, a pair plus a single
+iteration, two pairs, two pairs plus a single one), with matrices of the standard
+form (a square one, a narrow one and one that does not tile by 256) in the same
+handle.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.parity_util import Shape, make_optimizer, rel, run_parity
+from workloads.generators import _rng, gaussian_params, log_uniform_spectrum, lowrank_plus_noise, power_law_spectrum
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [Shape(256, 512), Shape(768, 3072), Shape(1536, 512), Shape(512, 512), Shape(512, 768), Shape(320, 640)]
+GEN = {"lowrank": lowrank_plus_noise, "powerlaw": power_law_spectrum, "loguniform": log_uniform_spectrum}
+
+
+def _inputs(kind, seed):
+    params = [gaussian_params(_rng(seed + 7777, i), s.rows, s.cols) for i, s in enumerate(SHAPES)]
+    grads = [GEN[kind](_rng(seed, i), s.rows, s.cols).to(torch.bfloat16).contiguous()
+             for i, s in enumerate(SHAPES)]
+    return params, grads
+
+
+@pytest.mark.parametrize("ns_steps", [3, 4, 5, 6])
+@pytest.mark.parametrize("kind", ["lowrank", "powerlaw", "loguniform"])
+def test_gram_pairs_match_the_oracle(kind, ns_steps):
+    params, grads = _inputs(kind, 9100 + ns_steps)
+    opt = make_optimizer(SHAPES, ns_steps=ns_steps, ns_form="gram_pairs", lr=0.03)
+    errs, opt, _ = run_parity(SHAPES, params, [grads], ns_steps=ns_steps, lr=0.03, opt=opt)
+    errs.assert_within()
+    work = opt.stage_work()
+    # the wide groups take the Gram-pair order: a pair launches T = A P' and A <- T P' in its
+    # first half and Q = P'' P' in its second
+    pairs = (ns_steps - 1) // 2
+    assert work["product"][2] == 3 * pairs, work
+    opt.close()
+
+
+def test_gram_pairs_and_standard_order_agree():
+    """Both orders on the same input: each within the oracle bound, and close to each other."""
+    from optimizer_nesterov_momentum_gb300 import MUON_STATE_ORTHO
+
+    params, grads = _inputs("powerlaw", 9300)
+    outs = {}
+    for form in ("standard", "gram_pairs"):
+        opt = make_optimizer(SHAPES, ns_form=form, lr=0.03)
+        errs, opt, _ = run_parity(SHAPES, [p.clone() for p in params], [grads], lr=0.03, opt=opt)
+        errs.assert_within()
+        outs[form] = [opt.get_state(MUON_STATE_ORTHO, k).double().cpu().numpy() for k in range(opt.num_matrices())]
+        if form == "standard":
+            assert opt.stage_work()["product"][2] == 0
+        opt.close()
+    for a, b in zip(outs["standard"], outs["gram_pairs"]):
+        assert rel(b, a) < 1e-2
+
+
+def test_gram_pairs_launch_plan():
+    """The step's launch count and per-stage work follow the plan of both orders."""
+    from optimizer_nesterov_momentum_gb300 import MatrixSpec, Muon
+
+    specs = [MatrixSpec(768, 3072), MatrixSpec(768, 768)]
+    std = Muon(specs, ns_form="standard")
+    gp = Muon(specs, ns_form="gram_pairs")
+    ws, wg = std.stage_work(), gp.stage_work()
+    m, n = 768, 3072
+    # standard: five Gram matrices, polynomials and updates per matrix
+    assert ws["gram"][0] == 5 * (m * (m + 1) * n + m * (m + 1) * m)
+    assert ws["update"][0] == 5 * (2 * m * m * n + 2 * m * m * m)
+    # Gram pairs (five iterations: one plain, two pairs): the wide matrix forms three Gram
+    # matrices and three updates, and six m x m products
+    assert wg["gram"][0] == 3 * m * (m + 1) * n + 5 * m * (m + 1) * m
+    assert wg["update"][0] == 3 * 2 * m * m * n + 5 * 2 * m * m * m
+    assert wg["product"][0] == 6 * m * m * (m + 1)
+    assert wg["poly"][0] == ws["poly"][0]
+    # the square matrix keeps its Gram and update launches in every iteration, so the pairs
+    # only add their product launches
+    assert gp.launch_count() == std.launch_count() + 6
+    std.close()
+    gp.close()

@@ -112,6 +112,63 @@ def test_ns_per_iteration_coefficients_closed_form():
     assert _rel(out, (u * s) @ vt) < 1e-12
 
 
+def _gram_pairs_fp64(x, coeffs):
+    """The order of operations of the GPU path's Gram-pair form (``MUON_NS_GRAM_PAIRS``),
+    restated in fp64 from two identities of the iteration X_{k+1} = P_k X_k with
+    P_k = a_k I + b_k A_k + c_k A_k^2 and A_k = X_k X_k^T: A_{k+1} = P_k A_k P_k, and
+    P_k commutes with A_k, so A_{k+1} = (A_k P_k) P_k and X_{k+2} = (P_{k+1} P_k) X_k.
+    The first iteration and a single one left at the end run in the plain form."""
+    m = x.shape[0]
+
+    def poly(A, t):
+        a, b, c = t
+        return a * np.eye(m) + b * A + c * (A @ A)
+
+    x = poly(x @ x.T, coeffs[0]) @ x
+    k = 1
+    while k < len(coeffs):
+        A = x @ x.T
+        P = poly(A, coeffs[k])
+        if k + 1 < len(coeffs):
+            A2 = (A @ P) @ P
+            x = (poly(A2, coeffs[k + 1]) @ P) @ x
+            k += 2
+        else:
+            x = P @ x
+            k += 1
+    return x
+
+
+@pytest.mark.parametrize("steps", [3, 4, 5, 6])
+def test_gram_pairs_equal_the_iteration(steps):
+    # Exact-arithmetic identity, checked in fp64 on a spectrum from 1e-4 to 1 with the
+    # pages' coefficients and with a per-iteration table.
+    rng = np.random.default_rng(100 + steps)
+    x = _rand_with_spectrum(rng, 24, 96, np.geomspace(1e-4, 1.0, 24))
+    x /= np.linalg.norm(x)
+    plain = [tuple(oracle.NS_COEFFS)] * steps
+    cycle = [(3.0, -3.2, 1.2), (2.0, -1.5, 0.5), (1.875, -1.25, 0.375), (3.4445, -4.7750, 2.0315)]
+    table = [cycle[k % 4] for k in range(steps)]
+    for coeffs in (plain, table):
+        ref = oracle.newton_schulz(x, steps=steps, coeffs=coeffs, form="poly")
+        assert _rel(_gram_pairs_fp64(x, coeffs), ref) < 1e-11
+
+
+def test_gram_pairs_identity_catches_a_wrong_order():
+    # The pin above is not vacuous: pairing the polynomials in the other order
+    # (P_k P_{k+1} built from A_k alone) differs from the iteration.
+    rng = np.random.default_rng(5)
+    x = _rand_with_spectrum(rng, 16, 48, np.geomspace(1e-3, 1.0, 16))
+    x /= np.linalg.norm(x)
+    a, b, c = oracle.NS_COEFFS
+    m = x.shape[0]
+    A = x @ x.T
+    P = a * np.eye(m) + b * A + c * A @ A
+    wrong = (P @ P) @ x  # uses A_k for both iterations
+    ref = oracle.newton_schulz(x, steps=2, form="poly")
+    assert _rel(wrong, ref) > 1e-2
+
+
 @pytest.mark.parametrize("m,n", [(16, 40), (24, 24), (8, 200)])
 def test_closed_form_matches_iteration(m, n):
     rng = np.random.default_rng(m + n)
