@@ -263,7 +263,8 @@ int muon_stage_work(muon_handle h, int64_t* flops, int64_t* bytes, int32_t* laun
 #define MUON_STAGE_UPDATE 4      /* S7, all iterations summed */
 #define MUON_STAGE_LANE 5        /* S8 + S9 factors (k_lane_stats) */
 #define MUON_STAGE_APPLY 6       /* S10 (k_apply) */
-#define MUON_STAGE_PRODUCT 7     /* the m x m products of Gram pairs (MUON_NS_GRAM_PAIRS) */
+#define MUON_STAGE_PRODUCT 7     /* MUON_NS_GRAM_PAIRS: each pair's product P_{k+1} P_k (its other
+                                    two m x m products run inside the Gram and update launches) */
 #define MUON_NUM_STAGES 8
 
 /* enable != 0: every later muon_step records CUDA events around each launch

@@ -113,6 +113,8 @@ struct ElemParams {
 struct GemmGroup {
     int32_t m, n, ldx, lda;
     int32_t ntile_n;
+    int32_t b_mn;            // SM-pair Gram launch: this group's tiles are plain products L R of two
+                             // symmetric m x m matrices (right operand MN-major, K = m), not X X^T
     int32_t sub0;            // sub index of the group's first matrix (subs are group-ordered)
     int64_t x_stride;        // elements between matrices in x / u arenas (m * ldx)
     int64_t a_stride;        // elements between matrices in a / p arenas (m * lda)

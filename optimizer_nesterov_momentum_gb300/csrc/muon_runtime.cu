@@ -88,7 +88,7 @@ struct Group {
     CUtensorMap map_x_mn128[2];  // X as MN-major boxes 128 rows deep (the SM-pair folded update's 128-deep k-blocks)
     // Gram-pair groups: P as the MN-major right operand of the plain products, the
     // second polynomial and T (or Q) as 128-row K-major left operands, and their stores
-    CUtensorMap map_p_mn, map_pb_k, map_pb_w32, map_t_k, map_t_w32;
+    CUtensorMap map_p_mn, map_p_mn128, map_pb_k, map_pb_w32, map_t_k, map_t_w32;
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_a_mn;      // 64 x 64 boxes of A: the MN-major right operand of the SM-pair polynomial
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
@@ -110,11 +110,11 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     int32_t upd_off = 0, upd_n = 0;
     int32_t pair_off = 0, pair_n = 0;  // 256 x 256 update tiles for SM pairs (0: chunk not eligible)
     int32_t spg_off = 0, spg_n = 0;    // 256 x 256 Gram tiles (J >= I) for SM pairs
-    // the same lists restricted to the groups that iterate in the standard form, and (symmetric
-    // tiles) to the Gram-pair groups
-    int32_t pair_std_off = 0, pair_std_n = 0;
-    int32_t spg_std_off = 0, spg_std_n = 0;
+    // Gram-pair chunks: the symmetric tiles of the Gram-pair groups alone, and the update
+    // tiles of the standard-form groups together with the full m x m tiles of the Gram-pair
+    // groups (the first half of a pair computes T = A P' in the update launch)
     int32_t spg_gs_off = 0, spg_gs_n = 0;
+    int32_t pair_t_off = 0, pair_t_n = 0;
 };
 
 // One Newton-Schulz launch of the step, in order.
@@ -285,9 +285,12 @@ cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* gra
 // with A_k = X_k X_k^T and P'_k a polynomial in A_k, X_{k+1} = P'_k X_k gives
 // A_{k+1} = P'_k A_k P'_k = (A_k P'_k) P'_k and X_{k+2} = (P'_{k+1} P'_k) X_k, so a pair
 // of iterations forms one Gram matrix and one update instead of two of each, for three
-// m x m products.  A single iteration left at the end runs in the standard form.
-enum GroupOp { OP_NONE, OP_GRAM, OP_POLY, OP_POLY_B, OP_PLAIN_T, OP_PLAIN_A, OP_PLAIN_Q, OP_UPD, OP_UPD_Q };
-enum Phase { PH_GRAM, PH_POLY, PH_PLAIN1, PH_PLAIN2, PH_UPDATE, PH_COUNT };
+// m x m products.  The products ride along with launches the other groups make anyway:
+// T = A_k P'_k with the first half's updates (on the update kernel, full m x m tiles),
+// A_{k+1} = T P'_k with the second half's Gram matrices; only Q = P'_{k+1} P'_k has a
+// launch of its own.  A single iteration left at the end runs in the standard form.
+enum GroupOp { OP_NONE, OP_GRAM, OP_POLY, OP_POLY_B, OP_PLAIN_A, OP_PLAIN_Q, OP_UPD, OP_UPD_T, OP_UPD_Q };
+enum Phase { PH_GRAM, PH_POLY, PH_PLAIN, PH_UPDATE, PH_COUNT };
 
 GroupOp group_op(const Group& g, int it, int steps, int phase) {
     int kind = 0;  // 0: standard, 1: first of a Gram pair, 2: second of a pair
@@ -296,11 +299,10 @@ GroupOp group_op(const Group& g, int it, int steps, int phase) {
         kind = pos == 1 ? 2 : (it + 1 < steps ? 1 : 0);
     }
     switch (phase) {
-        case PH_GRAM: return kind == 2 ? OP_NONE : OP_GRAM;
+        case PH_GRAM: return kind == 2 ? OP_PLAIN_A : OP_GRAM;
         case PH_POLY: return kind == 2 ? OP_POLY_B : OP_POLY;
-        case PH_PLAIN1: return kind == 1 ? OP_PLAIN_T : (kind == 2 ? OP_PLAIN_Q : OP_NONE);
-        case PH_PLAIN2: return kind == 1 ? OP_PLAIN_A : OP_NONE;
-        default: return kind == 1 ? OP_NONE : (kind == 2 ? OP_UPD_Q : OP_UPD);
+        case PH_PLAIN: return kind == 2 ? OP_PLAIN_Q : OP_NONE;
+        default: return kind == 1 ? OP_UPD_T : (kind == 2 ? OP_UPD_Q : OP_UPD);
     }
 }
 
@@ -308,8 +310,10 @@ GroupOp group_op(const Group& g, int it, int steps, int phase) {
 // and every later update flips it.
 int final_buffer(const Group& g, int steps) {
     int cur = 0;
-    for (int it = 1; it < steps; ++it)
-        if (group_op(g, it, steps, PH_UPDATE) != OP_NONE) cur ^= 1;
+    for (int it = 1; it < steps; ++it) {
+        const GroupOp op = group_op(g, it, steps, PH_UPDATE);
+        if (op == OP_UPD || op == OP_UPD_Q) cur ^= 1;
+    }
     return cur;
 }
 
@@ -671,14 +675,16 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 const bool gs = h->groups[ch.gi[sl]].gs != 0;
                 return which == 0 || (which == 1 && !gs) || (which == 2 && gs);
             };
-            auto upd_list = [&](int which, int32_t& o, int32_t& n) {
+            // square: the Gram-pair groups' tiles cover their m x m products (T = A P')
+            auto upd_list = [&](int which, bool square, int32_t& o, int32_t& n) {
                 std::vector<T> pr;
                 for (int sl = 0; sl < ch.ng; ++sl) {
                     if (!member(sl, which)) continue;
                     const Group& g = h->groups[ch.gi[sl]];
+                    const int cols = square && g.gs ? g.m : g.n;
                     for (int idx = 0; idx < g.count; ++idx)
                         for (int ti = 0; ti < g.m / 256; ++ti)
-                            for (int tj = 0; tj < g.n / 256; ++tj)
+                            for (int tj = 0; tj < cols / 256; ++tj)
                                 pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
                 }
                 emit(pr, o, n);
@@ -695,19 +701,13 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 }
                 emit(sg, o, n);
             };
-            upd_list(0, ch.pair_off, ch.pair_n);
+            upd_list(0, false, ch.pair_off, ch.pair_n);
             sym_list(0, ch.spg_off, ch.spg_n);
             bool any_gs = false;
             for (int sl = 0; sl < ch.ng; ++sl) any_gs = any_gs || member(sl, 2);
             if (any_gs) {
-                upd_list(1, ch.pair_std_off, ch.pair_std_n);
-                sym_list(1, ch.spg_std_off, ch.spg_std_n);
+                upd_list(0, true, ch.pair_t_off, ch.pair_t_n);
                 sym_list(2, ch.spg_gs_off, ch.spg_gs_n);
-            } else {
-                ch.pair_std_off = ch.pair_off;
-                ch.pair_std_n = ch.pair_n;
-                ch.spg_std_off = ch.spg_off;
-                ch.spg_std_n = ch.spg_n;
             }
         }
         h->chunks.push_back(ch);
@@ -788,6 +788,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
              encode_bf16_3d(enc, &g.map_p_mir, g.p16, g.m, g.m, g.count, g.lda, 64);
         if (ok && g.gs)
             ok = encode_bf16_3d(enc, &g.map_p_mn, g.p16, g.m, g.m, g.count, g.lda, 64) &&
+                 encode_bf16_3d(enc, &g.map_p_mn128, g.p16, g.m, g.m, g.count, g.lda, 128) &&
                  encode_bf16_3d(enc, &g.map_pb_k, g.pb16, g.m, g.m, g.count, g.lda, kBM) &&
                  encode_bf16_3d(enc, &g.map_t_k, g.t16, g.m, g.m, g.count, g.lda, kBM) &&
                  encode_3d(enc, &g.map_pb_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.pb16, g.m, g.m, g.count, g.lda,
@@ -876,9 +877,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 case OP_GRAM: fl = m * (m + 1) * n; by = 2 * m * n + 2 * m * m; break;
                 case OP_POLY:
                 case OP_POLY_B: fl = m * m * (m + 1); by = 4 * m * m; break;
-                case OP_PLAIN_T:
                 case OP_PLAIN_A:
                 case OP_PLAIN_Q: fl = m * m * (m + 1); by = 6 * m * m; break;
+                case OP_UPD_T: fl = 2 * m * m * m; by = 6 * m * m; break;  // the update kernel's full tiles
                 case OP_UPD: fl = 2 * m * m * n; by = 2 * m * m + (first ? 6 : 4) * m * n; break;
                 case OP_UPD_Q: fl = 2 * m * m * n; by = 2 * m * m + 4 * m * n; break;
                 default: break;
@@ -958,18 +959,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.opl16 = g.a16;
                                 G.opr16 = g.a16;
                                 break;
-                            case OP_PLAIN_T:  // T = A P'
-                                gp.map_a[sl] = g.map_a_k;
-                                gp.map_b[sl] = g.map_p_mn;
-                                gp.map_out[sl] = g.map_t_w32;
-                                G.out16 = g.t16;
-                                G.opl16 = g.a16;
-                                G.opr16 = g.p16;
-                                break;
-                            case OP_PLAIN_A:  // A <- T P'
+                            case OP_PLAIN_A:  // A <- T P', in the Gram launch
                                 gp.map_a[sl] = g.map_t_k;
                                 gp.map_b[sl] = g.map_p_mn;
                                 gp.map_out[sl] = g.map_a_w32;
+                                G.b_mn = 1;
                                 G.out16 = g.a16;
                                 G.opl16 = g.t16;
                                 G.opr16 = g.p16;
@@ -996,6 +990,14 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.opl16 = g.p16;
                                 G.opr16 = xin16;
                                 break;
+                            case OP_UPD_T:  // T = A P', full m x m tiles in the update launch
+                                gp.map_a[sl] = g.map_a_k;
+                                gp.map_b[sl] = g.map_p_mn128;
+                                gp.map_out[sl] = g.map_t_w32;
+                                G.x16_out = g.t16;
+                                G.opl16 = g.a16;
+                                G.opr16 = g.p16;
+                                break;
                             case OP_UPD_Q:  // X_{k+2} = Q X_k
                                 gp.map_a[sl] = g.map_t_k;
                                 gp.map_b[sl] = g.map_x_mn128[cb];
@@ -1008,9 +1010,16 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         }
                     }
                     if (n_in == 0) continue;
-                    // the tile list of the groups that take part
+                    // the tile list of the groups that take part: every group of the chunk, or the
+                    // Gram-pair groups alone (their own product Q)
                     const bool all_in = n_in == ch.ng;
-                    const bool std_only = n_in_gs == 0 && n_in == ch.ng - n_gs;
+                    bool has_t = false;
+                    for (int sl = 0; sl < ch.ng; ++sl) has_t = has_t || ops[sl] == OP_UPD_T;
+                    if (!all_in && !(n_in == n_gs && n_in_gs == n_gs)) {
+                        cudaFree(h->arena);
+                        delete h;
+                        return fail(nullptr, MUON_ERR_CUDA, "internal error: launch plan group set");
+                    }
                     const bool rev = (nlaunch[c]++ & 1) != 0;
                     auto pick = [&](int32_t off, int32_t n) {
                         gp.tiles = h->d_gemm_tiles + off + (rev ? n : 0);
@@ -1020,11 +1029,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                              : (ph == PH_POLY ? MODE_POLY : (ph == PH_UPDATE ? MODE_UPDATE : MODE_PLAIN));
                     if (pairs) {
                         if (mode == MODE_UPDATE)
-                            pick(all_in ? ch.pair_off : ch.pair_std_off, all_in ? ch.pair_n : ch.pair_std_n);
+                            pick(has_t ? ch.pair_t_off : ch.pair_off, has_t ? ch.pair_t_n : ch.pair_n);
                         else if (all_in)
                             pick(ch.spg_off, ch.spg_n);
-                        else if (std_only)
-                            pick(ch.spg_std_off, ch.spg_std_n);
                         else
                             pick(ch.spg_gs_off, ch.spg_gs_n);
                     } else {
@@ -1042,9 +1049,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     h->gparams.push_back(gp);
                 }
             }
-            // groups that updated now hold their iterate in the other buffer
-            for (size_t gi = 0; gi < h->groups.size(); ++gi)
-                if (group_op(h->groups[gi], it, steps, PH_UPDATE) != OP_NONE) cur[gi] = first ? 0 : cur[gi] ^ 1;
+            // groups that updated their iterate now hold it in the other buffer
+            for (size_t gi = 0; gi < h->groups.size(); ++gi) {
+                const GroupOp op = group_op(h->groups[gi], it, steps, PH_UPDATE);
+                if (op == OP_UPD || op == OP_UPD_Q) cur[gi] = first ? 0 : cur[gi] ^ 1;
+            }
         }
         for (size_t gi = 0; gi < h->groups.size(); ++gi)
             if (cur[gi] != h->groups[gi].final_buf) {

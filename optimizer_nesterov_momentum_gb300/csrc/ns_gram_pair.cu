@@ -9,8 +9,10 @@
 //                                      the diagonal: P' = a I + P)
 //   MODE_PLAIN  C = L R               (L, R symmetric polynomials in one Gram matrix,
 //                                      so they commute and C is symmetric: the
-//                                      Gram-space products T = A P', A = T P' and
-//                                      Q = P'' P')
+//                                      Gram-space product Q = P'' P')
+// A Gram launch may also carry plain products for some of its groups (GemmGroup.b_mn:
+// the Gram-space product A <- T P' rides along with the Gram matrices of the other
+// groups): those tiles take the plain product's operands and K.
 //
 // with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) issued by CTA 0 of a
 // two-CTA cluster.  A pair tile is the 256 x 256 block (I, J), J >= I, of the
@@ -71,8 +73,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     using C = SymPairCfg<MODE>;
     constexpr int STAGES = C::STAGES;
     // the polynomial's and the plain product's right operand is MN-major (columns of a
-    // symmetric matrix)
+    // symmetric matrix); a Gram launch's groups with b_mn set take the same layout
     constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/C::MNB, F16);
+    constexpr uint32_t IDESC_MN = make_idesc_16bit(256, 256, /*b_mn_major=*/true, F16);
     // the polynomial of the second and later iterations adds a to the diagonal of P
     constexpr bool FOLD = C::POLY && F16;
 
@@ -140,7 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
         if (lane == 0 && run) {
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_a[g]);
-                if (C::MNB) tma_prefetch_desc(&p.map_b[g]);
+                if (C::MNB || p.grp[g].b_mn) tma_prefetch_desc(&p.map_b[g]);
             }
             const uint32_t full0 = cluster_addr(&full[0], 0);
             int stage = 0;
@@ -152,9 +155,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
-                const int K = C::MNB ? p.grp[g].m : p.grp[g].n;
+                const bool mnb = C::MNB || p.grp[g].b_mn;
+                const int K = mnb ? p.grp[g].m : p.grp[g].n;
                 const int nkb = (K + kBK - 1) / kBK;
-                const bool diag = MODE == MODE_GRAM && ti == tj;  // a diagonal Gram tile stages one set of rows
+                const bool diag = !mnb && ti == tj;  // a diagonal Gram tile stages one set of rows
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
@@ -164,7 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     const uint32_t bar = full0 + (uint32_t)(stage * 8);
                     uint8_t* dst = sS + stage * kSymStage;
                     tma_load_3d_pair(dst, &p.map_a[g], bar, kb * kBK, ti * 256 + (int)rank * kBM, idx);
-                    if (C::MNB) {
+                    if (mnb) {
                         // columns 256 J + 128 r .. + 127 of the right operand for k-block rows kb:
                         // two 64-column boxes
                         const int col = tj * 256 + (int)rank * 128;
@@ -195,9 +199,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             for (int t = pr; t < p.ntiles && ok; t += npairs) {
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
-                const int K = C::MNB ? p.grp[tile.x].m : p.grp[tile.x].n;
+                const bool mnb = C::MNB || p.grp[tile.x].b_mn;
+                const int K = mnb ? p.grp[tile.x].m : p.grp[tile.x].n;
                 const int nkb = (K + kBK - 1) / kBK;
-                const bool diag = MODE == MODE_GRAM && tile.z == tile.w;
+                const bool diag = !mnb && tile.z == tile.w;
+                const uint32_t idesc = mnb ? IDESC_MN : IDESC;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -231,12 +237,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                             // (16-byte units): 32 bytes along a K-major operand, 16 rows of 128 bytes
                             // along an MN-major one (8 KB between its 64-column boxes)
                             const uint64_t ad = make_sdesc_sw128(a_st, 16, 1024);
-                            const uint64_t bd = C::MNB ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
-                                                       : make_sdesc_sw128(b_st, 16, 1024);
-                            constexpr uint64_t b_step = C::MNB ? 128 : 2;
+                            const uint64_t bd = mnb ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
+                                                    : make_sdesc_sw128(b_st, 16, 1024);
+                            const uint64_t b_step = mnb ? 128 : 2;
 #pragma unroll
                             for (int kk = 0; kk < kBK / 16; ++kk)
-                                umma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + b_step * (uint64_t)kk, IDESC,
+                                umma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + b_step * (uint64_t)kk, idesc,
                                               (kb | h | kk) != 0 ? 1u : 0u);
                             any = true;
                             umma_commit_pair(&empty[st]);

@@ -39,10 +39,10 @@ def test_gram_pairs_match_the_oracle(kind, ns_steps):
     errs, opt, _ = run_parity(SHAPES, params, [grads], ns_steps=ns_steps, lr=0.03, opt=opt)
     errs.assert_within()
     work = opt.stage_work()
-    # the wide groups take the Gram-pair order: a pair launches T = A P' and A <- T P' in its
-    # first half and Q = P'' P' in its second
+    # the wide groups take the Gram-pair order: a pair adds one launch of its own (Q = P'' P');
+    # T = A P' and A <- T P' ride along with the update and Gram launches
     pairs = (ns_steps - 1) // 2
-    assert work["product"][2] == 3 * pairs, work
+    assert work["product"][2] == pairs, work
     opt.close()
 
 
@@ -77,13 +77,14 @@ def test_gram_pairs_launch_plan():
     assert ws["gram"][0] == 5 * (m * (m + 1) * n + m * (m + 1) * m)
     assert ws["update"][0] == 5 * (2 * m * m * n + 2 * m * m * m)
     # Gram pairs (five iterations: one plain, two pairs): the wide matrix forms three Gram
-    # matrices and three updates, and six m x m products
-    assert wg["gram"][0] == 3 * m * (m + 1) * n + 5 * m * (m + 1) * m
-    assert wg["update"][0] == 3 * 2 * m * m * n + 5 * 2 * m * m * m
-    assert wg["product"][0] == 6 * m * m * (m + 1)
+    # matrices and three updates; per pair A <- T P' runs in a Gram launch (symmetric, m^2(m+1)),
+    # T = A P' in an update launch (full tiles, 2 m^3) and Q = P'' P' in a launch of its own
+    assert wg["gram"][0] == 3 * m * (m + 1) * n + 5 * m * (m + 1) * m + 2 * m * m * (m + 1)
+    assert wg["update"][0] == 3 * 2 * m * m * n + 5 * 2 * m * m * m + 2 * 2 * m * m * m
+    assert wg["product"][0] == 2 * m * m * (m + 1)
     assert wg["poly"][0] == ws["poly"][0]
     # the square matrix keeps its Gram and update launches in every iteration, so the pairs
-    # only add their product launches
-    assert gp.launch_count() == std.launch_count() + 6
+    # only add their Q launches
+    assert gp.launch_count() == std.launch_count() + 2
     std.close()
     gp.close()
