@@ -319,7 +319,7 @@ def run_ours(args):
     bank = [[g.to(dev) for g in grads_for(wl, k, device=str(dev))] for k in range(nbank)]
     grad_bytes = 2 if wl.grad_dtype == "bf16" else 4
     opt = Muon(specs, lr=wl.lr, momentum=wl.momentum, beta2=wl.beta2, weight_decay=wl.weight_decay,
-               ns_steps=wl.ns_steps, normuon=wl.normuon, grad_dtype=wl.grad_dtype)
+               ns_steps=wl.ns_steps, normuon=wl.normuon, grad_dtype=wl.grad_dtype, ns_form=args.ns_form)
     launches = opt.launch_count()
     model = work_model(wl, grad_bytes)
 
@@ -505,15 +505,21 @@ def run_ours(args):
     kern["apply"] = {"ms": stage_ms["apply"], "bound": "hbm",
                      "achieved": model["apply_bytes"] / (stage_ms["apply"] * 1e-3) / 1e9, "unit": "GB/s",
                      "algorithmic_per_launch": model["apply_bytes"]}
-    for name in ("gram", "poly", "update"):
+    # the Newton-Schulz stages' work as the library planned it (the Gram-pair order moves
+    # m x m products into the Gram and update launches and adds a product stage)
+    planned = opt.stage_work()
+    for name in ("gram", "poly", "update", "product"):
         # a product is bound by whichever of its flops (at the tensor peak) and its
         # HBM bytes (at the copy peak) takes longer; both fractions are reported
-        per_launch_ms = stage_ms[name] / nsi
-        flops, nbytes = model[f"{name}_flops"], model[f"{name}_bytes"]
+        fl_step, by_step, n_launch = planned[name]
+        if n_launch == 0:
+            continue
+        per_launch_ms = stage_ms[name] / n_launch
+        flops, nbytes = fl_step / n_launch, by_step / n_launch
         tflops = flops / (per_launch_ms * 1e-3) / 1e12
         gbs = nbytes / (per_launch_ms * 1e-3) / 1e9
         hbm_bound = nbytes / hbm > flops / 1e3 / tc_peak
-        kern[name] = {"ms": stage_ms[name], "ms_per_launch": per_launch_ms,
+        kern[name] = {"ms": stage_ms[name], "ms_per_launch": per_launch_ms, "launches": n_launch,
                       "bound": "hbm" if hbm_bound else "tensor",
                       "achieved": gbs if hbm_bound else tflops, "unit": "GB/s" if hbm_bound else "TFLOP/s",
                       "algorithmic_per_launch": nbytes if hbm_bound else flops,
@@ -526,10 +532,12 @@ def run_ours(args):
         if "achieved" in v:
             v["peak"] = hbm if v["unit"] == "GB/s" else tc_peak
             v["frac"] = v["achieved"] / v["peak"]
-    ns_ms = stage_ms["gram"] + stage_ms["poly"] + stage_ms["update"]
-    ns_tflops = model["ns_flops"] / (ns_ms * 1e-3) / 1e12
+    ns_ms = stage_ms["gram"] + stage_ms["poly"] + stage_ms["update"] + stage_ms.get("product", 0.0)
+    ns_flops_exec = sum(planned[k][0] for k in ("gram", "poly", "update", "product"))
+    ns_tflops = ns_flops_exec / (ns_ms * 1e-3) / 1e12
     total_stage = sum(stage_ms.values())
-    dom = max(("momentum", "apply", "gram", "poly", "update"), key=lambda k: kern[k]["ms"])
+    dom = max((k for k in ("momentum", "apply", "gram", "poly", "update", "product") if k in kern),
+              key=lambda k: kern[k]["ms"])
     # DRAM traffic per launch of the dominant kernel, from the single-pass ncu capture summarised in
     # profiles/dram_traffic_<workload>.md (a line "traffic_bytes_per_launch <stage> <bytes>")
     traffic = None
@@ -572,10 +580,17 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (grads+params+momentum "
                        f"{(model['elems'] * (grad_bytes + 8)) / 1e6:.0f} MB > 129 MB)",
                        "parallelism": "replicas" if world > 1 else "single"},
-            "ns": {"tflops_algorithmic": ns_tflops, "frac_of_bf16_peak": ns_tflops / tc_peak,
+            "ns": {"order": args.ns_form,
+                   "tflops_algorithmic": ns_tflops, "flops_algorithmic": ns_flops_exec,
+                   "frac_of_bf16_peak": ns_tflops / tc_peak,
                    "frac_of_burst": ns_tflops / tc_burst, "frac_of_sustained": ns_tflops / tc_sustained,
+                   "flops_standard_order": model["ns_flops"],
+                   "tflops_standard_order_equivalent": model["ns_flops"] / (ns_ms * 1e-3) / 1e12,
                    "tflops_dense_equivalent": model["ns_flops_dense"] / (ns_ms * 1e-3) / 1e12,
-                   "ms": ns_ms, "peak_tflops": tc_peak, "peak_source": f"{peak_src} ({tc_key})"},
+                   "ms": ns_ms, "peak_tflops": tc_peak, "peak_source": f"{peak_src} ({tc_key})",
+                   "note": "tflops_algorithmic: the products the step runs (symmetric ones counted once per "
+                           "upper-triangle element); the *_equivalent rates divide the standard order's work "
+                           "by the same time"},
             "eager_ms_per_step": eager_ms,
             "kernels": kern,
             "roofline": roofline,
@@ -606,6 +621,8 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-group measurement")
+    ap.add_argument("--ns-form", default="gram_pairs", choices=["gram_pairs", "standard"],
+                    help="order of the Newton-Schulz products (muon_config.ns_form)")
     ap.add_argument("--ref-budget", type=float, default=150.0,
                     help="seconds the reference arm (the fp64 oracle) may spend on warm-up + timed steps")
     args = ap.parse_args()
