@@ -542,7 +542,8 @@ def run_ours(args):
     # profiles/dram_traffic_<workload>.md (a line "traffic_bytes_per_launch <stage> <bytes>")
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", f"dram_traffic_{wl.name}.md")
-    if os.path.exists(tr_path):
+    # the capture was taken in the default (Gram-pair) order; another order's launches differ
+    if os.path.exists(tr_path) and args.ns_form == "gram_pairs":
         with open(tr_path) as f:
             for line in f:
                 parts = line.split()
