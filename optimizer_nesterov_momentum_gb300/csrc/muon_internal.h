@@ -58,9 +58,7 @@ constexpr int kStatusFatal = STATUS_TIMEOUT | STATUS_PAIR;
 // NorMuon lanes (muon_config.normuon_lanes)
 enum { LANES_SHORT_SIDE = 0, LANES_ROWS = 1, LANES_COLS = 2 };
 
-// MODE_PLAIN: C = L R of two symmetric m x m matrices that commute (polynomials in one
-// Gram matrix), so C is symmetric: the products of the Gram-space iterations.
-enum GemmMode { MODE_GRAM = 0, MODE_POLY = 1, MODE_UPDATE = 2, MODE_PLAIN = 3 };
+enum GemmMode { MODE_GRAM = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
 
 struct SubDesc {
     // caller-side addressing (original orientation, rows x cols)

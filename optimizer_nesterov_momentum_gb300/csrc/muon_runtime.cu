@@ -110,11 +110,11 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     int32_t upd_off = 0, upd_n = 0;
     int32_t pair_off = 0, pair_n = 0;  // 256 x 256 update tiles for SM pairs (0: chunk not eligible)
     int32_t spg_off = 0, spg_n = 0;    // 256 x 256 Gram tiles (J >= I) for SM pairs
-    // Gram-pair chunks: the symmetric tiles of the Gram-pair groups alone, and the update
-    // tiles of the standard-form groups together with the full m x m tiles of the Gram-pair
-    // groups (the first half of a pair computes T = A P' in the update launch)
-    int32_t spg_gs_off = 0, spg_gs_n = 0;
+    // Gram-pair chunks: the update tiles of the standard-form groups together with the full
+    // m x m tiles of the Gram-pair groups (the first half of a pair computes T = A P' in the
+    // update launch), and the full m x m tiles of the Gram-pair groups alone (Q = P'' P')
     int32_t pair_t_off = 0, pair_t_n = 0;
+    int32_t pair_q_off = 0, pair_q_n = 0;
 };
 
 // One Newton-Schulz launch of the step, in order.
@@ -285,11 +285,15 @@ cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* gra
 // with A_k = X_k X_k^T and P'_k a polynomial in A_k, X_{k+1} = P'_k X_k gives
 // A_{k+1} = P'_k A_k P'_k = (A_k P'_k) P'_k and X_{k+2} = (P'_{k+1} P'_k) X_k, so a pair
 // of iterations forms one Gram matrix and one update instead of two of each, for three
-// m x m products.  The products ride along with launches the other groups make anyway:
+// m x m products.  Two of them ride along with launches the other groups make anyway:
 // T = A_k P'_k with the first half's updates (on the update kernel, full m x m tiles),
-// A_{k+1} = T P'_k with the second half's Gram matrices; only Q = P'_{k+1} P'_k has a
-// launch of its own.  A single iteration left at the end runs in the standard form.
-enum GroupOp { OP_NONE, OP_GRAM, OP_POLY, OP_POLY_B, OP_PLAIN_A, OP_PLAIN_Q, OP_UPD, OP_UPD_T, OP_UPD_Q };
+// A_{k+1} = T P'_k with the second half's Gram matrices (symmetric tiles).  Q =
+// P'_{k+1} P'_k has a launch of its own on the update kernel: it is symmetric only in
+// exact arithmetic (the computed P' and P'' commute up to rounding), and storing its
+// upper triangle mirrored measurably raised the error of the output, where the full
+// product keeps it at the standard form's level.  A single iteration left at the end
+// runs in the standard form.
+enum GroupOp { OP_NONE, OP_GRAM, OP_POLY, OP_POLY_B, OP_PLAIN_A, OP_PROD_Q, OP_UPD, OP_UPD_T, OP_UPD_Q };
 enum Phase { PH_GRAM, PH_POLY, PH_PLAIN, PH_UPDATE, PH_COUNT };
 
 GroupOp group_op(const Group& g, int it, int steps, int phase) {
@@ -301,7 +305,7 @@ GroupOp group_op(const Group& g, int it, int steps, int phase) {
     switch (phase) {
         case PH_GRAM: return kind == 2 ? OP_PLAIN_A : OP_GRAM;
         case PH_POLY: return kind == 2 ? OP_POLY_B : OP_POLY;
-        case PH_PLAIN: return kind == 2 ? OP_PLAIN_Q : OP_NONE;
+        case PH_PLAIN: return kind == 2 ? OP_PROD_Q : OP_NONE;
         default: return kind == 1 ? OP_UPD_T : (kind == 2 ? OP_UPD_Q : OP_UPD);
     }
 }
@@ -707,7 +711,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             for (int sl = 0; sl < ch.ng; ++sl) any_gs = any_gs || member(sl, 2);
             if (any_gs) {
                 upd_list(0, true, ch.pair_t_off, ch.pair_t_n);
-                sym_list(2, ch.spg_gs_off, ch.spg_gs_n);
+                upd_list(2, true, ch.pair_q_off, ch.pair_q_n);
             }
         }
         h->chunks.push_back(ch);
@@ -877,9 +881,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 case OP_GRAM: fl = m * (m + 1) * n; by = 2 * m * n + 2 * m * m; break;
                 case OP_POLY:
                 case OP_POLY_B: fl = m * m * (m + 1); by = 4 * m * m; break;
-                case OP_PLAIN_A:
-                case OP_PLAIN_Q: fl = m * m * (m + 1); by = 6 * m * m; break;
-                case OP_UPD_T: fl = 2 * m * m * m; by = 6 * m * m; break;  // the update kernel's full tiles
+                case OP_PLAIN_A: fl = m * m * (m + 1); by = 6 * m * m; break;
+                case OP_UPD_T:
+                case OP_PROD_Q: fl = 2 * m * m * m; by = 6 * m * m; break;  // the update kernel's full tiles
                 case OP_UPD: fl = 2 * m * m * n; by = 2 * m * m + (first ? 6 : 4) * m * n; break;
                 case OP_UPD_Q: fl = 2 * m * m * n; by = 2 * m * m + 4 * m * n; break;
                 default: break;
@@ -968,11 +972,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.opl16 = g.t16;
                                 G.opr16 = g.p16;
                                 break;
-                            case OP_PLAIN_Q:  // Q = P'' P' (into T's buffer)
+                            case OP_PROD_Q:  // Q = P'' P', full m x m tiles on the update kernel (into T's buffer)
                                 gp.map_a[sl] = g.map_pb_k;
-                                gp.map_b[sl] = g.map_p_mn;
+                                gp.map_b[sl] = g.map_p_mn128;
                                 gp.map_out[sl] = g.map_t_w32;
-                                G.out16 = g.t16;
+                                G.x16_out = g.t16;
                                 G.opl16 = g.pb16;
                                 G.opr16 = g.p16;
                                 break;
@@ -1025,23 +1029,23 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         gp.tiles = h->d_gemm_tiles + off + (rev ? n : 0);
                         gp.ntiles = n;
                     };
-                    int mode = ph == PH_GRAM ? MODE_GRAM
-                                             : (ph == PH_POLY ? MODE_POLY : (ph == PH_UPDATE ? MODE_UPDATE : MODE_PLAIN));
+                    // the Gram-pair product Q runs on the update kernel
+                    int mode = ph == PH_GRAM ? MODE_GRAM : (ph == PH_POLY ? MODE_POLY : MODE_UPDATE);
                     if (pairs) {
-                        if (mode == MODE_UPDATE)
+                        if (ph == PH_PLAIN)
+                            pick(ch.pair_q_off, ch.pair_q_n);
+                        else if (mode == MODE_UPDATE)
                             pick(has_t ? ch.pair_t_off : ch.pair_off, has_t ? ch.pair_t_n : ch.pair_n);
-                        else if (all_in)
-                            pick(ch.spg_off, ch.spg_n);
                         else
-                            pick(ch.spg_gs_off, ch.spg_gs_n);
+                            pick(ch.spg_off, ch.spg_n);
                     } else {
                         pick(mode == MODE_GRAM ? ch.gram_off : (mode == MODE_POLY ? ch.poly_off : ch.upd_off),
                              mode == MODE_GRAM ? ch.gram_n : (mode == MODE_POLY ? ch.poly_n : ch.upd_n));
                     }
-                    const int stage = mode == MODE_GRAM ? MUON_STAGE_GRAM
-                                                        : (mode == MODE_POLY ? MUON_STAGE_POLY
-                                                                             : (mode == MODE_UPDATE ? MUON_STAGE_UPDATE
-                                                                                                    : MUON_STAGE_PRODUCT));
+                    const int stage = ph == PH_PLAIN ? MUON_STAGE_PRODUCT
+                                                     : (mode == MODE_GRAM ? MUON_STAGE_GRAM
+                                                                          : (mode == MODE_POLY ? MUON_STAGE_POLY
+                                                                                               : MUON_STAGE_UPDATE));
                     for (int sl = 0; sl < ch.ng; ++sl)
                         if (ops[sl] != OP_NONE) add_work(stage, h->groups[ch.gi[sl]], ops[sl], first);
                     h->work_launches[stage]++;
@@ -1132,7 +1136,6 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
                                : (f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
                                       : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s));
                     break;
-                case MODE_PLAIN: e = launch_ns_sym_pair<MODE_PLAIN, true>(gp, h->num_sms, s); break;
                 default:
                     e = L.pair ? launch_ns_update_pair(gp, !f16, h->num_sms, s)
                                : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)

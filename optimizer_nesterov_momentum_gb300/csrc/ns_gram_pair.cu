@@ -7,12 +7,10 @@
 //                                      as the Gram with A's rows for X's; from the
 //                                      second iteration on the epilogue adds a to
 //                                      the diagonal: P' = a I + P)
-//   MODE_PLAIN  C = L R               (L, R symmetric polynomials in one Gram matrix,
-//                                      so they commute and C is symmetric: the
-//                                      Gram-space product Q = P'' P')
-// A Gram launch may also carry plain products for some of its groups (GemmGroup.b_mn:
-// the Gram-space product A <- T P' rides along with the Gram matrices of the other
-// groups): those tiles take the plain product's operands and K.
+// A Gram launch may also carry plain products C = L R for some of its groups
+// (GemmGroup.b_mn: L and R symmetric polynomials in one Gram matrix, so they commute and
+// C is symmetric; the Gram-space product A <- T P' rides along with the Gram matrices of
+// the other groups): those tiles take an MN-major right operand and K = m.
 //
 // with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) issued by CTA 0 of a
 // two-CTA cluster.  A pair tile is the 256 x 256 block (I, J), J >= I, of the
@@ -55,7 +53,7 @@ constexpr int kOutSlots = 2;  // per warp: blocks and mirrors in flight
 template <int MODE>
 struct SymPairCfg {
     static constexpr bool POLY = MODE == MODE_POLY;
-    static constexpr bool MNB = MODE != MODE_GRAM;  // right operand MN-major (columns of a symmetric matrix)
+    static constexpr bool MNB = MODE == MODE_POLY;  // right operand MN-major (columns of a symmetric matrix)
     // the polynomial gives up one stage for its per-warp input ring (two 32 x 32 blocks of A)
     static constexpr int STAGES = POLY ? 5 : 6;
     static constexpr int IN_SLOTS = POLY ? 2 : 0;
@@ -72,8 +70,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     k_ns_sym_pair(const __grid_constant__ GemmParams p) {
     using C = SymPairCfg<MODE>;
     constexpr int STAGES = C::STAGES;
-    // the polynomial's and the plain product's right operand is MN-major (columns of a
-    // symmetric matrix); a Gram launch's groups with b_mn set take the same layout
+    // the polynomial's right operand is MN-major (columns of the symmetric A); a Gram
+    // launch's groups with b_mn set take the same layout
     constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/C::MNB, F16);
     constexpr uint32_t IDESC_MN = make_idesc_16bit(256, 256, /*b_mn_major=*/true, F16);
     // the polynomial of the second and later iterations adds a to the diagonal of P
@@ -456,15 +454,14 @@ cudaError_t ns_gram_pair_configure() {
     if (e == cudaSuccess) e = configure_sym<MODE_GRAM, true>();
     if (e == cudaSuccess) e = configure_sym<MODE_POLY, false>();
     if (e == cudaSuccess) e = configure_sym<MODE_POLY, true>();
-    if (e == cudaSuccess) e = configure_sym<MODE_PLAIN, true>();
     return e;
 }
 
 // p.tiles: 256 x 256 tiles {group slot, index, tile row I, tile column J >= I} (units of 256).
 // MODE_GRAM: p.map_a = 128-row boxes of the iterate (K = n); MODE_POLY: of A (K = m), with
 // p.map_b = A's 64 x 64 boxes (the MN-major right operand) and p.map_ein = A's 32 x 32 boxes
-// for the b A term; MODE_PLAIN: p.map_a = 128-row boxes of L, p.map_b = 64 x 64 boxes of R
-// (K = m).  p.map_out: 32 x 32 boxes of the result.
+// for the b A term; groups with b_mn set: p.map_a = 128-row boxes of L, p.map_b = 64 x 64
+// boxes of R (K = m).  p.map_out: 32 x 32 boxes of the result.
 template <int MODE, bool F16>
 cudaError_t launch_ns_sym_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
@@ -477,6 +474,5 @@ template cudaError_t launch_ns_sym_pair<MODE_GRAM, false>(const GemmParams&, int
 template cudaError_t launch_ns_sym_pair<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_ns_sym_pair<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_ns_sym_pair<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_PLAIN, true>(const GemmParams&, int, cudaStream_t);
 
 }  // namespace muon

@@ -79,9 +79,10 @@ def test_gram_pairs_launch_plan():
     # Gram pairs (five iterations: one plain, two pairs): the wide matrix forms three Gram
     # matrices and three updates; per pair A <- T P' runs in a Gram launch (symmetric, m^2(m+1)),
     # T = A P' in an update launch (full tiles, 2 m^3) and Q = P'' P' in a launch of its own
+    # (full tiles on the update kernel)
     assert wg["gram"][0] == 3 * m * (m + 1) * n + 5 * m * (m + 1) * m + 2 * m * m * (m + 1)
     assert wg["update"][0] == 3 * 2 * m * m * n + 5 * 2 * m * m * m + 2 * 2 * m * m * m
-    assert wg["product"][0] == 2 * m * m * (m + 1)
+    assert wg["product"][0] == 2 * 2 * m * m * m  # Q as a full product (update kernel)
     assert wg["poly"][0] == ws["poly"][0]
     # the square matrix keeps its Gram and update launches in every iteration, so the pairs
     # only add their Q launches
