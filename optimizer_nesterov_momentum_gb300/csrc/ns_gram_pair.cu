@@ -324,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     if (c == 2) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
+                        if (lane == 0) mbar_arrive_cluster_relaxed(tempty0 + (uint32_t)(acc * 8));
                     }
                 }
                 const int col0 = tj * 256 + c * 64 + half * 32;  // this block's first column

@@ -304,7 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     if (c + LB == 4) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * 8));
+                        if (lane == 0) mbar_arrive_cluster_relaxed(tempty0 + (uint32_t)(acc * 8));
                     }
                 }
                 const uint32_t* r32 = raw[c % LB];

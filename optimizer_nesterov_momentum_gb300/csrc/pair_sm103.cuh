@@ -37,8 +37,15 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+// Arrive on an mbarrier of either CTA of the pair (`addr` is a cluster address), without
+// release semantics.  For signals that publish no memory writes: a TMEM accumulator
+// drained by tcgen05.ld, whose completion the caller has waited for (tcgen05.wait::ld)
+// and ordered with tcgen05.fence::before_thread_sync.  A release at cluster scope would
+// make the arrive wait for the SM's outstanding memory traffic, in-flight tensor copies
+// included: one such arrive per 32 KB stage cut the copies' throughput from 138 to 48
+// GB/s per SM in a probe; the relaxed form left it at 138.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 // Tensor copy into this CTA's shared memory whose completion is counted on an
