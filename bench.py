@@ -460,30 +460,36 @@ def run_ours(args):
             dgr_flat[slot].copy_(host_grads[k % nbank], non_blocking=True)
             in_done[slot].record(s_in)
 
-    torch.cuda.synchronize()
-    barrier()
-    start.record(main)
-    copy_in(0)
-    for k in range(args.steps):
-        slot = k % 2
-        if k + 1 < args.steps:
-            copy_in(k + 1)
-        main.wait_event(in_done[slot])
-        opt.step(e2e_params, dgr[slot], stream=main)
-        if k >= 2:
-            main.wait_event(out_done[slot])  # the copy-out of step k - 2 is done with this snapshot
-        snap[slot].copy_(pflat, non_blocking=True)
-        step_done[slot].record(main)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(step_done[slot])
-            host_params.copy_(snap[slot], non_blocking=True)
-            out_done[slot].record(s_out)
-    main.wait_stream(s_in)
-    main.wait_stream(s_out)
-    end.record(main)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(start.elapsed_time(end) / args.steps)
+    def pipelined_pass():
+        torch.cuda.synchronize()
+        barrier()
+        start.record(main)
+        copy_in(0)
+        for k in range(args.steps):
+            slot = k % 2
+            if k + 1 < args.steps:
+                copy_in(k + 1)
+            main.wait_event(in_done[slot])
+            opt.step(e2e_params, dgr[slot], stream=main)
+            if k >= 2:
+                main.wait_event(out_done[slot])  # the copy-out of step k - 2 is done with this snapshot
+            snap[slot].copy_(pflat, non_blocking=True)
+            step_done[slot].record(main)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(step_done[slot])
+                host_params.copy_(snap[slot], non_blocking=True)
+                out_done[slot].record(s_out)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+        end.record(main)
+        torch.cuda.synchronize()
+        barrier()
+        return max_over_ranks(start.elapsed_time(end) / args.steps)
+
+    # the host link's rate varies from run to run (other tenants of the machine share it):
+    # three passes, the median reported, all three listed
+    e2e_passes = [pipelined_pass() for _ in range(3)]
+    e2e_ms = statistics.median(e2e_passes)
     opt.sync_status()
 
     # ---- roofline of each stage.  The tensor peak is the burst figure when the clock record
@@ -598,10 +604,10 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "step_ms_stats": step_stats,
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "pipelined": True, "serial_ms": e2e_serial_ms,
+                    "pipelined": True, "passes_ms": e2e_passes, "serial_ms": e2e_serial_ms,
                     "note": "gradients copied in from pinned host memory and parameters read back every step; "
                             "copies of neighbouring steps overlap the step on two copy streams; one flat "
-                            "buffer per direction (three copies per step)"},
+                            "buffer per direction (three copies per step); median of three timed passes"},
             "gpu_launches": launches * args.steps,
             "clocks": clocks,
             "next_rows": {"adam": adam},
