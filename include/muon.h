@@ -143,12 +143,18 @@ typedef struct {
                               for (3.4445, -4.7750, 2.0315) every iteration; copied */
     int32_t normuon_lanes; /* MUON_LANES_*: the second moment's lanes (NorMuon only) */
     int32_t ns_form;       /* MUON_NS_*: order of the Newton-Schulz products */
+    int32_t launch_overlap;/* 1: every launch of a step after its first may begin while the previous
+                              kernel finishes (programmatic dependent launch: the next kernel's CTAs
+                              take the SMs the previous one no longer fills, set up their shared
+                              memory and tensor memory, and wait in the kernel for its results);
+                              0: plain stream order.  Results are identical either way. */
 } muon_config;
 
 /* Fills *cfg with: lr 0.02, momentum 0.95, beta2 0.95, weight_decay 0, ns_steps 5,
  * nesterov 1, lerp_form 1, normuon 1, norm_preserve 1, grad_dtype BF16,
  * gemm_engine TCGEN05, NULL arrays, normuon_lanes MUON_LANES_SHORT_SIDE,
- * ns_form MUON_NS_GRAM_PAIRS.  Layout: 80 bytes, ns_form at offset 76. */
+ * ns_form MUON_NS_GRAM_PAIRS, launch_overlap 1.  Layout: 88 bytes (84 used), ns_form at
+ * offset 76, launch_overlap at offset 80. */
 void muon_config_default(muon_config* cfg);
 
 /* Builds the execution plan for `n_mats` matrices on CUDA device `device`:

@@ -72,13 +72,16 @@ class Muon:
     ``ns_form`` is "gram_pairs" (default: wide matrices take the Newton-Schulz
     iterations after the first two at a time in Gram space) or "standard" (every
     iteration as the write-ups order it; see MUON_NS_* in include/muon.h).
+    ``launch_overlap`` (default True) lets each launch of a step after the first
+    begin while the previous kernel finishes (``muon_config.launch_overlap``).
     """
 
     def __init__(self, specs: Sequence, *, lr: float = 0.02, momentum: float = 0.95, beta2: float = 0.95,
                  weight_decay: float = 0.0, ns_steps: int = 5, nesterov: bool = True, lerp_form: bool = True,
                  normuon: bool = True, norm_preserve: bool = True, grad_dtype: str = "bf16",
                  gemm_engine: str = "tcgen05", ns_coeffs: Optional[Sequence[Sequence[float]]] = None,
-                 normuon_lanes: str = "short_side", ns_form: str = "gram_pairs", device: Optional[int] = None):
+                 normuon_lanes: str = "short_side", ns_form: str = "gram_pairs", launch_overlap: bool = True,
+                 device: Optional[int] = None):
         import torch
 
         self.specs = [s if isinstance(s, MatrixSpec) else MatrixSpec(*s) for s in specs]
@@ -96,6 +99,7 @@ class Muon:
         cfg.normuon_lanes = {"short_side": MUON_LANES_SHORT_SIDE, "rows": MUON_LANES_ROWS,
                              "cols": MUON_LANES_COLS}[normuon_lanes]
         cfg.ns_form = {"standard": MUON_NS_STANDARD, "gram_pairs": MUON_NS_GRAM_PAIRS}[ns_form]
+        cfg.launch_overlap = int(bool(launch_overlap))
         n = len(self.specs)
         self._lr_mul = (ctypes.c_float * n)(*[s.lr_mul for s in self.specs])
         self._wd_mul = (ctypes.c_float * n)(*[s.wd_mul for s in self.specs])

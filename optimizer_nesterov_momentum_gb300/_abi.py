@@ -134,6 +134,7 @@ class muon_config(ctypes.Structure):
         ("ns_coeffs", POINTER(c_float)),
         ("normuon_lanes", c_int32),
         ("ns_form", c_int32),
+        ("launch_overlap", c_int32),
     ]
 
 

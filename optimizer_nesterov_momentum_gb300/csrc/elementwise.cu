@@ -145,10 +145,13 @@ template <int CAP, bool GRAD_F32>
 __global__ void __launch_bounds__(256, 6) k_momentum(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float su[kTile][kTile + 1];
     __shared__ float red[8];
-    // the status word is loaded alongside the tile and descriptor loads and tested after them
-    const int fatal = *p.status & kStatusFatal;
+    // the tile list and the descriptors are written once, at create: they are read before the
+    // wait for the previous kernel; the status word after it
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
+    grid_dep_wait();
+    grid_dep_launch();
+    const int fatal = *p.status & kStatusFatal;
     if (fatal) return;  // an earlier step failed: leave the momentum as it is (uniform over the block)
     const int r0 = tile.y, c0 = tile.z;
     const float mu = p.hp[HP_MU];
@@ -223,6 +226,8 @@ __global__ void __launch_bounds__(256, 6) k_momentum(const __grid_constant__ Ele
 __global__ void __launch_bounds__(256) k_norm_scale(const __grid_constant__ NormParams p) {
     __shared__ float red[8];
     const SubDesc& d = p.subs[blockIdx.x];
+    grid_dep_wait();
+    grid_dep_launch();
     float s = 0.f;
     for (int t = threadIdx.x; t < d.k1_ntiles; t += 256) s += p.norm_part[d.k1_tile0 + t];
     const float total = block_sum_256(s, red);
@@ -244,6 +249,8 @@ __global__ void __launch_bounds__(256) k_norm_scale(const __grid_constant__ Norm
 __global__ void __launch_bounds__(256) k_col_sumsq(const __grid_constant__ ColSumParams p) {
     const int2 w = p.work[blockIdx.x];
     const SubDesc& d = p.subs[w.x];
+    grid_dep_wait();
+    grid_dep_launch();
     const int r0 = w.y * kTile, r1 = min(r0 + kTile, d.m);
     float* out = d.colsq + (int64_t)w.y * d.n;
     for (int j0 = threadIdx.x * 8; j0 < d.n; j0 += 256 * 8) {
@@ -275,6 +282,8 @@ constexpr int kLaneThreads = 1024;  // one block per matrix, one thread per lane
 __global__ void __launch_bounds__(kLaneThreads) k_lane_stats(const __grid_constant__ LaneParams p) {
     __shared__ float red[32];
     const SubDesc& d = p.subs[blockIdx.x];
+    grid_dep_wait();
+    grid_dep_launch();
     // a failed step (fatal status) or a non-finite direction: the second moment stays as it is
     if ((*p.status & kStatusFatal) || *d.skip) return;
     const float eff = p.hp[HP_LR] * d.lr_mul;
@@ -321,13 +330,16 @@ template <int CAP>
 __global__ void __launch_bounds__(256, 5) k_apply(const __grid_constant__ ElemParams<CAP> p) {
     __shared__ float so[kTile][kTile + 1];
     // Everything a block needs before its data loads sits on a chain of dependent loads
-    // (tile -> matrix descriptor -> parameter pointer); the status word, the hyper-parameters
-    // and the skip flag are loaded alongside, and tested only once the data loads are in
-    // flight, so they add no latency of their own.
-    const int fatal = *p.status & kStatusFatal;  // a Newton-Schulz launch failed: keep the parameters
-    const float lr = p.hp[HP_LR], wd = p.hp[HP_WD];
+    // (tile -> matrix descriptor -> parameter pointer).  The tile list and the descriptors are
+    // written once, at create, so they are read before the wait for the previous kernel.  The
+    // status word, the hyper-parameters and the skip flag are loaded alongside the data, and
+    // tested only once the data loads are in flight, so they add no latency of their own.
     const int4 tile = p.tiles[blockIdx.x];
     const SubDesc d = p.subs[tile.x];
+    grid_dep_wait();
+    grid_dep_launch();
+    const int fatal = *p.status & kStatusFatal;  // a Newton-Schulz launch failed: keep the parameters
+    const float lr = p.hp[HP_LR], wd = p.hp[HP_WD];
     const int r0 = tile.y, c0 = tile.z;
     const int tr = threadIdx.x >> 3, tc = threadIdx.x & 7;
     float* P = p.ptr.param[d.parent] + d.grad_off;
@@ -477,39 +489,33 @@ __global__ void k_schedule_advance(float* hp, DevSchedule* sc) {
 }
 
 // ------------------------------------------------------------------ launchers
+// overlap: launched with programmatic stream serialization (see launch_kernel)
 template <int CAP>
-cudaError_t launch_momentum(const ElemParams<CAP>& p, bool grad_f32, cudaStream_t s) {
+cudaError_t launch_momentum(const ElemParams<CAP>& p, bool grad_f32, bool overlap, cudaStream_t s) {
     if (p.ntiles <= 0) return cudaSuccess;
-    if (grad_f32)
-        k_momentum<CAP, true><<<p.ntiles, 256, 0, s>>>(p);
-    else
-        k_momentum<CAP, false><<<p.ntiles, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    if (grad_f32) return launch_kernel(k_momentum<CAP, true>, dim3(p.ntiles), dim3(256), 0, s, overlap, p);
+    return launch_kernel(k_momentum<CAP, false>, dim3(p.ntiles), dim3(256), 0, s, overlap, p);
 }
 
 template <int CAP>
-cudaError_t launch_apply(const ElemParams<CAP>& p, cudaStream_t s) {
+cudaError_t launch_apply(const ElemParams<CAP>& p, bool overlap, cudaStream_t s) {
     if (p.ntiles <= 0) return cudaSuccess;
-    k_apply<CAP><<<p.ntiles, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k_apply<CAP>, dim3(p.ntiles), dim3(256), 0, s, overlap, p);
 }
 
-cudaError_t launch_norm_scale(const NormParams& p, cudaStream_t s) {
+cudaError_t launch_norm_scale(const NormParams& p, bool overlap, cudaStream_t s) {
     if (p.nsubs <= 0) return cudaSuccess;
-    k_norm_scale<<<p.nsubs, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k_norm_scale, dim3(p.nsubs), dim3(256), 0, s, overlap, p);
 }
 
-cudaError_t launch_col_sumsq(const ColSumParams& p, cudaStream_t s) {
+cudaError_t launch_col_sumsq(const ColSumParams& p, bool overlap, cudaStream_t s) {
     if (p.nwork <= 0) return cudaSuccess;
-    k_col_sumsq<<<p.nwork, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k_col_sumsq, dim3(p.nwork), dim3(256), 0, s, overlap, p);
 }
 
-cudaError_t launch_lane_stats(const LaneParams& p, cudaStream_t s) {
+cudaError_t launch_lane_stats(const LaneParams& p, bool overlap, cudaStream_t s) {
     if (p.nsubs <= 0) return cudaSuccess;
-    k_lane_stats<<<p.nsubs, kLaneThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k_lane_stats, dim3(p.nsubs), dim3(kLaneThreads), 0, s, overlap, p);
 }
 
 cudaError_t launch_set_hparams(float* hp, float lr, float mu, float beta2, float wd, cudaStream_t s) {
@@ -528,8 +534,8 @@ cudaError_t launch_schedule_advance(float* hp, DevSchedule* sc, cudaStream_t s) 
 }
 
 #define MUON_INSTANTIATE_CAP(CAP)                                                           \
-    template cudaError_t launch_momentum<CAP>(const ElemParams<CAP>&, bool, cudaStream_t); \
-    template cudaError_t launch_apply<CAP>(const ElemParams<CAP>&, cudaStream_t);
+    template cudaError_t launch_momentum<CAP>(const ElemParams<CAP>&, bool, bool, cudaStream_t); \
+    template cudaError_t launch_apply<CAP>(const ElemParams<CAP>&, bool, cudaStream_t);
 MUON_INSTANTIATE_CAP(64)
 MUON_INSTANTIATE_CAP(256)
 MUON_INSTANTIATE_CAP(1024)

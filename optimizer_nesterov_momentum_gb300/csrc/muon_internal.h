@@ -25,6 +25,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 namespace muon {
 
@@ -173,5 +174,25 @@ struct ColSumParams {
     const int2* work;         // {sub, slab}
     int32_t nwork;
 };
+
+// Launches kernel<<<grid, block, smem, s>>>(args...).  With `overlap` the launch carries
+// programmatic stream serialization: its CTAs may be scheduled while the stream's
+// previous kernel is still finishing, so the kernel must call grid_dep_wait() before it
+// touches memory that earlier work wrote or reads.  Every kernel of the Muon step does.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 bool overlap, const Args&... args) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 }  // namespace muon

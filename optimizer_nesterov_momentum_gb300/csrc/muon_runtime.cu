@@ -27,12 +27,12 @@
 namespace muon {
 // kernels (elementwise.cu, ns_gemm_tc.cu, ns_gemm_simt.cu)
 template <int CAP>
-cudaError_t launch_momentum(const ElemParams<CAP>&, bool, cudaStream_t);
+cudaError_t launch_momentum(const ElemParams<CAP>&, bool, bool, cudaStream_t);
 template <int CAP>
-cudaError_t launch_apply(const ElemParams<CAP>&, cudaStream_t);
-cudaError_t launch_norm_scale(const NormParams&, cudaStream_t);
-cudaError_t launch_lane_stats(const LaneParams&, cudaStream_t);
-cudaError_t launch_col_sumsq(const ColSumParams&, cudaStream_t);
+cudaError_t launch_apply(const ElemParams<CAP>&, bool, cudaStream_t);
+cudaError_t launch_norm_scale(const NormParams&, bool, cudaStream_t);
+cudaError_t launch_lane_stats(const LaneParams&, bool, cudaStream_t);
+cudaError_t launch_col_sumsq(const ColSumParams&, bool, cudaStream_t);
 cudaError_t launch_set_hparams(float*, float, float, float, float, cudaStream_t);
 cudaError_t launch_schedule_set(DevSchedule*, const DevSchedule&, cudaStream_t);
 cudaError_t launch_schedule_advance(float*, DevSchedule*, cudaStream_t);
@@ -40,12 +40,12 @@ cudaError_t launch_combine_hilo(float*, const uint16_t*, const uint16_t*, int, i
 cudaError_t launch_scale_f16(float*, const uint16_t*, const float*, int, int, int, cudaStream_t);
 cudaError_t ns_gemm_tc_configure();
 cudaError_t ns_update_pair_configure();
-cudaError_t launch_ns_update_pair(const GemmParams&, bool, int, cudaStream_t);
+cudaError_t launch_ns_update_pair(const GemmParams&, bool, int, bool, cudaStream_t);
 cudaError_t ns_gram_pair_configure();
 template <int MODE, bool F16>
-cudaError_t launch_ns_sym_pair(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_ns_sym_pair(const GemmParams&, int, bool, cudaStream_t);
 template <int MODE, bool F16>
-cudaError_t launch_ns_gemm_tc(const GemmParams&, int, cudaStream_t);
+cudaError_t launch_ns_gemm_tc(const GemmParams&, int, bool, cudaStream_t);
 template <int MODE>
 cudaError_t launch_ns_gemm_simt(const GemmParams&, int, int, cudaStream_t);
 }  // namespace muon
@@ -255,7 +255,8 @@ void fill_ptrs(PtrTable<CAP>& t, float* const* params, const void* const* grads,
 }
 
 template <int CAP>
-cudaError_t run_elem(muon_s* h, float* const* params, const void* const* grads, bool apply, cudaStream_t s) {
+cudaError_t run_elem(muon_s* h, float* const* params, const void* const* grads, bool apply, bool overlap,
+                     cudaStream_t s) {
     ElemParams<CAP> ep;
     memset(&ep, 0, sizeof(ep));
     fill_ptrs<CAP>(ep.ptr, params, grads, (int)h->shapes.size());
@@ -267,15 +268,16 @@ cudaError_t run_elem(muon_s* h, float* const* params, const void* const* grads, 
     ep.nesterov = h->cfg.nesterov;
     ep.lerp_form = h->cfg.lerp_form;
     ep.status = h->status;
-    if (apply) return launch_apply<CAP>(ep, s);
-    return launch_momentum<CAP>(ep, h->cfg.grad_dtype == MUON_GRAD_F32, s);
+    if (apply) return launch_apply<CAP>(ep, overlap, s);
+    return launch_momentum<CAP>(ep, h->cfg.grad_dtype == MUON_GRAD_F32, overlap, s);
 }
 
-cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* grads, bool apply, cudaStream_t s) {
+cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* grads, bool apply, bool overlap,
+                         cudaStream_t s) {
     const size_t n = h->shapes.size();
-    if (n <= 64) return run_elem<64>(h, params, grads, apply, s);
-    if (n <= 256) return run_elem<256>(h, params, grads, apply, s);
-    return run_elem<1024>(h, params, grads, apply, s);
+    if (n <= 64) return run_elem<64>(h, params, grads, apply, overlap, s);
+    if (n <= 256) return run_elem<256>(h, params, grads, apply, overlap, s);
+    return run_elem<1024>(h, params, grads, apply, overlap, s);
 }
 
 // What a group does in one Newton-Schulz iteration.  Standard form (the write-ups'
@@ -360,6 +362,7 @@ void muon_config_default(muon_config* cfg) {
     cfg->gemm_engine = MUON_GEMM_TCGEN05;
     cfg->normuon_lanes = MUON_LANES_SHORT_SIDE;
     cfg->ns_form = MUON_NS_GRAM_PAIRS;
+    cfg->launch_overlap = 1;
 }
 
 const char* muon_error_string(int code) {
@@ -408,6 +411,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         return fail(nullptr, MUON_ERR_ARG, "bad normuon_lanes");
     if (cfg.ns_form != MUON_NS_STANDARD && cfg.ns_form != MUON_NS_GRAM_PAIRS)
         return fail(nullptr, MUON_ERR_ARG, "bad ns_form");
+    if (cfg.launch_overlap != 0 && cfg.launch_overlap != 1)
+        return fail(nullptr, MUON_ERR_ARG, "launch_overlap must be 0 or 1");
 
     // ---- shapes -> split matrices (host-only validation first)
     struct Pending {
@@ -1098,12 +1103,17 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     MUON_CUDA(h, cudaSetDevice(h->device));
     h->n_recorded = 0;
+    // Every launch after the step's first one may overlap the previous kernel's last tiles
+    // (muon_config.launch_overlap): its CTAs start on SMs that kernel no longer fills, set
+    // up their shared memory and TMEM, and wait in the kernel for its results.  The first
+    // launch keeps plain stream order behind the caller's work.
+    const bool ov = h->cfg.launch_overlap != 0;
     MUON_CUDA(h, mark(h, MUON_STAGE_MOMENTUM, s));
     if (h->schedule_on) MUON_CUDA(h, launch_schedule_advance(h->hp, h->sched, s));
-    MUON_CUDA(h, run_elem_any(h, params, grads, false, s));
+    MUON_CUDA(h, run_elem_any(h, params, grads, false, ov && h->schedule_on, s));
     NormParams np{h->d_subs, (int32_t)h->subs.size(), h->norm_part, h->norm_scale, h->iter_scale, h->status};
     MUON_CUDA(h, mark(h, MUON_STAGE_NORM, s));
-    MUON_CUDA(h, launch_norm_scale(np, s));
+    MUON_CUDA(h, launch_norm_scale(np, ov, s));
     for (size_t k = 0; k < h->plan.size(); ++k) {
         const Launch& L = h->plan[k];
         const GemmParams* gpp = &h->gparams[k];
@@ -1125,21 +1135,21 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
             cudaError_t e = cudaSuccess;
             switch (L.mode) {
                 case MODE_GRAM:
-                    e = L.pair ? (f16 ? launch_ns_sym_pair<MODE_GRAM, true>(gp, h->num_sms, s)
-                                      : launch_ns_sym_pair<MODE_GRAM, false>(gp, h->num_sms, s))
-                               : (f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, s)
-                                      : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, s));
+                    e = L.pair ? (f16 ? launch_ns_sym_pair<MODE_GRAM, true>(gp, h->num_sms, ov, s)
+                                      : launch_ns_sym_pair<MODE_GRAM, false>(gp, h->num_sms, ov, s))
+                               : (f16 ? launch_ns_gemm_tc<MODE_GRAM, true>(gp, h->num_sms, ov, s)
+                                      : launch_ns_gemm_tc<MODE_GRAM, false>(gp, h->num_sms, ov, s));
                     break;
                 case MODE_POLY:
-                    e = L.pair ? (f16 ? launch_ns_sym_pair<MODE_POLY, true>(gp, h->num_sms, s)
-                                      : launch_ns_sym_pair<MODE_POLY, false>(gp, h->num_sms, s))
-                               : (f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, s)
-                                      : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, s));
+                    e = L.pair ? (f16 ? launch_ns_sym_pair<MODE_POLY, true>(gp, h->num_sms, ov, s)
+                                      : launch_ns_sym_pair<MODE_POLY, false>(gp, h->num_sms, ov, s))
+                               : (f16 ? launch_ns_gemm_tc<MODE_POLY, true>(gp, h->num_sms, ov, s)
+                                      : launch_ns_gemm_tc<MODE_POLY, false>(gp, h->num_sms, ov, s));
                     break;
                 default:
-                    e = L.pair ? launch_ns_update_pair(gp, !f16, h->num_sms, s)
-                               : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, s)
-                                      : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, s));
+                    e = L.pair ? launch_ns_update_pair(gp, !f16, h->num_sms, ov, s)
+                               : (f16 ? launch_ns_gemm_tc<MODE_UPDATE, true>(gp, h->num_sms, ov, s)
+                                      : launch_ns_gemm_tc<MODE_UPDATE, false>(gp, h->num_sms, ov, s));
                     break;
             }
             MUON_CUDA(h, e);
@@ -1157,11 +1167,11 @@ int muon_step(muon_handle h, float* const* params, const void* const* grads, voi
     MUON_CUDA(h, mark(h, MUON_STAGE_LANE, s));
     if (h->n_colwork > 0) {
         ColSumParams cp{h->d_subs, h->d_colwork, h->n_colwork};
-        MUON_CUDA(h, launch_col_sumsq(cp, s));
+        MUON_CUDA(h, launch_col_sumsq(cp, ov, s));
     }
-    MUON_CUDA(h, launch_lane_stats(lp, s));
+    MUON_CUDA(h, launch_lane_stats(lp, ov, s));
     MUON_CUDA(h, mark(h, MUON_STAGE_APPLY, s));
-    MUON_CUDA(h, run_elem_any(h, params, grads, true, s));
+    MUON_CUDA(h, run_elem_any(h, params, grads, true, ov, s));
     MUON_CUDA(h, mark(h, -1, s));
     return MUON_OK;
 }

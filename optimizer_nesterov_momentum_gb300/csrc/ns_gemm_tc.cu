@@ -172,6 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_ns_gemm_tc(const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // everything above touches only this CTA's shared memory and TMEM, and may overlap the
+    // previous kernel's last tiles; global memory only from here on
+    grid_dep_wait();
+    grid_dep_launch();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
@@ -596,19 +600,18 @@ cudaError_t ns_gemm_tc_configure() {
 }
 
 template <int MODE, bool F16>
-cudaError_t launch_ns_gemm_tc(const GemmParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_ns_gemm_tc(const GemmParams& p, int num_sms, bool overlap, cudaStream_t stream) {
     using C = TcCfg<MODE, F16>;
     if (p.ntiles <= 0) return cudaSuccess;
     const int grid = p.ntiles < num_sms ? p.ntiles : num_sms;
-    k_ns_gemm_tc<MODE, F16><<<grid, kThreads, C::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k_ns_gemm_tc<MODE, F16>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream, overlap, p);
 }
 
-template cudaError_t launch_ns_gemm_tc<MODE_GRAM, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_UPDATE, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_gemm_tc<MODE_UPDATE, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_GRAM, false>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_GRAM, true>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_POLY, false>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_POLY, true>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_UPDATE, false>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_gemm_tc<MODE_UPDATE, true>(const GemmParams&, int, bool, cudaStream_t);
 
 }  // namespace muon

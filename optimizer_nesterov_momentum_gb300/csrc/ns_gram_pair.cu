@@ -122,6 +122,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     tc_fence_before();
     cluster_sync_all();  // barriers initialised and the allocation written in both CTAs
     tc_fence_after();
+    // everything above touches only this pair's shared memory and TMEM, and may overlap the
+    // previous kernel's last tiles; global memory only from here on
+    grid_dep_wait();
+    grid_dep_launch();
     if (threadIdx.x == 32) {
         const uint32_t mine = *tmem_slot;
         const uint32_t peer = ld_cluster_u32(cluster_addr(tmem_slot, rank ^ 1u));
@@ -463,16 +467,16 @@ cudaError_t ns_gram_pair_configure() {
 // for the b A term; groups with b_mn set: p.map_a = 128-row boxes of L, p.map_b = 64 x 64
 // boxes of R (K = m).  p.map_out: 32 x 32 boxes of the result.
 template <int MODE, bool F16>
-cudaError_t launch_ns_sym_pair(const GemmParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_ns_sym_pair(const GemmParams& p, int num_sms, bool overlap, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
     const int pairs = p.ntiles < num_sms / 2 ? p.ntiles : num_sms / 2;
-    k_ns_sym_pair<MODE, F16><<<2 * pairs, kSymThreads, SymPairCfg<MODE>::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(k_ns_sym_pair<MODE, F16>, dim3(2 * pairs), dim3(kSymThreads), SymPairCfg<MODE>::SMEM, stream,
+                         overlap, p);
 }
 
-template cudaError_t launch_ns_sym_pair<MODE_GRAM, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_GRAM, true>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_POLY, false>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_ns_sym_pair<MODE_POLY, true>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_GRAM, false>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_GRAM, true>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_POLY, false>(const GemmParams&, int, bool, cudaStream_t);
+template cudaError_t launch_ns_sym_pair<MODE_POLY, true>(const GemmParams&, int, bool, cudaStream_t);
 
 }  // namespace muon

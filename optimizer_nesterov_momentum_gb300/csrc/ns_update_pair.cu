@@ -127,6 +127,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tc_fence_before();
     cluster_sync_all();  // barriers initialised and the allocation written in both CTAs
     tc_fence_after();
+    // everything above touches only this pair's shared memory and TMEM, and may overlap the
+    // previous kernel's last tiles; global memory only from here on
+    grid_dep_wait();
+    grid_dep_launch();
     if (threadIdx.x == 32) {
         const uint32_t mine = *tmem_slot;
         const uint32_t peer = ld_cluster_u32(cluster_addr(tmem_slot, rank ^ 1u));
@@ -422,14 +426,14 @@ cudaError_t ns_update_pair_configure() {
 
 // p.tiles: 256 x 256 tiles {group slot, index, tile row (of 256), tile column (of 256)}.
 // hilo: the first iteration (bf16 operands, u read as hi + lo for the a u term).
-cudaError_t launch_ns_update_pair(const GemmParams& p, bool hilo, int num_sms, cudaStream_t stream) {
+cudaError_t launch_ns_update_pair(const GemmParams& p, bool hilo, int num_sms, bool overlap, cudaStream_t stream) {
     if (p.ntiles <= 0) return cudaSuccess;
     const int pairs = p.ntiles < num_sms / 2 ? p.ntiles : num_sms / 2;
     if (hilo)
-        k_ns_update_pair<true><<<2 * pairs, kPairThreads, UpdPairCfg<true>::SMEM, stream>>>(p);
-    else
-        k_ns_update_pair<false><<<2 * pairs, kPairThreads, UpdPairCfg<false>::SMEM, stream>>>(p);
-    return cudaGetLastError();
+        return launch_kernel(k_ns_update_pair<true>, dim3(2 * pairs), dim3(kPairThreads), UpdPairCfg<true>::SMEM, stream,
+                             overlap, p);
+    return launch_kernel(k_ns_update_pair<false>, dim3(2 * pairs), dim3(kPairThreads), UpdPairCfg<false>::SMEM, stream,
+                         overlap, p);
 }
 
 }  // namespace muon

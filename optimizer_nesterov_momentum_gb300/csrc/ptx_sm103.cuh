@@ -23,6 +23,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// stream's previous kernel is still running.  grid_dep_wait blocks the calling thread
+// until that kernel has finished and its memory operations are visible; every thread
+// that touches global memory written or read by earlier work calls it first.  Without
+// the launch attribute it returns at once.  grid_dep_launch lets the stream's next
+// kernel start its CTAs on SMs that this grid no longer fills (each of them still
+// waits for this grid to finish before it touches memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

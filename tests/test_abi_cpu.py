@@ -47,7 +47,8 @@ def test_struct_layouts_match_header():
     assert _abi.muon_config.lr_mul.offset == 48
     assert _abi.muon_config.normuon_lanes.offset == 72
     assert _abi.muon_config.ns_form.offset == 76
-    assert ctypes.sizeof(_abi.muon_config) == 80
+    assert _abi.muon_config.launch_overlap.offset == 80
+    assert ctypes.sizeof(_abi.muon_config) == 88
     assert ctypes.sizeof(_abi.muon_schedule) == 40
     assert [getattr(_abi.muon_schedule, f).offset for f, _ in _abi.muon_schedule._fields_] == [0, 4, 8, 16, 24, 28, 32]
     assert ctypes.sizeof(_abi.muon_adam_tensor) == 16 and ctypes.sizeof(_abi.muon_adam_config) == 16
@@ -235,6 +236,15 @@ def test_ns_form_is_validated(lib):
     cfg = A.muon_config_default()
     assert cfg.ns_form == A.MUON_NS_GRAM_PAIRS
     cfg.ns_form = 2
+    assert _create(lib, [A.muon_shape(64, 256, 0, 1, 0)], cfg) == A.MUON_ERR_ARG
+
+
+def test_launch_overlap_is_validated(lib):
+    from optimizer_nesterov_momentum_gb300 import _abi as A
+
+    cfg = A.muon_config_default()
+    assert cfg.launch_overlap == 1
+    cfg.launch_overlap = 2
     assert _create(lib, [A.muon_shape(64, 256, 0, 1, 0)], cfg) == A.MUON_ERR_ARG
 
 
