@@ -315,6 +315,36 @@ def test_gpt2_124m_steps_are_bitwise_reproducible():
     assert not bad_p and not bad_o, (bad_p, bad_o)
 
 
+def test_launch_overlap_changes_no_bit():
+    """Launches that overlap the previous kernel's tail (muon_config.launch_overlap) wait in
+    the kernel for its results: every parameter equals, bit for bit, a run in plain stream
+    order, eager and under graph replay, over one-SM, SM-pair and Gram-pair shapes."""
+    shapes = [Shape(256, 768), Shape(768, 256), Shape(128, 512, split=4), Shape(512, 1024), Shape(320, 96)]
+    params, grads = _inputs(shapes, 3, seed=29)
+    outs = []
+    for ov in (False, True):
+        opt = make_optimizer(shapes, lr=0.03, launch_overlap=ov)
+        p = [x.cuda() for x in params]
+        gs = [[x.cuda() for x in g] for g in grads]
+        for k in range(2):
+            opt.step(p, gs[k])
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            opt.step(p, gs[2])  # warm the allocator-free path on the capture stream
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            opt.step(p, gs[2])
+        g.replay()
+        torch.cuda.synchronize()
+        opt.sync_status()
+        outs.append([x.cpu() for x in p])
+        opt.close()
+    bad = [i for i, (a, b) in enumerate(zip(*outs)) if not torch.equal(a, b)]
+    assert not bad, bad
+
+
 def test_state_roundtrip_checkpoint():
     from optimizer_nesterov_momentum_gb300 import MUON_STATE_MOMENTUM, MUON_STATE_SECOND_MOMENT
 
