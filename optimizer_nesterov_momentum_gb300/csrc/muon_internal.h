@@ -114,6 +114,12 @@ struct GemmGroup {
     int32_t ntile_n;
     int32_t b_mn;            // SM-pair Gram launch: this group's tiles are plain products L R of two
                              // symmetric m x m matrices (right operand MN-major, K = m), not X X^T
+    // SM-pair kernels: the left (sym_l) or right (sym_r) operand is a symmetric m x m matrix
+    // stored as its upper block triangle (256 x 256 blocks (I, J) with J >= I; the SM-pair
+    // symmetric products store nothing below).  A k-block below the diagonal is read from
+    // the mirror block through the operand's other view (map_al / map_bk) and fed to the
+    // tensor cores in the other major-ness.
+    int32_t sym_l, sym_r;
     int32_t sub0;            // sub index of the group's first matrix (subs are group-ordered)
     int64_t x_stride;        // elements between matrices in x / u arenas (m * ldx)
     int64_t a_stride;        // elements between matrices in a / p arenas (m * lda)
@@ -134,6 +140,8 @@ struct GemmParams {
     CUtensorMap map_ein2[kMaxGroupsPerLaunch];  // epilogue input: first update lo half of u
     CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: A / P tile; update: X' tile
     CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored tile
+    CUtensorMap map_al[kMaxGroupsPerLaunch];    // sym_l: the left operand's MN-major boxes (64 columns)
+    CUtensorMap map_bk[kMaxGroupsPerLaunch];    // sym_r: the right operand's K-major boxes (128 rows x 64)
     GemmGroup grp[kMaxGroupsPerLaunch];
     const int4* tiles;       // {group slot, index in group, tile row, tile col}
     int32_t ntiles;

@@ -89,6 +89,9 @@ struct Group {
     // Gram-pair groups: P as the MN-major right operand of the plain products, the
     // second polynomial and T (or Q) as 128-row K-major left operands, and their stores
     CUtensorMap map_p_mn, map_p_mn128, map_pb_k, map_pb_w32, map_t_k, map_t_w32;
+    // MN-major 64 x 128 boxes of A and of the second polynomial: the SM-pair update kernel's
+    // left operand below the diagonal (T = A P', Q = P'' P'; see GemmGroup.sym_l)
+    CUtensorMap map_a_mn128, map_pb_mn128;
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_a_mn;      // 64 x 64 boxes of A: the MN-major right operand of the SM-pair polynomial
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
@@ -794,10 +797,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
              encode_3d(enc, &g.map_u_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.ulo16, g.n, g.m, g.count, g.ldx, 32,
                        kBM, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_bf16_3d(enc, &g.map_a_mir, g.a16, g.m, g.m, g.count, g.lda, 64) &&
-             encode_bf16_3d(enc, &g.map_p_mir, g.p16, g.m, g.m, g.count, g.lda, 64);
+             encode_bf16_3d(enc, &g.map_p_mir, g.p16, g.m, g.m, g.count, g.lda, 64) &&
+             encode_bf16_3d(enc, &g.map_p_mn, g.p16, g.m, g.m, g.count, g.lda, 64) &&
+             encode_bf16_3d(enc, &g.map_p_mn128, g.p16, g.m, g.m, g.count, g.lda, 128);
         if (ok && g.gs)
-            ok = encode_bf16_3d(enc, &g.map_p_mn, g.p16, g.m, g.m, g.count, g.lda, 64) &&
-                 encode_bf16_3d(enc, &g.map_p_mn128, g.p16, g.m, g.m, g.count, g.lda, 128) &&
+            ok = encode_bf16_3d(enc, &g.map_a_mn128, g.a16, g.m, g.m, g.count, g.lda, 128) &&
+                 encode_bf16_3d(enc, &g.map_pb_mn128, g.pb16, g.m, g.m, g.count, g.lda, 128) &&
                  encode_bf16_3d(enc, &g.map_pb_k, g.pb16, g.m, g.m, g.count, g.lda, kBM) &&
                  encode_bf16_3d(enc, &g.map_t_k, g.t16, g.m, g.m, g.count, g.lda, kBM) &&
                  encode_3d(enc, &g.map_pb_w32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.pb16, g.m, g.m, g.count, g.lda,
@@ -879,14 +884,18 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         const int steps = cfg.ns_steps;
         std::vector<int> cur(h->groups.size(), 0);      // iterate buffer holding the current X (after the first iteration)
         std::vector<int> nlaunch(h->chunks.size(), 0);  // per chunk: launches so far (alternating tile order)
-        auto add_work = [&](int stage, const Group& g, GroupOp op, bool first) {
+        auto add_work = [&](int stage, const Group& g, GroupOp op, bool first, bool pairs) {
             const double m = g.m, n = g.n;
+            // a symmetric result: the SM-pair kernels write its upper block triangle (256 x 256
+            // blocks), the one-SM kernels the whole matrix
+            const double nb = std::ceil(m / 256.0);
+            const double sym_out = pairs ? 2 * 256.0 * 256.0 * nb * (nb + 1) / 2 : 2 * m * m;
             double fl = 0, by = 0;
             switch (op) {
-                case OP_GRAM: fl = m * (m + 1) * n; by = 2 * m * n + 2 * m * m; break;
+                case OP_GRAM: fl = m * (m + 1) * n; by = 2 * m * n + sym_out; break;
                 case OP_POLY:
-                case OP_POLY_B: fl = m * m * (m + 1); by = 4 * m * m; break;
-                case OP_PLAIN_A: fl = m * m * (m + 1); by = 6 * m * m; break;
+                case OP_POLY_B: fl = m * m * (m + 1); by = 2 * m * m + sym_out; break;
+                case OP_PLAIN_A: fl = m * m * (m + 1); by = 4 * m * m + sym_out; break;
                 case OP_UPD_T:
                 case OP_PROD_Q: fl = 2 * m * m * m; by = 6 * m * m; break;  // the update kernel's full tiles
                 case OP_UPD: fl = 2 * m * m * n; by = 2 * m * m + (first ? 6 : 4) * m * n; break;
@@ -944,6 +953,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         gp.map_ein2[sl] = g.map_a_w32;
                         gp.map_out[sl] = g.map_a_w32;
                         gp.map_out2[sl] = g.map_a_mir;
+                        gp.map_al[sl] = g.map_a_mn;
+                        gp.map_bk[sl] = g.map_a_k;
                         if (op == OP_NONE) continue;
                         ++n_in;
                         n_in_gs += g.gs ? 1 : 0;
@@ -967,6 +978,11 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.out16 = op == OP_POLY_B ? g.pb16 : g.p16;
                                 G.opl16 = g.a16;
                                 G.opr16 = g.a16;
+                                // on SM pairs A is stored as its upper block triangle: A's rows below
+                                // the diagonal come from its columns, its columns from its rows
+                                G.sym_l = G.sym_r = pairs ? 1 : 0;
+                                gp.map_al[sl] = g.map_a_mn;
+                                gp.map_bk[sl] = g.map_a_k;
                                 break;
                             case OP_PLAIN_A:  // A <- T P', in the Gram launch
                                 gp.map_a[sl] = g.map_t_k;
@@ -976,6 +992,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.out16 = g.a16;
                                 G.opl16 = g.t16;
                                 G.opr16 = g.p16;
+                                G.sym_r = 1;  // P' as its upper block triangle (T is a full product)
+                                gp.map_bk[sl] = g.map_p_k;
                                 break;
                             case OP_PROD_Q:  // Q = P'' P', full m x m tiles on the update kernel (into T's buffer)
                                 gp.map_a[sl] = g.map_pb_k;
@@ -984,6 +1002,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.x16_out = g.t16;
                                 G.opl16 = g.pb16;
                                 G.opr16 = g.p16;
+                                G.sym_l = G.sym_r = 1;  // P'' and P' as their upper block triangles
+                                gp.map_al[sl] = g.map_pb_mn128;
+                                gp.map_bk[sl] = g.map_p_k;
                                 break;
                             case OP_UPD:
                                 gp.map_a[sl] = g.map_p_k;
@@ -998,6 +1019,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.x16_out = g.x16[nb];
                                 G.opl16 = g.p16;
                                 G.opr16 = xin16;
+                                // on SM pairs P' is stored as its upper block triangle (the first
+                                // update takes 64-deep k-blocks, later ones 128-deep)
+                                G.sym_l = pairs ? 1 : 0;
+                                gp.map_al[sl] = first ? g.map_p_mn : g.map_p_mn128;
                                 break;
                             case OP_UPD_T:  // T = A P', full m x m tiles in the update launch
                                 gp.map_a[sl] = g.map_a_k;
@@ -1006,6 +1031,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.x16_out = g.t16;
                                 G.opl16 = g.a16;
                                 G.opr16 = g.p16;
+                                G.sym_l = G.sym_r = 1;  // A and P' as their upper block triangles
+                                gp.map_al[sl] = g.map_a_mn128;
+                                gp.map_bk[sl] = g.map_p_k;
                                 break;
                             case OP_UPD_Q:  // X_{k+2} = Q X_k
                                 gp.map_a[sl] = g.map_t_k;
@@ -1052,7 +1080,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                                                           : (mode == MODE_POLY ? MUON_STAGE_POLY
                                                                                                : MUON_STAGE_UPDATE));
                     for (int sl = 0; sl < ch.ng; ++sl)
-                        if (ops[sl] != OP_NONE) add_work(stage, h->groups[ch.gi[sl]], ops[sl], first);
+                        if (ops[sl] != OP_NONE) add_work(stage, h->groups[ch.gi[sl]], ops[sl], first, pairs);
                     h->work_launches[stage]++;
                     h->plan.push_back(Launch{stage, mode, c, it, pairs ? 1 : 0, it > 0 ? 1 : 0});
                     h->gparams.push_back(gp);

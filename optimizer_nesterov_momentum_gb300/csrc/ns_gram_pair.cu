@@ -23,18 +23,30 @@
 // a diagonal Gram tile, whose two halves are the same rows, 16 KB.  CTA r's
 // TMEM receives rows 128 r .. + 127 of the tile.
 //
+// Storage of the symmetric results: the upper block triangle only.  A result is
+// stored as its 256 x 256 blocks (I, J) with J >= I (a diagonal block whole, both
+// triangles); nothing is written below.  Every SM-pair product that reads such a
+// matrix (the polynomial here, the update kernel's products) takes a k-block that
+// lies below the diagonal from the mirror block above it, loaded in the other
+// layout: a left operand's rows 256 I + .. for k in block K < I are the columns
+// 256 I + .. of rows k, an MN-major box; a right operand's columns 256 J + .. for k
+// in block K > J are the rows 256 J + .. of columns k, a K-major box.  The tensor
+// cores take either layout per k-block (instruction-descriptor major-ness bits), so
+// a consumer reads exactly the bytes it read from a full matrix, and the producer
+// stores a third fewer (six of nine blocks of a 768-wide matrix).
+//
 // The epilogue works warp by warp: warp (quad, half) owns TMEM lanes
 // 32 quad .. + 31 and columns 32 half .. + 31 of each 64-column chunk, i.e.
-// four 32 x 32 blocks per tile.  It stores each block, and for an
-// off-diagonal tile (I < J) also its transpose at (J, I), from its own ring of
-// shared-memory slots; a diagonal tile is computed whole (both triangles) and
-// stored once.  The polynomial's b A term comes from A's own 32 x 32 blocks,
-// which each warp TMA-loads two blocks ahead into a private two-slot ring.
-// No barrier spans warps.
+// four 32 x 32 blocks per tile, and stores each block from its own ring of
+// shared-memory slots.  The polynomial's b A term comes from A's own 32 x 32
+// blocks (block (I, J) is stored), which each warp TMA-loads two blocks ahead
+// into a private two-slot ring.  No barrier spans warps.
 //
 // Warp 0: TMA producer (both CTAs), warp 1: pair-wide TMEM allocation (both)
 // and the MMA issuer (CTA 0), warps 2-9: epilogue (both).  All mbarrier waits
 // are bounded (2 s) and raise the status word.
+#include <type_traits>
+
 #include "muon_internal.h"
 #include "pair_sm103.cuh"
 #include "ptx_sm103.cuh"
@@ -70,10 +82,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
     k_ns_sym_pair(const __grid_constant__ GemmParams p) {
     using C = SymPairCfg<MODE>;
     constexpr int STAGES = C::STAGES;
-    // the polynomial's right operand is MN-major (columns of the symmetric A); a Gram
-    // launch's groups with b_mn set take the same layout
-    constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/C::MNB, F16);
-    constexpr uint32_t IDESC_MN = make_idesc_16bit(256, 256, /*b_mn_major=*/true, F16);
+    // Instruction descriptors by operand major-ness.  The Gram's operands are K-major; the
+    // polynomial's right operand is MN-major (columns of the symmetric A), and so is that of
+    // a Gram launch's groups with b_mn set.  A symmetric operand's k-blocks below the
+    // diagonal come from its mirror blocks in the other major-ness (GemmGroup.sym_l / sym_r).
+    constexpr uint32_t IDESC_KK = make_idesc_16bit_ab(256, 256, false, false, F16);
+    constexpr uint32_t IDESC_KM = make_idesc_16bit_ab(256, 256, false, true, F16);
+    constexpr uint32_t IDESC_MK = make_idesc_16bit_ab(256, 256, true, false, F16);
+    constexpr uint32_t IDESC_MM = make_idesc_16bit_ab(256, 256, true, true, F16);
     // the polynomial of the second and later iterations adds a to the diagonal of P
     constexpr bool FOLD = C::POLY && F16;
 
@@ -146,6 +162,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_a[g]);
                 if (C::MNB || p.grp[g].b_mn) tma_prefetch_desc(&p.map_b[g]);
+                if (p.grp[g].sym_l) tma_prefetch_desc(&p.map_al[g]);
+                if (p.grp[g].sym_r) tma_prefetch_desc(&p.map_bk[g]);
             }
             const uint32_t full0 = cluster_addr(&full[0], 0);
             int stage = 0;
@@ -158,31 +176,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
                 const bool mnb = C::MNB || p.grp[g].b_mn;
+                const bool syl = p.grp[g].sym_l != 0, syr = p.grp[g].sym_r != 0;
                 const int K = mnb ? p.grp[g].m : p.grp[g].n;
                 const int nkb = (K + kBK - 1) / kBK;
                 const bool diag = !mnb && ti == tj;  // a diagonal Gram tile stages one set of rows
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-                        ok = false;
-                        break;
+                // k-blocks kb0 .. kb1 - 1 with one operand layout throughout: the left operand from
+                // its mirror (LMN, MN-major) or its own rows; the right operand from its mirror
+                // (RK, K-major) or as usual.  A loop per layout keeps each one's body minimal.
+                auto produce = [&](auto lmn, auto rk, int kb0, int kb1) {
+                    constexpr bool LMN = decltype(lmn)::value, RK = decltype(rk)::value;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                            ok = false;
+                            return;
+                        }
+                        if (leader) mbar_arrive_expect_tx(&full[stage], diag ? 2 * kSymRows : 2 * kSymStage);
+                        const uint32_t bar = full0 + (uint32_t)(stage * 8);
+                        uint8_t* dst = sS + stage * kSymStage;
+                        if (LMN) {
+                            // rows 256 I + 128 r .. + 127 of a symmetric left operand, k-block left
+                            // of the diagonal: its mirror, rows kb of columns 256 I + 128 r .., as
+                            // two MN-major 64-column boxes
+                            const int col = ti * 256 + (int)rank * kBM;
+                            tma_load_3d_pair(dst, &p.map_al[g], bar, col, kb * kBK, idx);
+                            tma_load_3d_pair(dst + 64 * kBK * 2, &p.map_al[g], bar, col + 64, kb * kBK, idx);
+                        } else {
+                            tma_load_3d_pair(dst, &p.map_a[g], bar, kb * kBK, ti * 256 + (int)rank * kBM, idx);
+                        }
+                        if (RK) {
+                            // a symmetric right operand's k-block below the diagonal: its mirror,
+                            // the K-major rows 256 J + 128 r .. + 127
+                            tma_load_3d_pair(dst + kSymRows, &p.map_bk[g], bar, kb * kBK, tj * 256 + (int)rank * 128,
+                                             idx);
+                        } else if (mnb) {
+                            // columns 256 J + 128 r .. + 127 of the right operand for k-block rows
+                            // kb: two 64-column boxes
+                            const int col = tj * 256 + (int)rank * 128;
+                            tma_load_3d_pair(dst + kSymRows, &p.map_b[g], bar, col, kb * kBK, idx);
+                            tma_load_3d_pair(dst + kSymRows + 64 * kBK * 2, &p.map_b[g], bar, col + 64, kb * kBK, idx);
+                        } else if (!diag) {
+                            tma_load_3d_pair(dst + kSymRows, &p.map_a[g], bar, kb * kBK, tj * 256 + (int)rank * kBM,
+                                             idx);
+                        }
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    if (leader) mbar_arrive_expect_tx(&full[stage], diag ? 2 * kSymRows : 2 * kSymStage);
-                    const uint32_t bar = full0 + (uint32_t)(stage * 8);
-                    uint8_t* dst = sS + stage * kSymStage;
-                    tma_load_3d_pair(dst, &p.map_a[g], bar, kb * kBK, ti * 256 + (int)rank * kBM, idx);
-                    if (mnb) {
-                        // columns 256 J + 128 r .. + 127 of the right operand for k-block rows kb:
-                        // two 64-column boxes
-                        const int col = tj * 256 + (int)rank * 128;
-                        tma_load_3d_pair(dst + kSymRows, &p.map_b[g], bar, col, kb * kBK, idx);
-                        tma_load_3d_pair(dst + kSymRows + 64 * kBK * 2, &p.map_b[g], bar, col + 64, kb * kBK, idx);
-                    } else if (!diag) {
-                        tma_load_3d_pair(dst + kSymRows, &p.map_a[g], bar, kb * kBK, tj * 256 + (int)rank * kBM, idx);
-                    }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                };
+                using F_ = std::false_type;
+                using T_ = std::true_type;
+                if (!syl && !syr) {
+                    produce(F_{}, F_{}, 0, nkb);
+                } else {
+                    // J >= I: the left operand's mirrored k-blocks (block K < I) all come before the
+                    // right operand's (block K > J)
+                    const int a_end = syl ? min(nkb, ti * (256 / kBK)) : 0;
+                    const int b_beg = (mnb && syr) ? min(nkb, (tj + 1) * (256 / kBK)) : nkb;
+                    produce(T_{}, F_{}, 0, a_end);
+                    if (ok) produce(F_{}, F_{}, a_end, b_beg);
+                    if (ok) produce(F_{}, T_{}, b_beg, nkb);
                 }
             }
         }
@@ -202,10 +255,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const bool mnb = C::MNB || p.grp[tile.x].b_mn;
+                const bool syl = p.grp[tile.x].sym_l != 0, syr = p.grp[tile.x].sym_r != 0;
                 const int K = mnb ? p.grp[tile.x].m : p.grp[tile.x].n;
                 const int nkb = (K + kBK - 1) / kBK;
                 const bool diag = !mnb && tile.z == tile.w;
-                const uint32_t idesc = mnb ? IDESC_MN : IDESC;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -235,16 +288,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                             const int st = h ? st1 : stage;
                             const uint32_t a_st = s_base + st * kSymStage;
                             const uint32_t b_st = diag ? a_st : a_st + kSymRows;  // a diagonal tile's halves are the same rows
+                            const int kblk = (kb + h) >> 2;
+                            const bool a_mn = syl && kblk < tile.z;
+                            const bool b_mn = mnb && !(syr && kblk > tile.w);
                             // the stage's descriptors; a 16-deep step adds to the start-address field
                             // (16-byte units): 32 bytes along a K-major operand, 16 rows of 128 bytes
                             // along an MN-major one (8 KB between its 64-column boxes)
-                            const uint64_t ad = make_sdesc_sw128(a_st, 16, 1024);
-                            const uint64_t bd = mnb ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
-                                                    : make_sdesc_sw128(b_st, 16, 1024);
-                            const uint64_t b_step = mnb ? 128 : 2;
+                            const uint64_t ad = a_mn ? make_sdesc_sw128(a_st, 64 * kBK * 2, 1024)
+                                                     : make_sdesc_sw128(a_st, 16, 1024);
+                            const uint64_t bd = b_mn ? make_sdesc_sw128(b_st, 64 * kBK * 2, 1024)
+                                                     : make_sdesc_sw128(b_st, 16, 1024);
+                            const uint64_t a_step = a_mn ? 128 : 2, b_step = b_mn ? 128 : 2;
+                            const uint32_t idesc = a_mn ? (b_mn ? IDESC_MM : IDESC_MK) : (b_mn ? IDESC_KM : IDESC_KK);
 #pragma unroll
                             for (int kk = 0; kk < kBK / 16; ++kk)
-                                umma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + b_step * (uint64_t)kk, idesc,
+                                umma_f16_pair(d_tmem, ad + a_step * (uint64_t)kk, bd + b_step * (uint64_t)kk, idesc,
                                               (kb | h | kk) != 0 ? 1u : 0u);
                             any = true;
                             umma_commit_pair(&empty[st]);
@@ -292,7 +350,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
             if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
             const int g = tile.x, idx = tile.y, ti = tile.z, tj = tile.w;
             const GemmGroup& G = p.grp[g];
-            const bool diag = ti == tj;
             const int row0 = ti * 256 + (int)rank * kBM + quad * 32;  // this warp's first row
             // POLY: A's block of chunk c at (row0, this warp's columns of chunk c), lane 0 issues
             auto load_in = [&](int c, int sl) {
@@ -396,23 +453,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         tma_store_3d(&p.map_out[g], slot, col0, row0, idx);
-                        bulk_commit();
-                    }
-                    ++nout;
-                }
-                if (!diag) {
-                    // its transpose at (col0, row0): element (lane, e) goes to row e, column lane
-                    uint8_t* slot = wout + (nout % kOutSlots) * kBlk;
-                    if (nout >= kOutSlots && lane == 0) bulk_wait_read<kOutSlots - 1>();
-                    __syncwarp();
-                    const uint32_t cj = (uint32_t)lane >> 3, cb2 = ((uint32_t)lane & 7u) * 2u;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        *reinterpret_cast<uint16_t*>(slot + sw64((uint32_t)e, cj) + cb2) = b[e];
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&p.map_out[g], slot, row0, col0, idx);
                         bulk_commit();
                     }
                     ++nout;

@@ -33,6 +33,8 @@
 // The allocation is checked before use: both CTAs must see the same TMEM
 // address, else the kernel reports the mismatch in the status word and does
 // no work.
+#include <type_traits>
+
 #include "muon_internal.h"
 #include "pair_sm103.cuh"
 #include "ptx_sm103.cuh"
@@ -68,7 +70,12 @@ struct UpdPairCfg {
     static constexpr int IN_WARP = HILO ? 2 * 2 * kWarpSlot : 0;  // two chunks in flight, hi and lo
     static constexpr int SMEM = STAGES * STAGE + kPairOutBytes + kPairEpiWarps * IN_WARP + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory budget");
-    static constexpr uint32_t IDESC = make_idesc_16bit(256, 256, /*b_mn_major=*/true, /*fp16=*/!HILO);
+    // by operand major-ness: P' (or another left operand) K-major and X MN-major, except
+    // where a symmetric operand's k-block comes from its mirror (GemmGroup.sym_l / sym_r)
+    static constexpr uint32_t IDESC_KM = make_idesc_16bit_ab(256, 256, false, true, /*fp16=*/!HILO);
+    static constexpr uint32_t IDESC_MM = make_idesc_16bit_ab(256, 256, true, true, !HILO);
+    static constexpr uint32_t IDESC_KK = make_idesc_16bit_ab(256, 256, false, false, !HILO);
+    static constexpr uint32_t IDESC_MK = make_idesc_16bit_ab(256, 256, true, false, !HILO);
 };
 
 }  // namespace
@@ -153,6 +160,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             for (int g = 0; g < p.ngroups; ++g) {
                 tma_prefetch_desc(&p.map_a[g]);
                 tma_prefetch_desc(&p.map_b[g]);
+                if (p.grp[g].sym_l) tma_prefetch_desc(&p.map_al[g]);
+                if (p.grp[g].sym_r) tma_prefetch_desc(&p.map_bk[g]);
             }
             const uint32_t full0 = cluster_addr(&full[0], 0);  // CTA 0's full barriers
             int stage = 0;
@@ -167,22 +176,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const int nkb = (p.grp[g].m + BK - 1) / BK;
                 const int row0 = ti * 2 * kBM + (int)rank * kBM;
                 const int col0 = tj * 256 + (int)rank * 128;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE);
-                    const uint32_t bar = full0 + (uint32_t)(stage * 8);
+                const bool syl = p.grp[g].sym_l != 0, syr = p.grp[g].sym_r != 0;
+                // k-blocks kb0 .. kb1 - 1 with one operand layout throughout: the left operand from
+                // its mirror (LMN) or its own rows, the right one from its mirror (RK) or as usual.
+                // A loop per layout keeps each one's body minimal.
+                auto produce = [&](auto lmn, auto rk, int kb0, int kb1) {
+                    constexpr bool LMN = decltype(lmn)::value, RK = decltype(rk)::value;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                            ok = false;
+                            return;
+                        }
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE);
+                        const uint32_t bar = full0 + (uint32_t)(stage * 8);
+                        uint8_t* da = sA + stage * C::A_BYTES;
+                        uint8_t* db = sB + stage * C::B_BYTES;
+                        if (LMN) {
+                            // a symmetric left operand left of the diagonal: the mirror block's
+                            // columns row0 .. + 127 of rows kb, two MN-major boxes of BK x 64
+                            tma_load_3d_pair(da, &p.map_al[g], bar, row0, kb * BK, idx);
+                            tma_load_3d_pair(da + BK * 128, &p.map_al[g], bar, row0 + 64, kb * BK, idx);
+                        } else {
 #pragma unroll
-                    for (int ks = 0; ks < BK / 64; ++ks)
-                        tma_load_3d_pair(sA + stage * C::A_BYTES + ks * (kBM * 128), &p.map_a[g], bar, kb * BK + ks * 64,
-                                         row0, idx);
-                    tma_load_3d_pair(sB + stage * C::B_BYTES, &p.map_b[g], bar, col0, kb * BK, idx);
-                    tma_load_3d_pair(sB + stage * C::B_BYTES + BK * 128, &p.map_b[g], bar, col0 + 64, kb * BK, idx);
-                    if (++stage == kPairStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                            for (int ks = 0; ks < BK / 64; ++ks)
+                                tma_load_3d_pair(da + ks * (kBM * 128), &p.map_a[g], bar, kb * BK + ks * 64, row0, idx);
+                        }
+                        if (RK) {
+                            // a symmetric right operand below the diagonal: the mirror block's rows
+                            // col0 .. + 127 of columns kb, BK / 64 K-major boxes of 128 x 64
+#pragma unroll
+                            for (int ks = 0; ks < BK / 64; ++ks)
+                                tma_load_3d_pair(db + ks * (128 * 128), &p.map_bk[g], bar, kb * BK + ks * 64, col0, idx);
+                        } else {
+                            tma_load_3d_pair(db, &p.map_b[g], bar, col0, kb * BK, idx);
+                            tma_load_3d_pair(db + BK * 128, &p.map_b[g], bar, col0 + 64, kb * BK, idx);
+                        }
+                        if (++stage == kPairStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                };
+                using F_ = std::false_type;
+                using T_ = std::true_type;
+                if (!syl && !syr) {
+                    produce(F_{}, F_{}, 0, nkb);
+                } else {
+                    // left mirrored for k in blocks K < I, right for K > J: at most three runs
+                    const int a_end = syl ? min(nkb, ti * (256 / BK)) : 0;
+                    const int b_beg = syr ? min(nkb, (tj + 1) * (256 / BK)) : nkb;
+                    if (a_end <= b_beg) {
+                        produce(T_{}, F_{}, 0, a_end);
+                        if (ok) produce(F_{}, F_{}, a_end, b_beg);
+                        if (ok) produce(F_{}, T_{}, b_beg, nkb);
+                    } else {
+                        produce(T_{}, F_{}, 0, b_beg);
+                        if (ok) produce(T_{}, T_{}, b_beg, a_end);
+                        if (ok) produce(F_{}, T_{}, a_end, nkb);
                     }
                 }
             }
@@ -204,6 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const int4 tile = tile_nx;
                 if (t + npairs < p.ntiles) tile_nx = p.tiles[t + npairs];
                 const int nkb = (p.grp[tile.x].m + BK - 1) / BK;
+                const bool syl = p.grp[tile.x].sym_l != 0, syr = p.grp[tile.x].sym_r != 0;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -216,14 +267,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     }
                     tc_fence_after();
                     // the stage's descriptors; a 16-deep step adds to the start-address field
-                    // (16-byte units): 32 bytes along a 64-wide K-major box of A (16 KB to the
-                    // next box), 16 rows of 128 bytes along MN-major B (BK rows per 64-column box)
-                    const uint64_t ad = make_sdesc_sw128(a_base + stage * C::A_BYTES, 16, 1024);
-                    const uint64_t bd = make_sdesc_sw128(b_base + stage * C::B_BYTES, BK * 128, 1024);
+                    // (16-byte units): 32 bytes along a 64-wide K-major box (16 KB to the next
+                    // box), 16 rows of 128 bytes along an MN-major operand (BK rows per 64-column
+                    // box).  Left K-major and right MN-major, except for a symmetric operand's
+                    // mirrored k-blocks.
+                    const int kblk = (kb * BK) >> 8;
+                    const bool a_mn = syl && kblk < tile.z;
+                    const bool b_mn = !(syr && kblk > tile.w);
+                    const uint64_t ad = make_sdesc_sw128(a_base + stage * C::A_BYTES, a_mn ? BK * 128 : 16, 1024);
+                    const uint64_t bd = make_sdesc_sw128(b_base + stage * C::B_BYTES, b_mn ? BK * 128 : 16, 1024);
+                    const uint32_t idesc =
+                        a_mn ? (b_mn ? C::IDESC_MM : C::IDESC_MK) : (b_mn ? C::IDESC_KM : C::IDESC_KK);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_f16_pair(tacc[acc], ad + (uint64_t)((kk >> 2) * (kBM * 128 / 16) + (kk & 3) * 2),
-                                      bd + (uint64_t)(kk * 128), C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t kmaj = (uint64_t)((kk >> 2) * (kBM * 128 / 16) + (kk & 3) * 2);
+                        const uint64_t mnmaj = (uint64_t)(kk * 128);
+                        umma_f16_pair(tacc[acc], ad + (a_mn ? mnmaj : kmaj), bd + (b_mn ? mnmaj : kmaj), idesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
+                    }
                     mma_any = true;
                     umma_commit_pair(&empty[stage]);
                     if (++stage == kPairStages) {

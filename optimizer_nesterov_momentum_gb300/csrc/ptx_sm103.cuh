@@ -194,16 +194,20 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, both operands
-// K-major unless b_mn_major.
-// kind::f16 instruction descriptor: fp32 accumulator, A and B both fp16 or both bf16.
-__host__ __device__ constexpr uint32_t make_idesc_16bit(int M, int N, bool b_mn_major, bool fp16) {
+// kind::f16 instruction descriptor: fp32 accumulator, A and B both fp16 or both bf16,
+// each operand K-major unless its MN-major flag is set.
+__host__ __device__ constexpr uint32_t make_idesc_16bit_ab(int M, int N, bool a_mn_major, bool b_mn_major, bool fp16) {
     return (1u << 4)                               // D format: f32
            | ((fp16 ? 0u : 1u) << 7)               // A format: 0 = f16, 1 = bf16
            | ((fp16 ? 0u : 1u) << 10)              // B format: the same type as A
+           | ((a_mn_major ? 1u : 0u) << 15)        // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)        // B major-ness
            | ((uint32_t)(N >> 3) << 17)            // N / 8
            | ((uint32_t)(M >> 4) << 24);           // M / 16
+}
+
+__host__ __device__ constexpr uint32_t make_idesc_16bit(int M, int N, bool b_mn_major, bool fp16) {
+    return make_idesc_16bit_ab(M, N, false, b_mn_major, fp16);
 }
 
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_major) {
