@@ -183,14 +183,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 // k-blocks kb0 .. kb1 - 1 with one operand layout throughout: the left operand from
                 // its mirror (LMN, MN-major) or its own rows; the right operand from its mirror
                 // (RK, K-major) or as usual.  A loop per layout keeps each one's body minimal.
-                auto produce = [&](auto lmn, auto rk, int kb0, int kb1) {
+                auto produce = [&](auto lmn, auto rk, auto mnbv, auto diagv, int kb0, int kb1) {
                     constexpr bool LMN = decltype(lmn)::value, RK = decltype(rk)::value;
+                    constexpr bool MN = decltype(mnbv)::value, DIAG = decltype(diagv)::value;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                             ok = false;
                             return;
                         }
-                        if (leader) mbar_arrive_expect_tx(&full[stage], diag ? 2 * kSymRows : 2 * kSymStage);
+                        if (leader) mbar_arrive_expect_tx(&full[stage], DIAG ? 2 * kSymRows : 2 * kSymStage);
                         const uint32_t bar = full0 + (uint32_t)(stage * 8);
                         uint8_t* dst = sS + stage * kSymStage;
                         if (LMN) {
@@ -208,13 +209,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                             // the K-major rows 256 J + 128 r .. + 127
                             tma_load_3d_pair(dst + kSymRows, &p.map_bk[g], bar, kb * kBK, tj * 256 + (int)rank * 128,
                                              idx);
-                        } else if (mnb) {
+                        } else if (MN) {
                             // columns 256 J + 128 r .. + 127 of the right operand for k-block rows
                             // kb: two 64-column boxes
                             const int col = tj * 256 + (int)rank * 128;
                             tma_load_3d_pair(dst + kSymRows, &p.map_b[g], bar, col, kb * kBK, idx);
                             tma_load_3d_pair(dst + kSymRows + 64 * kBK * 2, &p.map_b[g], bar, col + 64, kb * kBK, idx);
-                        } else if (!diag) {
+                        } else if (!DIAG) {
                             tma_load_3d_pair(dst + kSymRows, &p.map_a[g], bar, kb * kBK, tj * 256 + (int)rank * kBM,
                                              idx);
                         }
@@ -226,16 +227,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSymThreads, 1)
                 };
                 using F_ = std::false_type;
                 using T_ = std::true_type;
-                if (!syl && !syr) {
-                    produce(F_{}, F_{}, 0, nkb);
-                } else {
+                if (mnb) {
                     // J >= I: the left operand's mirrored k-blocks (block K < I) all come before the
                     // right operand's (block K > J)
                     const int a_end = syl ? min(nkb, ti * (256 / kBK)) : 0;
-                    const int b_beg = (mnb && syr) ? min(nkb, (tj + 1) * (256 / kBK)) : nkb;
-                    produce(T_{}, F_{}, 0, a_end);
-                    if (ok) produce(F_{}, F_{}, a_end, b_beg);
-                    if (ok) produce(F_{}, T_{}, b_beg, nkb);
+                    const int b_beg = syr ? min(nkb, (tj + 1) * (256 / kBK)) : nkb;
+                    produce(T_{}, F_{}, T_{}, F_{}, 0, a_end);
+                    if (ok) produce(F_{}, F_{}, T_{}, F_{}, a_end, b_beg);
+                    if (ok) produce(F_{}, T_{}, T_{}, F_{}, b_beg, nkb);
+                } else if (diag) {
+                    produce(F_{}, F_{}, F_{}, T_{}, 0, nkb);
+                } else {
+                    produce(F_{}, F_{}, F_{}, F_{}, 0, nkb);
                 }
             }
         }
