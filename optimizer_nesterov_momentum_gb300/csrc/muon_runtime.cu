@@ -118,6 +118,14 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     // update launch), and the full m x m tiles of the Gram-pair groups alone (Q = P'' P')
     int32_t pair_t_off = 0, pair_t_n = 0;
     int32_t pair_q_off = 0, pair_q_n = 0;
+    // The launch of Q also takes the first update tiles of the standard-form groups (they
+    // depend only on their own polynomial, which precedes it) when that fills its last wave
+    // of SM pairs and saves one in the update launch after it: q_fill[sl] of group slot sl's
+    // tiles move.  pair_qx: the Q tiles and those; pair_ux: every update tile but those.
+    int32_t q_fill[kMaxGroupsPerLaunch] = {};
+    int32_t q_fill_n = 0;
+    int32_t pair_qx_off = 0, pair_qx_n = 0;
+    int32_t pair_ux_off = 0, pair_ux_n = 0;
 };
 
 // One Newton-Schulz launch of the step, in order.
@@ -720,6 +728,44 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
             if (any_gs) {
                 upd_list(0, true, ch.pair_t_off, ch.pair_t_n);
                 upd_list(2, true, ch.pair_q_off, ch.pair_q_n);
+                // Q's launch and the update launch after it hold tiles of one size when every
+                // group has the same m; then move s standard update tiles, the fewest that
+                // minimise the two launches' waves over the SM pairs
+                std::vector<T> std_t, gs_t, q_t;
+                bool one_m = true;
+                for (int sl = 0; sl < ch.ng; ++sl) {
+                    const Group& g = h->groups[ch.gi[sl]];
+                    one_m = one_m && g.m == h->groups[ch.gi[0]].m;
+                    for (int idx = 0; idx < g.count; ++idx)
+                        for (int ti = 0; ti < g.m / 256; ++ti) {
+                            for (int tj = 0; tj < g.n / 256; ++tj)
+                                (g.gs ? gs_t : std_t).push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+                            if (g.gs)
+                                for (int tj = 0; tj < g.m / 256; ++tj)
+                                    q_t.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
+                        }
+                }
+                const int64_t P = std::max(1, h->num_sms / 2);
+                const int64_t nq = (int64_t)q_t.size(), nu = (int64_t)(std_t.size() + gs_t.size());
+                auto waves = [&](int64_t x) { return (x + P - 1) / P; };
+                int64_t best = 0;
+                if (one_m)
+                    for (int64_t sft = 1; sft <= std::min<int64_t>((int64_t)std_t.size(), P - 1); ++sft)
+                        if (waves(nq + sft) + waves(nu - sft) < waves(nq + best) + waves(nu - best)) best = sft;
+                if (best > 0) {
+                    ch.q_fill_n = (int32_t)best;
+                    std::vector<T> qx(q_t), ux(gs_t);
+                    for (size_t i = 0; i < std_t.size(); ++i) {
+                        if ((int64_t)i < best) {
+                            qx.push_back(std_t[i]);
+                            ch.q_fill[std_t[i].t.x]++;
+                        } else {
+                            ux.push_back(std_t[i]);
+                        }
+                    }
+                    emit(qx, ch.pair_qx_off, ch.pair_qx_n);
+                    emit(ux, ch.pair_ux_off, ch.pair_ux_n);
+                }
             }
         }
         h->chunks.push_back(ch);
@@ -884,7 +930,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
         const int steps = cfg.ns_steps;
         std::vector<int> cur(h->groups.size(), 0);      // iterate buffer holding the current X (after the first iteration)
         std::vector<int> nlaunch(h->chunks.size(), 0);  // per chunk: launches so far (alternating tile order)
-        auto add_work = [&](int stage, const Group& g, GroupOp op, bool first, bool pairs) {
+        // frac: the share of the group's tiles this launch computes
+        auto add_work = [&](int stage, const Group& g, GroupOp op, bool first, bool pairs, double frac) {
             const double m = g.m, n = g.n;
             // a symmetric result: the SM-pair kernels write its upper block triangle (256 x 256
             // blocks), the one-SM kernels the whole matrix
@@ -902,8 +949,8 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 case OP_UPD_Q: fl = 2 * m * m * n; by = 2 * m * m + 4 * m * n; break;
                 default: break;
             }
-            h->work_flops[stage] += (int64_t)(fl * g.count);
-            h->work_bytes[stage] += (int64_t)(by * g.count);
+            h->work_flops[stage] += (int64_t)(fl * g.count * frac);
+            h->work_bytes[stage] += (int64_t)(by * g.count * frac);
         };
         for (int it = 0; it < steps; ++it) {
             const bool first = it == 0, last = it == steps - 1;
@@ -922,7 +969,13 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     gp.first = first;
                     gp.last = last;
                     gp.f16 = it > 0;
-                    gp.want_rowsq = ph == PH_UPDATE && last && cfg.normuon;
+                    // this iteration's launch of Q = P'' P' (a Gram-pair chunk's second iteration of
+                    // a pair); it may carry standard-form update tiles (Chunk.q_fill)
+                    bool q_launch = false;
+                    for (int sl = 0; sl < ch.ng; ++sl)
+                        q_launch = q_launch || group_op(h->groups[ch.gi[sl]], it, steps, PH_PLAIN) == OP_PROD_Q;
+                    const bool q_fill = pairs && q_launch && ch.q_fill_n > 0;
+                    gp.want_rowsq = (ph == PH_UPDATE || (ph == PH_PLAIN && q_fill)) && last && cfg.normuon;
                     gp.status = h->status;
                     gp.pair = pairs ? 1 : 0;
                     int n_in = 0, n_in_gs = 0, n_gs = 0;
@@ -942,7 +995,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                         G.a16 = g.a16;
                         G.rowsq = g.rowsq;
                         const uint16_t* xin16 = first ? g.u16 : g.x16[cb];
-                        const GroupOp op = group_op(g, it, steps, ph);
+                        GroupOp op = group_op(g, it, steps, ph);
+                        if (ph == PH_PLAIN && q_fill && op == OP_NONE && ch.q_fill[sl] > 0 &&
+                            group_op(g, it, steps, PH_UPDATE) == OP_UPD)
+                            op = OP_UPD;  // some of its update tiles ride along with Q
                         ops[sl] = op;
                         n_gs += g.gs ? 1 : 0;
                         // every slot carries valid descriptors (the kernels prefetch all of them);
@@ -1002,6 +1058,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.x16_out = g.t16;
                                 G.opl16 = g.pb16;
                                 G.opr16 = g.p16;
+                                G.rowsq = nullptr;  // Q is not an output: no row sums
                                 G.sym_l = G.sym_r = 1;  // P'' and P' as their upper block triangles
                                 gp.map_al[sl] = g.map_pb_mn128;
                                 gp.map_bk[sl] = g.map_p_k;
@@ -1052,7 +1109,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     const bool all_in = n_in == ch.ng;
                     bool has_t = false;
                     for (int sl = 0; sl < ch.ng; ++sl) has_t = has_t || ops[sl] == OP_UPD_T;
-                    if (!all_in && !(n_in == n_gs && n_in_gs == n_gs)) {
+                    if (!all_in && !(n_in == n_gs && n_in_gs == n_gs) && !(ph == PH_PLAIN && q_fill)) {
                         cudaFree(h->arena);
                         delete h;
                         return fail(nullptr, MUON_ERR_CUDA, "internal error: launch plan group set");
@@ -1065,8 +1122,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     // the Gram-pair product Q runs on the update kernel
                     int mode = ph == PH_GRAM ? MODE_GRAM : (ph == PH_POLY ? MODE_POLY : MODE_UPDATE);
                     if (pairs) {
-                        if (ph == PH_PLAIN)
+                        if (ph == PH_PLAIN && q_fill)
+                            pick(ch.pair_qx_off, ch.pair_qx_n);
+                        else if (ph == PH_PLAIN)
                             pick(ch.pair_q_off, ch.pair_q_n);
+                        else if (mode == MODE_UPDATE && q_fill)
+                            pick(ch.pair_ux_off, ch.pair_ux_n);
                         else if (mode == MODE_UPDATE)
                             pick(has_t ? ch.pair_t_off : ch.pair_off, has_t ? ch.pair_t_n : ch.pair_n);
                         else
@@ -1079,8 +1140,16 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                                      : (mode == MODE_GRAM ? MUON_STAGE_GRAM
                                                                           : (mode == MODE_POLY ? MUON_STAGE_POLY
                                                                                                : MUON_STAGE_UPDATE));
-                    for (int sl = 0; sl < ch.ng; ++sl)
-                        if (ops[sl] != OP_NONE) add_work(stage, h->groups[ch.gi[sl]], ops[sl], first, pairs);
+                    for (int sl = 0; sl < ch.ng; ++sl) {
+                        if (ops[sl] == OP_NONE) continue;
+                        const Group& g = h->groups[ch.gi[sl]];
+                        double frac = 1.0;
+                        if (q_fill && ops[sl] == OP_UPD) {
+                            const double moved = (double)ch.q_fill[sl] / ((double)g.count * (g.m / 256) * (g.n / 256));
+                            frac = ph == PH_PLAIN ? moved : 1.0 - moved;
+                        }
+                        add_work(stage, g, ops[sl], first, pairs, frac);
+                    }
                     h->work_launches[stage]++;
                     h->plan.push_back(Launch{stage, mode, c, it, pairs ? 1 : 0, it > 0 ? 1 : 0});
                     h->gparams.push_back(gp);

@@ -442,7 +442,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 }
                 ++wchunk;
             }
-            if (p.want_rowsq) {
+            if (p.want_rowsq && G.rowsq != nullptr) {
                 const int row = row0 + lane;
                 if (row < G.m)  // part-major: [matrix][256-column tile, half][row]
                     G.rowsq[((int64_t)idx * G.ntile_n * 2 + tj * 2 + half) * G.m + row] = sumsq;

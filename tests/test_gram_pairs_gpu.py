@@ -89,3 +89,33 @@ def test_gram_pairs_launch_plan():
     assert gp.launch_count() == std.launch_count() + 2
     std.close()
     gp.close()
+
+
+def test_q_launch_takes_standard_tiles_to_fill_its_last_wave():
+    """With the GPT-2-124M shapes the launch of Q = P'' P' (216 tiles) leaves its last wave of
+    SM pairs part empty while the update launch after it (1296 tiles) starts a wave for a few
+    tiles: the plan moves the fewest standard-form update tiles that save that wave into Q's
+    launch.  The work moves between the two stages; the sum stays the same."""
+    from optimizer_nesterov_momentum_gb300 import MatrixSpec, Muon
+
+    specs = [MatrixSpec(768, 768)] * 48 + [MatrixSpec(768, 3072)] * 24
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    m = 768
+    nq, nu, n_std = 24 * 9, 48 * 9 + 24 * 36, 48 * 9
+
+    def waves(x):
+        return -(-x // pairs)
+
+    best = 0
+    for s in range(1, min(n_std, pairs - 1) + 1):
+        if waves(nq + s) + waves(nu - s) < waves(nq + best) + waves(nu - best):
+            best = s
+    gp = Muon(specs, ns_form="gram_pairs")
+    w = gp.stage_work()
+    q_fl = 2 * 24 * 2 * m ** 3                # two Q launches, full m x m products
+    tile_fl = 2 * m * m * m / 9               # one 256 x 256 tile of a square matrix's update
+    assert w["product"][0] == pytest.approx(q_fl + 2 * best * tile_fl, rel=1e-9)
+    upd_all = 48 * 5 * 2 * m ** 3 + 24 * (3 * 2 * m * m * 3072 + 2 * 2 * m ** 3)
+    assert w["update"][0] + w["product"][0] == pytest.approx(upd_all + q_fl, rel=1e-9)
+    assert w["product"][2] == 2
+    gp.close()
