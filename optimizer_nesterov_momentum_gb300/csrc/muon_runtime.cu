@@ -90,8 +90,9 @@ struct Group {
     // second polynomial and T (or Q) as 128-row K-major left operands, and their stores
     CUtensorMap map_p_mn, map_p_mn128, map_pb_k, map_pb_w32, map_t_k, map_t_w32;
     // MN-major 64 x 128 boxes of A and of the second polynomial: the SM-pair update kernel's
-    // left operand below the diagonal (T = A P', Q = P'' P'; see GemmGroup.sym_l)
-    CUtensorMap map_a_mn128, map_pb_mn128;
+    // left operand below the diagonal (T = A P', Q = P'' P'; see GemmGroup.sym_l); 64 x 64
+    // boxes of T: the left operand of A <- T P' below the diagonal
+    CUtensorMap map_a_mn128, map_pb_mn128, map_t_mn;
     CUtensorMap map_u_k256, map_x_k256[2], map_a_k256;  // 64 x 256 boxes: right operand of gram / poly
     CUtensorMap map_a_mn;      // 64 x 64 boxes of A: the MN-major right operand of the SM-pair polynomial
     CUtensorMap map_u_hi, map_u_lo, map_x_o32[2], map_a_mir, map_p_mir;
@@ -113,9 +114,10 @@ struct Chunk {        // up to kMaxGroupsPerLaunch groups per GEMM launch
     int32_t upd_off = 0, upd_n = 0;
     int32_t pair_off = 0, pair_n = 0;  // 256 x 256 update tiles for SM pairs (0: chunk not eligible)
     int32_t spg_off = 0, spg_n = 0;    // 256 x 256 Gram tiles (J >= I) for SM pairs
-    // Gram-pair chunks: the update tiles of the standard-form groups together with the full
-    // m x m tiles of the Gram-pair groups (the first half of a pair computes T = A P' in the
-    // update launch), and the full m x m tiles of the Gram-pair groups alone (Q = P'' P')
+    // Gram-pair chunks: the update tiles of the standard-form groups together with the m x m
+    // tiles on or above the diagonal of the Gram-pair groups (the first half of a pair computes
+    // the symmetric T = A P' in the update launch), and the full m x m tiles of the Gram-pair
+    // groups alone (Q = P'' P')
     int32_t pair_t_off = 0, pair_t_n = 0;
     int32_t pair_q_off = 0, pair_q_n = 0;
     // The launch of Q also takes the first update tiles of the standard-form groups (they
@@ -299,13 +301,14 @@ cudaError_t run_elem_any(muon_s* h, float* const* params, const void* const* gra
 // A_{k+1} = P'_k A_k P'_k = (A_k P'_k) P'_k and X_{k+2} = (P'_{k+1} P'_k) X_k, so a pair
 // of iterations forms one Gram matrix and one update instead of two of each, for three
 // m x m products.  Two of them ride along with launches the other groups make anyway:
-// T = A_k P'_k with the first half's updates (on the update kernel, full m x m tiles),
-// A_{k+1} = T P'_k with the second half's Gram matrices (symmetric tiles).  Q =
-// P'_{k+1} P'_k has a launch of its own on the update kernel: it is symmetric only in
-// exact arithmetic (the computed P' and P'' commute up to rounding), and storing its
-// upper triangle mirrored measurably raised the error of the output, where the full
-// product keeps it at the standard form's level.  A single iteration left at the end
-// runs in the standard form.
+// T = A_k P'_k with the first half's updates (on the update kernel, the m x m tiles on or
+// above the diagonal: T is symmetric, its computed asymmetry is at the level of P''s
+// rounding, and it is read as its upper block triangle like A and P'), A_{k+1} = T P'_k
+// with the second half's Gram matrices (symmetric tiles).  Q = P'_{k+1} P'_k has a launch
+// of its own on the update kernel: it is symmetric only in exact arithmetic (the computed
+// P' and P'' commute up to the error of A_{k+1}), and storing its upper triangle mirrored
+// measurably raised the error of the output, where the full product keeps it at the
+// standard form's level.  A single iteration left at the end runs in the standard form.
 enum GroupOp { OP_NONE, OP_GRAM, OP_POLY, OP_POLY_B, OP_PLAIN_A, OP_PROD_Q, OP_UPD, OP_UPD_T, OP_UPD_Q };
 enum Phase { PH_GRAM, PH_POLY, PH_PLAIN, PH_UPDATE, PH_COUNT };
 
@@ -695,8 +698,10 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 const bool gs = h->groups[ch.gi[sl]].gs != 0;
                 return which == 0 || (which == 1 && !gs) || (which == 2 && gs);
             };
-            // square: the Gram-pair groups' tiles cover their m x m products (T = A P')
-            auto upd_list = [&](int which, bool square, int32_t& o, int32_t& n) {
+            // square: the Gram-pair groups' tiles cover their m x m products; upper: only the
+            // blocks on or above the diagonal of those (T = A P', symmetric, is stored as its
+            // upper block triangle; Q is a full product)
+            auto upd_list = [&](int which, bool square, bool upper, int32_t& o, int32_t& n) {
                 std::vector<T> pr;
                 for (int sl = 0; sl < ch.ng; ++sl) {
                     if (!member(sl, which)) continue;
@@ -704,7 +709,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                     const int cols = square && g.gs ? g.m : g.n;
                     for (int idx = 0; idx < g.count; ++idx)
                         for (int ti = 0; ti < g.m / 256; ++ti)
-                            for (int tj = 0; tj < cols / 256; ++tj)
+                            for (int tj = (upper && square && g.gs) ? ti : 0; tj < cols / 256; ++tj)
                                 pr.push_back({make_int4(sl, idx, ti, tj), (int64_t)g.m});
                 }
                 emit(pr, o, n);
@@ -721,13 +726,13 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 }
                 emit(sg, o, n);
             };
-            upd_list(0, false, ch.pair_off, ch.pair_n);
+            upd_list(0, false, false, ch.pair_off, ch.pair_n);
             sym_list(0, ch.spg_off, ch.spg_n);
             bool any_gs = false;
             for (int sl = 0; sl < ch.ng; ++sl) any_gs = any_gs || member(sl, 2);
             if (any_gs) {
-                upd_list(0, true, ch.pair_t_off, ch.pair_t_n);
-                upd_list(2, true, ch.pair_q_off, ch.pair_q_n);
+                upd_list(0, true, true, ch.pair_t_off, ch.pair_t_n);
+                upd_list(2, true, false, ch.pair_q_off, ch.pair_q_n);
                 // Q's launch and the update launch after it hold tiles of one size when every
                 // group has the same m; then move s standard update tiles, the fewest that
                 // minimise the two launches' waves over the SM pairs
@@ -848,6 +853,7 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
              encode_bf16_3d(enc, &g.map_p_mn128, g.p16, g.m, g.m, g.count, g.lda, 128);
         if (ok && g.gs)
             ok = encode_bf16_3d(enc, &g.map_a_mn128, g.a16, g.m, g.m, g.count, g.lda, 128) &&
+                 encode_bf16_3d(enc, &g.map_t_mn, g.t16, g.m, g.m, g.count, g.lda, 64) &&
                  encode_bf16_3d(enc, &g.map_pb_mn128, g.pb16, g.m, g.m, g.count, g.lda, 128) &&
                  encode_bf16_3d(enc, &g.map_pb_k, g.pb16, g.m, g.m, g.count, g.lda, kBM) &&
                  encode_bf16_3d(enc, &g.map_t_k, g.t16, g.m, g.m, g.count, g.lda, kBM) &&
@@ -943,8 +949,12 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                 case OP_POLY:
                 case OP_POLY_B: fl = m * m * (m + 1); by = 2 * m * m + sym_out; break;
                 case OP_PLAIN_A: fl = m * m * (m + 1); by = 4 * m * m + sym_out; break;
+                // on the update kernel: Q as a full product, T (symmetric) as its upper block triangle
                 case OP_UPD_T:
-                case OP_PROD_Q: fl = 2 * m * m * m; by = 6 * m * m; break;  // the update kernel's full tiles
+                    fl = pairs ? 2 * m * m * m * (nb + 1) / (2 * nb) : 2 * m * m * m;
+                    by = 4 * m * m + sym_out;
+                    break;
+                case OP_PROD_Q: fl = 2 * m * m * m; by = 6 * m * m; break;
                 case OP_UPD: fl = 2 * m * m * n; by = 2 * m * m + (first ? 6 : 4) * m * n; break;
                 case OP_UPD_Q: fl = 2 * m * m * n; by = 2 * m * m + 4 * m * n; break;
                 default: break;
@@ -1048,7 +1058,9 @@ int muon_create(const muon_shape* shapes, int32_t n_mats, const muon_config* cfg
                                 G.out16 = g.a16;
                                 G.opl16 = g.t16;
                                 G.opr16 = g.p16;
-                                G.sym_r = 1;  // P' as its upper block triangle (T is a full product)
+                                // T and P' as their upper block triangles
+                                G.sym_l = G.sym_r = 1;
+                                gp.map_al[sl] = g.map_t_mn;
                                 gp.map_bk[sl] = g.map_p_k;
                                 break;
                             case OP_PROD_Q:  // Q = P'' P', full m x m tiles on the update kernel (into T's buffer)

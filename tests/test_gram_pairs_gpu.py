@@ -78,10 +78,10 @@ def test_gram_pairs_launch_plan():
     assert ws["update"][0] == 5 * (2 * m * m * n + 2 * m * m * m)
     # Gram pairs (five iterations: one plain, two pairs): the wide matrix forms three Gram
     # matrices and three updates; per pair A <- T P' runs in a Gram launch (symmetric, m^2(m+1)),
-    # T = A P' in an update launch (full tiles, 2 m^3) and Q = P'' P' in a launch of its own
-    # (full tiles on the update kernel)
+    # T = A P' in an update launch (its 256 x 256 blocks on or above the diagonal: 6 of 9) and
+    # Q = P'' P' in a launch of its own (full tiles on the update kernel)
     assert wg["gram"][0] == 3 * m * (m + 1) * n + 5 * m * (m + 1) * m + 2 * m * m * (m + 1)
-    assert wg["update"][0] == 3 * 2 * m * m * n + 5 * 2 * m * m * m + 2 * 2 * m * m * m
+    assert wg["update"][0] == 3 * 2 * m * m * n + 5 * 2 * m * m * m + 2 * 2 * m * m * m * 6 // 9
     assert wg["product"][0] == 2 * 2 * m * m * m  # Q as a full product (update kernel)
     assert wg["poly"][0] == ws["poly"][0]
     # the square matrix keeps its Gram and update launches in every iteration, so the pairs
@@ -115,7 +115,7 @@ def test_q_launch_takes_standard_tiles_to_fill_its_last_wave():
     q_fl = 2 * 24 * 2 * m ** 3                # two Q launches, full m x m products
     tile_fl = 2 * m * m * m / 9               # one 256 x 256 tile of a square matrix's update
     assert w["product"][0] == pytest.approx(q_fl + 2 * best * tile_fl, rel=1e-9)
-    upd_all = 48 * 5 * 2 * m ** 3 + 24 * (3 * 2 * m * m * 3072 + 2 * 2 * m ** 3)
+    upd_all = 48 * 5 * 2 * m ** 3 + 24 * (3 * 2 * m * m * 3072 + 2 * 2 * m ** 3 * 6 // 9)
     assert w["update"][0] + w["product"][0] == pytest.approx(upd_all + q_fl, rel=1e-9)
     assert w["product"][2] == 2
     gp.close()
