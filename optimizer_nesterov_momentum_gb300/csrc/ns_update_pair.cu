@@ -13,6 +13,14 @@
 // tile stages 48 KB for: the update's mainloop is bound by how fast shared
 // memory fills, so this is 1.5x the math per staged byte.
 //
+// The same kernel computes the Gram pairs' m x m products T = A P' and
+// Q = P'' P'.  A symmetric operand (P', A, P'') is stored as its upper block
+// triangle (GemmGroup.sym_l / sym_r): a left-operand k-block left of the
+// diagonal comes from the mirror block as MN-major boxes, a right-operand
+// k-block below it as K-major boxes, and the MMA's instruction descriptor
+// takes the matching major-ness per k-block.  The producer runs one copy loop
+// per layout run of a tile (at most three).
+//
 // Warp roles (320 threads per CTA, one CTA per SM):
 //   warp 0     TMA producer (both CTAs): loads its own halves into its own
 //              stage ring; every copy signals CTA 0's "full" mbarrier, which
