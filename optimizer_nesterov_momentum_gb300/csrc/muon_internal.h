@@ -139,7 +139,7 @@ struct GemmParams {
     CUtensorMap map_ein[kMaxGroupsPerLaunch];   // epilogue input: poly A tile, first update hi half of u
     CUtensorMap map_ein2[kMaxGroupsPerLaunch];  // epilogue input: first update lo half of u
     CUtensorMap map_out[kMaxGroupsPerLaunch];   // gram/poly: A / P tile; update: X' tile
-    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // gram/poly: mirrored tile
+    CUtensorMap map_out2[kMaxGroupsPerLaunch];  // one-SM gram/poly: mirrored tile (the SM-pair kernels store none)
     CUtensorMap map_al[kMaxGroupsPerLaunch];    // sym_l: the left operand's MN-major boxes (64 columns)
     CUtensorMap map_bk[kMaxGroupsPerLaunch];    // sym_r: the right operand's K-major boxes (128 rows x 64)
     GemmGroup grp[kMaxGroupsPerLaunch];

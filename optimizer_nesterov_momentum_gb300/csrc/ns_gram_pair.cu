@@ -60,7 +60,7 @@ constexpr int kSymStage = 2 * kSymRows;  // left half | right half
 constexpr int kBlk = 32 * 32 * 2;        // one 32 x 32 16-bit block (64-byte rows, 64-byte swizzle)
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kNoTmem = 0xFFFFFFFFu;
-constexpr int kOutSlots = 2;  // per warp: blocks and mirrors in flight
+constexpr int kOutSlots = 2;  // per warp: output blocks in flight
 
 template <int MODE>
 struct SymPairCfg {
