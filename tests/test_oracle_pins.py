@@ -154,6 +154,32 @@ def test_gram_pairs_equal_the_iteration(steps):
         assert _rel(_gram_pairs_fp64(x, coeffs), ref) < 1e-11
 
 
+def test_gram_pair_products_are_symmetric_in_exact_arithmetic():
+    # T = A_k P_k and Q = P_{k+1} P_k are symmetric: P_k is a polynomial in A_k, so it commutes
+    # with A_k, and A_{k+1} = T P_k is a polynomial in A_k too, so P_{k+1} commutes with P_k.
+    # This is what allows a symmetric product to be stored as one triangle; a product of two
+    # symmetric matrices that do not commute is not symmetric (the last check).
+    rng = np.random.default_rng(11)
+    x = _rand_with_spectrum(rng, 20, 64, np.geomspace(1e-3, 1.0, 20))
+    x /= np.linalg.norm(x)
+    a, b, c = oracle.NS_COEFFS
+    m = x.shape[0]
+
+    def poly(A):
+        return a * np.eye(m) + b * A + c * (A @ A)
+
+    A = x @ x.T
+    P = poly(A)
+    T = A @ P
+    A2 = T @ P
+    Q = poly(A2) @ P
+    for M in (T, A2, Q):
+        assert _rel(M, M.T) < 1e-13
+    S = rng.standard_normal((m, m))
+    S = S + S.T
+    assert _rel(S @ P, (S @ P).T) > 1e-2
+
+
 def test_gram_pairs_identity_catches_a_wrong_order():
     # The pin above is not vacuous: pairing the polynomials in the other order
     # (P_k P_{k+1} built from A_k alone) differs from the iteration.
